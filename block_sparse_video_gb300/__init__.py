@@ -1,0 +1,252 @@
+"""GB300-native video sparse attention (VSA) forward.
+
+Thin Python binding over the C ABI in ``include/vsa.h`` (``libvsa.so``, built
+in-tree by ``block_sparse_video_gb300.build``). The functions keep the C names
+and only marshal arguments: torch tensors are used for device memory and
+streams; every step of the computation runs in the library's CUDA kernels.
+If the library has not been built, importing the binding raises: there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libvsa.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "vsa.h")
+
+VSA_OK = 0
+VSA_ERR_INVALID_ARG = 1
+VSA_ERR_UNSUPPORTED = 2
+VSA_ERR_CUDA = 3
+VSA_ERR_DEVICE_TIMEOUT = 4
+VSA_ERR_INTERNAL = 5
+
+
+class VsaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {vsa_status_string(status)} (status {status})")
+
+
+class vsa_shape_t(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("len_text", ctypes.c_int64),
+        ("len_audio", ctypes.c_int64),
+        ("len_video", ctypes.c_int64),
+        ("keep_fraction", ctypes.c_double),
+    ]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libvsa.so (once). Raises if it is missing: build it first."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run block_sparse_video_gb300.build.build() "
+                           "(or __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    sig = {
+        "vsa_plan_create": (i32, [ctypes.POINTER(vsa_shape_t), ctypes.c_int, ctypes.POINTER(vp)]),
+        "vsa_plan_info": (i32, [vp, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(sz)]),
+        "vsa_forward": (i32, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "vsa_plan_host_path_bytes": (i32, [vp, ctypes.POINTER(sz)]),
+        "vsa_forward_host": (i32, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "vsa_debug_views": (i32, [vp, vp] + [ctypes.POINTER(vp)] * 5),
+        "vsa_check": (i32, [vp, vp, vp]),
+        "vsa_plan_set_stage_events": (i32, [vp, ctypes.POINTER(vp)]),
+        "vsa_plan_destroy": (None, [vp]),
+        "vsa_status_string": (ctypes.c_char_p, [i32]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def header_functions(path: str = HEADER_PATH):
+    """Names of the functions include/vsa.h declares."""
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vsa_[a-z_]+)\s*\(", text)))
+
+
+def vsa_status_string(status: int) -> str:
+    return load_library().vsa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != VSA_OK:
+        raise VsaError(status, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def vsa_plan_create(batch, num_heads, len_text, len_audio, len_video, keep_fraction,
+                    head_dim=128, device=0):
+    """Returns an opaque plan handle (an int). Host only."""
+    shape = vsa_shape_t(batch, num_heads, head_dim, len_text, len_audio, len_video, keep_fraction)
+    out = ctypes.c_void_p()
+    _check(load_library().vsa_plan_create(ctypes.byref(shape), int(device), ctypes.byref(out)),
+           "vsa_plan_create")
+    return out.value
+
+
+def vsa_plan_info(plan):
+    """(n_tiles T, kept tiles k, workspace bytes)."""
+    t, k, ws = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_size_t()
+    _check(load_library().vsa_plan_info(plan, ctypes.byref(t), ctypes.byref(k), ctypes.byref(ws)),
+           "vsa_plan_info")
+    return t.value, k.value, ws.value
+
+
+def vsa_plan_host_path_bytes(plan):
+    n = ctypes.c_size_t()
+    _check(load_library().vsa_plan_host_path_bytes(plan, ctypes.byref(n)), "vsa_plan_host_path_bytes")
+    return n.value
+
+
+def vsa_plan_destroy(plan):
+    if plan:
+        load_library().vsa_plan_destroy(plan)
+
+
+def _check_tensor(x, name, shape, device=None):
+    if x.dtype != torch.bfloat16 or tuple(x.shape) != tuple(shape) or not x.is_contiguous():
+        raise ValueError(f"{name}: expected contiguous bf16 {tuple(shape)}, got {x.dtype} {tuple(x.shape)}")
+    if device is not None and x.device != device:
+        raise ValueError(f"{name}: expected a tensor on {device}, got {x.device}")
+
+
+def vsa_forward(plan, q, k, v, gate, out, workspace, stream=None):
+    """Enqueue the forward on ``stream`` (default: torch's current stream)."""
+    _check(load_library().vsa_forward(plan, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out),
+                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream_handle(stream)), "vsa_forward")
+
+
+def vsa_forward_host(plan, q, k, v, gate, out, device_buffer, stream=None):
+    """Forward on host (ideally pinned) tensors; blocks until ``out`` is filled."""
+    _check(load_library().vsa_forward_host(plan, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out),
+                                           _ptr(device_buffer),
+                                           device_buffer.numel() * device_buffer.element_size(),
+                                           _stream_handle(stream)), "vsa_forward_host")
+
+
+def vsa_check(plan, workspace, stream=None):
+    """Synchronise and raise VsaError if a bounded wait inside a kernel gave up."""
+    _check(load_library().vsa_check(plan, _ptr(workspace), _stream_handle(stream)), "vsa_check")
+
+
+def vsa_plan_set_stage_events(plan, events):
+    """events: four torch.cuda.Event (created with enable_timing=True), or None."""
+    if events is None:
+        _check(load_library().vsa_plan_set_stage_events(plan, None), "vsa_plan_set_stage_events")
+        return
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event on its first record
+            e.record()
+    arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(load_library().vsa_plan_set_stage_events(plan, arr), "vsa_plan_set_stage_events")
+
+
+def vsa_debug_views(plan, workspace, batch, num_heads):
+    """Torch views of the intermediates in ``workspace``: pooled q/k/v and coarse
+    (fp32 [B, H, T, 128]) and the tile selection (int32 [B, H, T, k])."""
+    ptrs = [ctypes.c_void_p() for _ in range(5)]
+    _check(load_library().vsa_debug_views(plan, _ptr(workspace), *[ctypes.byref(p) for p in ptrs]),
+           "vsa_debug_views")
+    t, k, _ = vsa_plan_info(plan)
+    base = workspace.data_ptr()
+    flat = workspace.view(torch.uint8)
+
+    def view(ptr, n_elem, dtype, shape):
+        off = ptr.value - base
+        nbytes = n_elem * torch.tensor([], dtype=dtype).element_size()
+        return flat[off:off + nbytes].view(dtype).view(*shape)
+
+    pooled = batch * num_heads * t * 128
+    return dict(
+        pooled_q=view(ptrs[0], pooled, torch.float32, (batch, num_heads, t, 128)),
+        pooled_k=view(ptrs[1], pooled, torch.float32, (batch, num_heads, t, 128)),
+        pooled_v=view(ptrs[2], pooled, torch.float32, (batch, num_heads, t, 128)),
+        tile_index=view(ptrs[3], batch * num_heads * t * k, torch.int32, (batch, num_heads, t, k)),
+        coarse=view(ptrs[4], pooled, torch.float32, (batch, num_heads, t, 128)),
+    )
+
+
+class VSA:
+    """Convenience owner of a plan and its workspace on one device."""
+
+    def __init__(self, batch, num_heads, len_text, len_audio, len_video, keep_fraction=0.2,
+                 device="cuda"):
+        self.device = torch.device(device)
+        if self.device.type != "cuda":
+            raise ValueError("the VSA forward runs on a CUDA device only")
+        idx = self.device.index if self.device.index is not None else torch.cuda.current_device()
+        self.device = torch.device("cuda", idx)
+        self.batch, self.num_heads = batch, num_heads
+        self.len_text, self.len_audio, self.len_video = len_text, len_audio, len_video
+        self.seq = len_text + len_audio + len_video
+        self.plan = vsa_plan_create(batch, num_heads, len_text, len_audio, len_video, keep_fraction,
+                                    device=idx)
+        self.n_tiles, self.k, self.workspace_bytes = vsa_plan_info(self.plan)
+        self.workspace = torch.empty(self.workspace_bytes, dtype=torch.uint8, device=self.device)
+
+    @property
+    def shape(self):
+        return (self.batch, self.seq, self.num_heads, 128)
+
+    def forward(self, q, k, v, gate, out=None, stream=None):
+        for name, x in (("q", q), ("k", k), ("v", v), ("gate", gate)):
+            _check_tensor(x, name, self.shape, self.device)
+        if out is None:
+            out = torch.empty(self.shape, dtype=torch.bfloat16, device=self.device)
+        _check_tensor(out, "out", self.shape, self.device)
+        vsa_forward(self.plan, q, k, v, gate, out, self.workspace, stream)
+        return out
+
+    __call__ = forward
+
+    def check(self, stream=None):
+        vsa_check(self.plan, self.workspace, stream)
+
+    def debug_views(self):
+        return vsa_debug_views(self.plan, self.workspace, self.batch, self.num_heads)
+
+    def __del__(self):
+        try:
+            vsa_plan_destroy(getattr(self, "plan", None))
+        except Exception:
+            pass
+
+
+__all__ = [
+    "VSA", "VsaError", "load_library", "header_functions", "vsa_plan_create", "vsa_plan_info",
+    "vsa_forward", "vsa_forward_host", "vsa_plan_host_path_bytes", "vsa_debug_views", "vsa_check",
+    "vsa_plan_set_stage_events", "vsa_plan_destroy", "vsa_status_string",
+]

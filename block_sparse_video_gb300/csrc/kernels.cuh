@@ -1,0 +1,52 @@
+// Internal interface between the C-ABI host code and the three kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace vsa {
+
+constexpr int kTile = 64;
+constexpr int kHeadDim = 128;
+
+// Problem geometry shared by the kernels. Token layout is [B, N, H, 128] with
+// the prefix (text then audio, P tokens) first and Lv video tokens after it.
+struct Geometry {
+  int B = 0, H = 0;
+  int P = 0;   // prefix tokens (text + audio)
+  int Lv = 0;  // video tokens
+  int N = 0;   // P + Lv
+  int T = 0;   // video tiles, ceil(Lv / 64)
+  int TP = 0;  // prefix tiles, ceil(P / 64)
+  int k = 0;   // kept video tiles per video query tile
+};
+
+// Tile pool: mean over the valid tokens of each video tile of q, k and v.
+// pooled_* are fp32 [B, H, T, 128].
+cudaError_t launch_pool(const Geometry& g, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                        const __nv_bfloat16* v, float* pooled_q, float* pooled_k,
+                        float* pooled_v, cudaStream_t stream);
+
+// Coarse attention over pooled tiles fused with the top-k tile selection.
+// coarse fp32 [B, H, T, 128]; tile_index int32 [B, H, T, k] ascending.
+size_t coarse_smem_bytes(const Geometry& g, int* rows_per_cta);
+cudaError_t launch_coarse_topk(const Geometry& g, const float* pooled_q, const float* pooled_k,
+                               const float* pooled_v, float* coarse, int32_t* tile_index,
+                               cudaStream_t stream);
+
+// Fine attention: prefix query tiles over every key, video query tiles over
+// the prefix plus their selected video tiles; epilogue adds sigmoid(gate) *
+// coarse on video rows and writes bf16 out.
+struct FineArgs {
+  const __nv_bfloat16* gate;
+  __nv_bfloat16* out;
+  const float* coarse;
+  const int32_t* tile_index;
+  unsigned int* err;  // 3 error words in the workspace
+};
+size_t fine_smem_bytes();
+cudaError_t launch_fine(const Geometry& g, const CUtensorMap& map_q, const CUtensorMap& map_k,
+                        const CUtensorMap& map_v, const FineArgs& a, cudaStream_t stream);
+
+}  // namespace vsa

@@ -1,0 +1,289 @@
+// Host side of the C ABI declared in include/vsa.h: shape validation, the
+// plan, the workspace layout, tensor-map encoding and the kernel launches.
+// The plan is host memory only; every device buffer belongs to the caller.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "kernels.cuh"
+#include "vsa.h"
+
+struct vsa_plan {
+  vsa_shape_t shape;
+  int device;
+  vsa::Geometry g;
+  size_t off_err, off_pq, off_pk, off_pv, off_coarse, off_idx, ws_bytes;
+  size_t tensor_bytes;  // one bf16 [B, N, H, 128] tensor
+  cudaEvent_t events[4];
+  bool have_events;
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int64_t kMaxTokens = int64_t(1) << 26;  // keeps token rows and TMA coordinates in int32
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// Tensor map over a bf16 [B, N, H, 128] tensor; one box = 64 channels x 64
+// tokens of one (batch, head), 128-byte swizzled (the tcgen05 operand layout).
+// Out-of-range token rows read as zeros.
+bool encode_bnhd(CUtensorMap* map, const void* ptr, const vsa::Geometry& g) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(vsa::kHeadDim), static_cast<cuuint64_t>(g.H),
+                              static_cast<cuuint64_t>(g.N), static_cast<cuuint64_t>(g.B)};
+  const cuuint64_t row = static_cast<cuuint64_t>(vsa::kHeadDim) * 2;
+  const cuuint64_t strides[3] = {row, row * g.H, row * g.H * static_cast<cuuint64_t>(g.N)};
+  const cuuint32_t box[4] = {64, 1, 64, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+// Selects the plan's device for the duration of a call.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    if (ok && prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+vsa_status_t record(const vsa_plan* p, int i, cudaStream_t s) {
+  if (!p->have_events) return VSA_OK;
+  return cudaEventRecord(p->events[i], s) == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* vsa_status_string(vsa_status_t s) {
+  switch (s) {
+    case VSA_OK: return "ok";
+    case VSA_ERR_INVALID_ARG: return "invalid argument";
+    case VSA_ERR_UNSUPPORTED: return "unsupported shape";
+    case VSA_ERR_CUDA: return "CUDA error";
+    case VSA_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel timed out";
+    case VSA_ERR_INTERNAL: return "internal error";
+  }
+  return "unknown status";
+}
+
+vsa_status_t vsa_plan_create(const vsa_shape_t* shape, int device, vsa_plan_t* out) {
+  if (!shape || !out) return VSA_ERR_INVALID_ARG;
+  *out = nullptr;
+  const vsa_shape_t s = *shape;
+  if (s.batch < 1 || s.num_heads < 1 || s.len_text < 0 || s.len_audio < 0 || s.len_video < 1 ||
+      device < 0)
+    return VSA_ERR_INVALID_ARG;
+  if (!(std::isfinite(s.keep_fraction) && s.keep_fraction > 0.0 && s.keep_fraction <= 1.0))
+    return VSA_ERR_INVALID_ARG;
+  if (s.head_dim != vsa::kHeadDim) return VSA_ERR_UNSUPPORTED;
+  const int64_t prefix = s.len_text + s.len_audio;
+  const int64_t n = prefix + s.len_video;
+  if (n > kMaxTokens || s.num_heads > 1024 || s.batch > 65535) return VSA_ERR_UNSUPPORTED;
+
+  vsa::Geometry g;
+  g.B = s.batch;
+  g.H = s.num_heads;
+  g.P = static_cast<int>(prefix);
+  g.Lv = static_cast<int>(s.len_video);
+  g.N = static_cast<int>(n);
+  g.T = static_cast<int>((s.len_video + vsa::kTile - 1) / vsa::kTile);
+  g.TP = static_cast<int>((prefix + vsa::kTile - 1) / vsa::kTile);
+  // "rounded to a whole number of tiles": round half up, in IEEE double, clamped to [1, T]
+  int64_t k = static_cast<int64_t>(std::floor(s.keep_fraction * static_cast<double>(g.T) + 0.5));
+  if (k < 1) k = 1;
+  if (k > g.T) k = g.T;
+  g.k = static_cast<int>(k);
+  if (static_cast<int64_t>(g.B) * g.H > 65535) return VSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(g.B) * g.H * (g.TP + g.T) >= (int64_t(1) << 31)) return VSA_ERR_UNSUPPORTED;
+  int rows = 0;
+  if (vsa::coarse_smem_bytes(g, &rows) == 0) return VSA_ERR_UNSUPPORTED;  // T too large
+
+  vsa_plan* p = new (std::nothrow) vsa_plan;
+  if (!p) return VSA_ERR_INTERNAL;
+  std::memset(p, 0, sizeof(*p));
+  p->shape = s;
+  p->device = device;
+  p->g = g;
+  const size_t pooled = static_cast<size_t>(g.B) * g.H * g.T * vsa::kHeadDim * sizeof(float);
+  const size_t idx = static_cast<size_t>(g.B) * g.H * g.T * g.k * sizeof(int32_t);
+  size_t off = 0;
+  p->off_err = off;  off += kAlign;
+  p->off_pq = off;   off += align_up(pooled);
+  p->off_pk = off;   off += align_up(pooled);
+  p->off_pv = off;   off += align_up(pooled);
+  p->off_coarse = off; off += align_up(pooled);
+  p->off_idx = off;  off += align_up(idx);
+  p->ws_bytes = off;
+  p->tensor_bytes = static_cast<size_t>(g.B) * g.N * g.H * vsa::kHeadDim * 2;
+  *out = p;
+  return VSA_OK;
+}
+
+vsa_status_t vsa_plan_info(vsa_plan_t plan, int64_t* n_tiles, int64_t* k, size_t* workspace_bytes) {
+  if (!plan) return VSA_ERR_INVALID_ARG;
+  if (n_tiles) *n_tiles = plan->g.T;
+  if (k) *k = plan->g.k;
+  if (workspace_bytes) *workspace_bytes = plan->ws_bytes;
+  return VSA_OK;
+}
+
+vsa_status_t vsa_plan_set_stage_events(vsa_plan_t plan, void* const* events) {
+  if (!plan) return VSA_ERR_INVALID_ARG;
+  if (!events) {
+    plan->have_events = false;
+    return VSA_OK;
+  }
+  for (int i = 0; i < 4; ++i) {
+    if (!events[i]) return VSA_ERR_INVALID_ARG;
+    plan->events[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  plan->have_events = true;
+  return VSA_OK;
+}
+
+vsa_status_t vsa_forward(vsa_plan_t plan, const void* q, const void* k, const void* v,
+                         const void* gate, void* out, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  if (!plan || !q || !k || !v || !gate || !out || !workspace) return VSA_ERR_INVALID_ARG;
+  if (workspace_bytes < plan->ws_bytes || !aligned(workspace, kAlign)) return VSA_ERR_INVALID_ARG;
+  const void* ins[4] = {q, k, v, gate};
+  const size_t tb = plan->tensor_bytes;
+  for (const void* x : ins) {
+    if (!aligned(x, 16)) return VSA_ERR_INVALID_ARG;
+    if (overlaps(x, tb, out, tb)) return VSA_ERR_INVALID_ARG;
+    if (overlaps(x, tb, workspace, plan->ws_bytes)) return VSA_ERR_INVALID_ARG;
+  }
+  if (!aligned(out, 16) || overlaps(out, tb, workspace, plan->ws_bytes)) return VSA_ERR_INVALID_ARG;
+
+  DeviceGuard guard(plan->device);
+  if (!guard.ok) return VSA_ERR_CUDA;
+  const vsa::Geometry& g = plan->g;
+  CUtensorMap mq, mk, mv;
+  if (!encode_bnhd(&mq, q, g) || !encode_bnhd(&mk, k, g) || !encode_bnhd(&mv, v, g))
+    return VSA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  unsigned int* err = reinterpret_cast<unsigned int*>(ws + plan->off_err);
+  float* pq = reinterpret_cast<float*>(ws + plan->off_pq);
+  float* pk = reinterpret_cast<float*>(ws + plan->off_pk);
+  float* pv = reinterpret_cast<float*>(ws + plan->off_pv);
+  float* coarse = reinterpret_cast<float*>(ws + plan->off_coarse);
+  int32_t* idx = reinterpret_cast<int32_t*>(ws + plan->off_idx);
+
+  if (cudaMemsetAsync(err, 0, 16, st) != cudaSuccess) return VSA_ERR_CUDA;
+  vsa_status_t rs = record(plan, 0, st);
+  if (rs != VSA_OK) return rs;
+  if (vsa::launch_pool(g, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+                       static_cast<const __nv_bfloat16*>(v), pq, pk, pv, st) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  if ((rs = record(plan, 1, st)) != VSA_OK) return rs;
+  if (vsa::launch_coarse_topk(g, pq, pk, pv, coarse, idx, st) != cudaSuccess) return VSA_ERR_CUDA;
+  if ((rs = record(plan, 2, st)) != VSA_OK) return rs;
+  vsa::FineArgs a;
+  a.gate = static_cast<const __nv_bfloat16*>(gate);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.coarse = coarse;
+  a.tile_index = idx;
+  a.err = err;
+  if (vsa::launch_fine(g, mq, mk, mv, a, st) != cudaSuccess) return VSA_ERR_CUDA;
+  return record(plan, 3, st);
+}
+
+vsa_status_t vsa_plan_host_path_bytes(vsa_plan_t plan, size_t* bytes) {
+  if (!plan || !bytes) return VSA_ERR_INVALID_ARG;
+  *bytes = 5 * align_up(plan->tensor_bytes) + plan->ws_bytes;
+  return VSA_OK;
+}
+
+vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, const void* v,
+                              const void* gate, void* out, void* device_buffer,
+                              size_t device_buffer_bytes, void* stream) {
+  if (!plan || !q || !k || !v || !gate || !out || !device_buffer) return VSA_ERR_INVALID_ARG;
+  size_t need = 0;
+  vsa_plan_host_path_bytes(plan, &need);
+  if (device_buffer_bytes < need || !aligned(device_buffer, kAlign)) return VSA_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->device);
+  if (!guard.ok) return VSA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t tb = plan->tensor_bytes, slot = align_up(tb);
+  uint8_t* d = static_cast<uint8_t*>(device_buffer);
+  const void* hin[4] = {q, k, v, gate};
+  for (int i = 0; i < 4; ++i)
+    if (cudaMemcpyAsync(d + i * slot, hin[i], tb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return VSA_ERR_CUDA;
+  vsa_status_t s = vsa_forward(plan, d, d + slot, d + 2 * slot, d + 3 * slot, d + 4 * slot,
+                               d + 5 * slot, plan->ws_bytes, stream);
+  if (s != VSA_OK) return s;
+  if (cudaMemcpyAsync(out, d + 4 * slot, tb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return VSA_ERR_CUDA;
+  return VSA_OK;
+}
+
+vsa_status_t vsa_debug_views(vsa_plan_t plan, void* workspace, const float** pooled_q,
+                             const float** pooled_k, const float** pooled_v,
+                             const int32_t** tile_index, const float** coarse) {
+  if (!plan || !workspace) return VSA_ERR_INVALID_ARG;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  if (pooled_q) *pooled_q = reinterpret_cast<const float*>(ws + plan->off_pq);
+  if (pooled_k) *pooled_k = reinterpret_cast<const float*>(ws + plan->off_pk);
+  if (pooled_v) *pooled_v = reinterpret_cast<const float*>(ws + plan->off_pv);
+  if (tile_index) *tile_index = reinterpret_cast<const int32_t*>(ws + plan->off_idx);
+  if (coarse) *coarse = reinterpret_cast<const float*>(ws + plan->off_coarse);
+  return VSA_OK;
+}
+
+vsa_status_t vsa_check(vsa_plan_t plan, void* workspace, void* stream) {
+  if (!plan || !workspace) return VSA_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->device);
+  if (!guard.ok) return VSA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return VSA_ERR_CUDA;
+  unsigned int words[3] = {0, 0, 0};
+  if (cudaMemcpy(words, static_cast<uint8_t*>(workspace) + plan->off_err, sizeof(words),
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  if (words[0] == 0) return VSA_OK;
+  if (words[0] == static_cast<unsigned int>(VSA_ERR_DEVICE_TIMEOUT)) return VSA_ERR_DEVICE_TIMEOUT;
+  return VSA_ERR_INTERNAL;
+}
+
+void vsa_plan_destroy(vsa_plan_t plan) { delete plan; }
+
+}  // extern "C"

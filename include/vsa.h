@@ -1,0 +1,143 @@
+/*
+ * vsa.h - C ABI of the GB300 (sm_103a) video sparse attention (VSA) forward.
+ *
+ * The operation is the attention of one joint text+audio+video DiT layer as
+ * "UniServe: serving FastH3 at its fastest" defines it:
+ *   - section "The FastH3 workload": the sequence is processed in tiles of 64
+ *     tokens; text and audio queries attend to every key; video queries attend
+ *     to every text and audio key and to the highest-scoring fraction (20% in
+ *     FastH3) of video key tiles, rounded to a whole number of tiles; a coarse
+ *     branch attends over mean-pooled tiles, and a learned gate adds its
+ *     output to the fine sparse-attention output;
+ *   - section "Fused attention preprocessing": tiles are pooled over their
+ *     valid tokens into FP32 pooled statistics;
+ *   - section "Fused output combination": O_i = O_i^fine + G_i * O^coarse_tile(i);
+ *   - section "Benchmarks / Setup": the top-k video tiles are selected exactly.
+ *
+ * Conventions fixed by this library where the page leaves them open:
+ *   - memory order of the segments is text | audio | video (prefix P = text +
+ *     audio tokens, then Lv video tokens, N = P + Lv); video tokens arrive
+ *     tile-contiguous: video tile j is tokens P + 64j .. P + 64j + n_j - 1,
+ *     T = ceil(Lv / 64) tiles, the last one may be ragged (n_j < 64);
+ *   - tile score s[t][j] = (mean-pooled Q of tile t) . (mean-pooled K of tile
+ *     j) / sqrt(128), computed in fp32; the coarse softmax runs over all T
+ *     video tiles; prefix tokens are not tiles of the coarse branch;
+ *   - k = max(1, min(T, floor(keep_fraction * T + 0.5))) in IEEE double;
+ *     equal scores go to the lower tile index; selections are stored in
+ *     ascending tile order;
+ *   - G = sigmoid(gate) per channel; text/audio rows get no coarse term;
+ *   - softmax scale 1/sqrt(128) in both branches.
+ *
+ * Data layout: q, k, v, gate and out are contiguous bf16 tensors of shape
+ * [batch, N, num_heads, 128] (token-major, heads interleaved: the natural
+ * output of the Q/K/V/gate projections), 16-byte aligned. All device buffers
+ * are owned by the caller; the library owns only the host-side plan.
+ *
+ * Errors: argument errors are returned synchronously and nothing is launched.
+ * CUDA errors at launch come back as VSA_ERR_CUDA. Every wait inside the
+ * kernels is bounded; a wait that runs out records VSA_ERR_DEVICE_TIMEOUT in
+ * the workspace's error words (the kernels then finish early), which
+ * vsa_check() reports. The library never aborts the process.
+ *
+ * Threading: a plan may be used from one host thread at a time. Concurrent
+ * forwards on different streams need different workspaces.
+ */
+#ifndef VSA_H_
+#define VSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  VSA_OK = 0,
+  VSA_ERR_INVALID_ARG = 1,    /* null pointer, bad length, keep fraction outside (0, 1], ... */
+  VSA_ERR_UNSUPPORTED = 2,    /* head_dim other than 128, sizes beyond the supported range */
+  VSA_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed */
+  VSA_ERR_DEVICE_TIMEOUT = 4, /* a bounded wait inside a kernel ran out (reported by vsa_check) */
+  VSA_ERR_INTERNAL = 5
+} vsa_status_t;
+
+/* Problem shape. head_dim must be 128. len_text and len_audio may be 0;
+ * len_video must be >= 1. keep_fraction in (0, 1]. batch, num_heads >= 1. */
+typedef struct {
+  int32_t batch;
+  int32_t num_heads;
+  int32_t head_dim;
+  int64_t len_text;
+  int64_t len_audio;
+  int64_t len_video;
+  double keep_fraction;
+} vsa_shape_t;
+
+typedef struct vsa_plan* vsa_plan_t; /* opaque, host memory, owned by the library */
+
+/* "vsa_plan": validate a shape and precompute T, k, the workspace size and the
+ * launch configuration for `device`. Host only: touches no GPU state and
+ * allocates no device memory, so it may run on a machine without a GPU.
+ * On success *out receives a plan to release with vsa_plan_destroy. */
+vsa_status_t vsa_plan_create(const vsa_shape_t* shape, int device, vsa_plan_t* out);
+
+/* Number of video tiles T, kept tiles per query tile k, and the device
+ * workspace vsa_forward needs, in bytes. Any output pointer may be NULL. */
+vsa_status_t vsa_plan_info(vsa_plan_t plan, int64_t* n_tiles, int64_t* k, size_t* workspace_bytes);
+
+/* The VSA forward: out = fine attention (+ sigmoid(gate) * coarse on video rows).
+ *   q, k, v, gate : device, bf16 [batch, N, num_heads, 128], read only
+ *   out           : device, bf16 [batch, N, num_heads, 128], written; must not
+ *                   alias any input
+ *   workspace     : device, >= workspace_bytes from vsa_plan_info, 256-byte
+ *                   aligned; holds pooled statistics, tile selections, the
+ *                   coarse output and the error words; contents on entry are
+ *                   ignored (the forward clears what must start at zero)
+ *   stream        : cudaStream_t to launch on (NULL = legacy default stream)
+ * Enqueues three kernels (tile pool; coarse attention + top-k; fine attention
+ * with the gated combination fused into its epilogue) and returns without
+ * synchronising. It allocates nothing and reads no device data on the host, so
+ * it can be captured into a CUDA graph. */
+vsa_status_t vsa_forward(vsa_plan_t plan, const void* q, const void* k, const void* v,
+                         const void* gate, void* out, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* Same forward on HOST buffers (q, k, v, gate read, out written, all bf16
+ * [batch, N, num_heads, 128]; pinned memory makes the copies asynchronous).
+ * `device_buffer` (>= host_path_bytes from vsa_plan_host_path_bytes, 256-byte
+ * aligned) receives the inputs, the output and the workspace. Copies in,
+ * runs the forward, copies out, and synchronises `stream` before returning. */
+vsa_status_t vsa_plan_host_path_bytes(vsa_plan_t plan, size_t* bytes);
+vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, const void* v,
+                              const void* gate, void* out, void* device_buffer,
+                              size_t device_buffer_bytes, void* stream);
+
+/* Device pointers to the intermediates a forward leaves in `workspace`:
+ *   pooled_q/k/v : fp32 [batch, num_heads, T, 128] tile means
+ *   tile_index   : int32 [batch, num_heads, T, k] selected video tiles, ascending
+ *   coarse       : fp32 [batch, num_heads, T, 128] coarse-branch output
+ * Any output pointer may be NULL. */
+vsa_status_t vsa_debug_views(vsa_plan_t plan, void* workspace, const float** pooled_q,
+                             const float** pooled_k, const float** pooled_v,
+                             const int32_t** tile_index, const float** coarse);
+
+/* Synchronise `stream` and report the device error words of `workspace`:
+ * VSA_OK, or VSA_ERR_DEVICE_TIMEOUT if a bounded wait gave up. */
+vsa_status_t vsa_check(vsa_plan_t plan, void* workspace, void* stream);
+
+/* Optional per-kernel timing. When `events` is non-NULL, each vsa_forward
+ * records events[0] before the pool kernel, events[1] before the coarse/top-k
+ * kernel, events[2] before the attention kernel and events[3] after it, on
+ * the forward's stream. The four cudaEvent_t handles are owned by the caller;
+ * pass NULL to stop recording. */
+vsa_status_t vsa_plan_set_stage_events(vsa_plan_t plan, void* const* events);
+
+void vsa_plan_destroy(vsa_plan_t plan);
+
+const char* vsa_status_string(vsa_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VSA_H_ */

@@ -1,0 +1,98 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/vsa.h declares, and vsa_plan_create validates shapes on the host."""
+import ctypes
+import os
+
+import pytest
+
+import block_sparse_video_gb300 as bsv
+from block_sparse_video_gb300.synthetic import CONFIGS
+from oracle import vsa_oracle as vo
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(bsv.LIB_PATH):
+        from block_sparse_video_gb300 import build
+        build.build()
+    return bsv.load_library()
+
+
+def test_exports_every_declared_function(lib):
+    names = bsv.header_functions()
+    assert {"vsa_plan_create", "vsa_plan_info", "vsa_forward", "vsa_forward_host", "vsa_check",
+            "vsa_debug_views", "vsa_plan_destroy", "vsa_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def _status(**kw):
+    shape = dict(batch=1, num_heads=2, head_dim=128, len_text=64, len_audio=64, len_video=1024,
+                 keep_fraction=0.2)
+    shape.update(kw)
+    s = bsv.vsa_shape_t(shape["batch"], shape["num_heads"], shape["head_dim"], shape["len_text"],
+                        shape["len_audio"], shape["len_video"], shape["keep_fraction"])
+    out = ctypes.c_void_p()
+    st = bsv.load_library().vsa_plan_create(ctypes.byref(s), 0, ctypes.byref(out))
+    if out.value:
+        bsv.vsa_plan_destroy(out.value)
+    return st
+
+
+def test_plan_validation_status_codes(lib):
+    assert _status() == bsv.VSA_OK
+    assert _status(head_dim=64) == bsv.VSA_ERR_UNSUPPORTED
+    assert _status(len_video=0) == bsv.VSA_ERR_INVALID_ARG
+    assert _status(len_text=-1) == bsv.VSA_ERR_INVALID_ARG
+    assert _status(batch=0) == bsv.VSA_ERR_INVALID_ARG
+    assert _status(num_heads=0) == bsv.VSA_ERR_INVALID_ARG
+    for f in (0.0, -0.1, 1.5, float("nan"), float("inf")):
+        assert _status(keep_fraction=f) == bsv.VSA_ERR_INVALID_ARG, f
+    assert _status(len_video=1 << 30) == bsv.VSA_ERR_UNSUPPORTED
+    assert _status(len_text=0, len_audio=0) == bsv.VSA_OK  # empty prefix is allowed
+    assert _status(len_video=1) == bsv.VSA_OK
+    assert _status(keep_fraction=1.0) == bsv.VSA_OK
+    assert lib.vsa_plan_create(None, 0, None) == bsv.VSA_ERR_INVALID_ARG
+
+
+def test_plan_counts_match_oracle(lib):
+    cases = [(c.len_video, f) for c in CONFIGS.values() for f in c.keep]
+    cases += [(1, 0.2), (64, 0.2), (65, 0.2), (320, 0.5), (640, 0.25), (448, 1.0), (192, 0.01)]
+    for lv, f in cases:
+        plan = bsv.vsa_plan_create(1, 1, 10, 20, lv, f)
+        try:
+            t, k, ws = bsv.vsa_plan_info(plan)
+        finally:
+            bsv.vsa_plan_destroy(plan)
+        assert t == vo.video_tile_count(lv)
+        assert k == vo.keep_count(t, f), (lv, f)
+        assert ws >= 256 + 4 * t * 128 * 4 + t * k * 4
+
+
+def test_forward_rejects_bad_arguments_without_launching(lib):
+    plan = bsv.vsa_plan_create(1, 2, 64, 64, 1024, 0.2)
+    try:
+        _, _, ws = bsv.vsa_plan_info(plan)
+        f = lib.vsa_forward
+        fake = ctypes.c_void_p(1 << 20)
+        assert f(plan, None, fake, fake, fake, fake, fake, ws, None) == bsv.VSA_ERR_INVALID_ARG
+        # workspace too small
+        assert f(plan, fake, fake, fake, fake, fake, fake, ws - 1, None) == bsv.VSA_ERR_INVALID_ARG
+        # misaligned input
+        a = ctypes.c_void_p((1 << 30) + 8)
+        assert f(plan, a, fake, fake, fake, ctypes.c_void_p(1 << 34), ctypes.c_void_p(1 << 36), ws,
+                 None) == bsv.VSA_ERR_INVALID_ARG
+        # out aliasing an input
+        x = ctypes.c_void_p(1 << 30)
+        assert f(plan, x, ctypes.c_void_p(1 << 31), ctypes.c_void_p(1 << 32), ctypes.c_void_p(1 << 33), x,
+                 ctypes.c_void_p(1 << 36), ws, None) == bsv.VSA_ERR_INVALID_ARG
+        assert lib.vsa_check(None, fake, None) == bsv.VSA_ERR_INVALID_ARG
+    finally:
+        bsv.vsa_plan_destroy(plan)
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert bsv.vsa_status_string(s)
+    assert "timed out" in bsv.vsa_status_string(bsv.VSA_ERR_DEVICE_TIMEOUT)

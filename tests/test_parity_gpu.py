@@ -1,0 +1,139 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Small shapes are checked on every head, query tile and prefix row, including
+the degenerate cases (empty prefix, non-64-aligned prefix, ragged last video
+tile, a single video tile, a single video token, k = 1, k = T). The workload
+sizes run in the same launch configuration the benchmark times and are
+checked on every pooled statistic, selection and coarse row of a seeded
+sample of heads and on a seeded sample of output rows.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_video_gb300 as bsv
+from block_sparse_video_gb300.synthetic import CONFIGS, bf16_bits, make_config_inputs, make_inputs
+from oracle import vsa_oracle as vo
+from tests.vsa_parity import assert_errors, compare_head, full_check, run_gpu, to_f64
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    "tiny": (1, 2, 64, 64, 1024, 0.2, 0),
+    "ragged_prefix_and_tail": (2, 3, 37, 50, 1000, 0.3, 5),
+    "no_prefix": (1, 2, 0, 0, 700, 0.25, 6),
+    "single_video_tile": (1, 2, 10, 20, 50, 0.2, 7),
+    "keep_all_is_dense": (1, 2, 40, 60, 640, 1.0, 8),
+    "k_is_one": (1, 2, 64, 0, 2048, 0.01, 9),
+    "one_video_token": (1, 1, 3, 2, 1, 0.2, 10),
+    "text_only_prefix": (1, 4, 130, 0, 4096, 0.2, 11),
+    "odd_tile_count": (1, 3, 64, 64, 64 * 37 + 5, 0.2, 12),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_shapes_full_parity(cuda_ok, name):
+    full_check(*SMALL[name])
+
+
+def test_medium_full_parity(cuda_ok):
+    c = CONFIGS["medium"]
+    full_check(c.batch, c.heads, c.len_text, c.len_audio, c.len_video, c.keep[0], c.seed)
+
+
+def _sampled(q, k, v, g, lt, la, lv, keep, pairs, tiles_per_head, prefix_pairs, seed):
+    _, out, views = run_gpu(q, k, v, g, lt, la, lv, keep)
+    bits = [bf16_bits(x.cpu()) for x in (q, k, v, g)]
+    out_cpu = out.cpu()
+    del out
+    t = vo.video_tile_count(lv)
+    p = lt + la
+    rng = np.random.default_rng(seed)
+    stats = []
+    for (b, h) in pairs:
+        tiles = set(rng.choice(t, size=min(t, tiles_per_head), replace=False).tolist()) | {0, t - 1}
+        if (b, h) in prefix_pairs:
+            prows = np.arange(p)
+        else:
+            prows = np.sort(rng.choice(p, size=min(p, 64), replace=False)) if p else np.arange(0)
+        stats.append(compare_head(*bits, views, lambda bb, hh, rows: out_cpu[bb, rows, hh].double().numpy(),
+                                  b, h, p, lv, keep, video_tiles=sorted(tiles), prefix_rows=prows))
+    return stats
+
+
+def _pairs(batch, heads, n, seed):
+    rng = np.random.default_rng(seed)
+    allp = [(b, h) for b in range(batch) for h in range(heads)]
+    pick = rng.choice(len(allp), size=min(n, len(allp)), replace=False)
+    return [allp[i] for i in sorted(pick)]
+
+
+@pytest.mark.parametrize("name", ["5s", "10s"])
+def test_workload_sampled_parity(cuda_ok, name):
+    c = CONFIGS[name]
+    q, k, v, g = make_config_inputs(c, device="cuda")
+    pairs = _pairs(c.batch, c.heads, 6 if name == "10s" else 4, c.seed)
+    stats = _sampled(q, k, v, g, c.len_text, c.len_audio, c.len_video, c.keep[0], pairs, 24,
+                     set(pairs[:1]), c.seed)
+    del q, k, v, g
+    gc.collect()
+    torch.cuda.empty_cache()
+    assert_errors(stats, name)
+
+
+def test_ragged_sweep_sampled_parity(cuda_ok):
+    c = CONFIGS["ragged"]
+    q, k, v, g = make_config_inputs(c, device="cuda")
+    for i, keep in enumerate(c.keep):
+        pairs = _pairs(c.batch, c.heads, 3, c.seed + i)
+        stats = _sampled(q, k, v, g, c.len_text, c.len_audio, c.len_video, keep, pairs, 16,
+                         set(pairs[:1]) if i == 0 else set(), c.seed + i)
+        assert_errors(stats, f"ragged f={keep}")
+    del q, k, v, g
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def test_long_video_smaller_coarse_tiles(cuda_ok):
+    """T = 1,500 video tiles: the coarse kernel switches to 16 query tiles per CTA."""
+    q, k, v, g = make_inputs(1, 2, 40, 24, 96000, 21, device="cuda")
+    stats = _sampled(q, k, v, g, 40, 24, 96000, 0.2, [(0, 0), (0, 1)], 24, {(0, 1)}, 21)
+    assert_errors(stats, "long video")
+
+
+def test_deterministic(cuda_ok):
+    c = CONFIGS["medium"]
+    q, k, v, g = make_config_inputs(c, device="cuda")
+    op = bsv.VSA(c.batch, c.heads, c.len_text, c.len_audio, c.len_video, c.keep[0])
+    a = op(q, k, v, g).clone()
+    ia = op.debug_views()["tile_index"].clone()
+    b = op(q, k, v, g)
+    op.check()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(ia, op.debug_views()["tile_index"])
+
+
+def test_host_buffer_path_matches_device_path(cuda_ok):
+    q, k, v, g = make_inputs(1, 2, 64, 64, 1024, 0, device="cuda")
+    op = bsv.VSA(1, 2, 64, 64, 1024, 0.2)
+    dev = op(q, k, v, g)
+    op.check()
+    hq, hk, hv, hg = [x.cpu().pin_memory() for x in (q, k, v, g)]
+    hout = torch.empty_like(hq).pin_memory()
+    buf = torch.empty(bsv.vsa_plan_host_path_bytes(op.plan), dtype=torch.uint8, device="cuda")
+    bsv.vsa_forward_host(op.plan, hq, hk, hv, hg, hout, buf)
+    assert torch.equal(hout.view(torch.int16), dev.cpu().view(torch.int16))
+
+
+def test_stage_events_time_each_kernel(cuda_ok):
+    q, k, v, g = make_inputs(1, 2, 64, 64, 1024, 0, device="cuda")
+    op = bsv.VSA(1, 2, 64, 64, 1024, 0.2)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    bsv.vsa_plan_set_stage_events(op.plan, ev)
+    op(q, k, v, g)
+    op.check()
+    bsv.vsa_plan_set_stage_events(op.plan, None)
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
+    assert all(t > 0 for t in times)
