@@ -1,0 +1,414 @@
+#!/usr/bin/env python
+"""Benchmark of the VSA forward at the 10 s FastH3 shape on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one VSA forward of one DiT attention layer (tile pool, coarse
+attention + top-k, fine attention with the gated combination) over the
+workload of "UniServe: serving FastH3 at its fastest", section "The FastH3
+workload": batch 1, 56 heads x 128, text 1,024 + audio 1,024 + video 72,576
+tokens (1,134 tiles, k = 227), bf16, seeded synthetic inputs (no checkpoint).
+
+value = effective TFLOP/s: the FLOPs the sparse pattern requires (fine
+attention over the keys each query attends to, plus the coarse branch),
+divided by the device time of the step, inputs resident in HBM; L2 is flushed
+between timed steps. e2e = the same metric through vsa_forward_host (pinned
+host buffers, host<->device copies inside the timed region).
+
+Under torchrun every rank runs its own full problem (weak scaling, no
+collective in the data path); the step time is the max over ranks.
+--impl reference times the CPU oracle on a bounded sample of the same
+workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from block_sparse_video_gb300.synthetic import CONFIGS, bf16_bits, make_config_inputs, make_inputs  # noqa: E402
+
+METRIC = "VSA fwd ms/layer & effective TFLOP/s (frac of BF16 peak), 10s FastH3 shape"
+UNIT = "TFLOP/s"
+CFG = CONFIGS["10s"]
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def workload_config(cfg=None, keep=None):
+    cfg = CFG if cfg is None else cfg
+    keep = cfg.keep[0] if keep is None else keep
+    t = cfg.n_video_tiles
+    k = max(1, min(t, int(np.floor(keep * t + 0.5))))
+    return {
+        "workload": (f"VSA forward, {cfg.name} shape: B{cfg.batch} H{cfg.heads} D128, text "
+                     f"{cfg.len_text} + audio {cfg.len_audio} + video {cfg.len_video} tokens "
+                     f"({t} tiles of 64, k={k}, keep {keep})"),
+        "batch": cfg.batch, "heads": cfg.heads, "head_dim": 128, "len_text": cfg.len_text,
+        "len_audio": cfg.len_audio, "len_video": cfg.len_video, "video_tiles": t, "kept_tiles": k,
+        "seed": cfg.seed, "l2": "flushed between timed steps (512 MB write); inputs 4.3 GB > L2",
+        "parallelism": "one full problem per GPU (weak scaling)",
+    }
+
+
+def effective_flops(cfg=None, keep=None, tile_index=None):
+    """FLOPs the sparse pattern requires: 4*D per (query, attended key) pair, plus
+    the coarse branch (4*D per pooled query/key tile pair). Keys counted are the
+    valid ones actually attended (a ragged tile counts its valid tokens)."""
+    cfg = CFG if cfg is None else cfg
+    keep = cfg.keep[0] if keep is None else keep
+    d, p, lv = 128, cfg.prefix, cfg.len_video
+    t = cfg.n_video_tiles
+    n_last = lv - 64 * (t - 1)
+    n = np.full(t, 64)
+    n[-1] = n_last
+    k = max(1, min(t, int(np.floor(keep * t + 0.5))))
+    if tile_index is None:
+        assert lv % 64 == 0, "ragged workloads need the selection to count keys"
+        video_pairs = lv * (p + 64 * k) * cfg.batch * cfg.heads
+    else:
+        sel_keys = n[tile_index].sum(axis=-1)  # [B, H, T]
+        video_pairs = int(((p + sel_keys) * n[None, None, :]).sum())
+    prefix_pairs = p * (p + lv) * cfg.batch * cfg.heads
+    fine = 4 * d * (video_pairs + prefix_pairs)
+    coarse = 4 * d * t * t * cfg.batch * cfg.heads
+    return {"fine": float(fine), "coarse": float(coarse), "total": float(fine + coarse)}
+
+
+def pool_bytes(cfg=None):
+    cfg = CFG if cfg is None else cfg
+    return 3 * cfg.batch * cfg.len_video * cfg.heads * 128 * 2 + 3 * cfg.batch * cfg.heads * cfg.n_video_tiles * 128 * 4
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms (read only)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+# ----------------------------------------------------------------- CPU oracle sample
+
+def oracle_sample(n_video_tiles=256, n_prefix_rows=256, seed=None):
+    """Time the CPU oracle on one head of the workload: pooling, tile scores,
+    selection and coarse branch for all tiles, plus fine attention for a seeded
+    sample of video query tiles and prefix rows. Returns (flops, seconds, text)."""
+    from oracle import vsa_oracle as vo
+    cfg = CFG
+    seed = cfg.seed if seed is None else seed
+    q, k, v, g = make_inputs(1, 1, cfg.len_text, cfg.len_audio, cfg.len_video, seed, device="cpu")
+    bits = [bf16_bits(x)[0, :, 0] for x in (q, k, v, g)]
+    t = cfg.n_video_tiles
+    rng = np.random.default_rng(seed)
+    tiles = np.sort(rng.choice(t, size=min(t, n_video_tiles), replace=False))
+    prows = np.sort(rng.choice(cfg.prefix, size=min(cfg.prefix, n_prefix_rows), replace=False))
+    t0 = time.perf_counter()
+    r = vo.vsa_head(*bits, cfg.prefix, cfg.len_video, cfg.keep[0], video_tiles=tiles, prefix_rows=prows)
+    secs = time.perf_counter() - t0
+    kk = r["k"]
+    flops = 4 * 128 * (t * t + len(tiles) * 64 * (cfg.prefix + 64 * kk) + len(prows) * cfg.seq)
+    text = (f"1 of {cfg.heads} heads of the {cfg.name} shape (synthetic, same recipe, own seed): pool, "
+            f"tile scores, top-{kk} selection and coarse branch over all {t} tiles, fine attention "
+            f"for {len(tiles)} sampled video query tiles and {len(prows)} sampled prefix rows; "
+            f"rate = FLOPs of that work / its wall time")
+    return float(flops), secs, text
+
+
+def cpu_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        blas = [i["num_threads"] for i in info if i.get("user_api") == "blas"]
+        if blas:
+            return int(max(blas))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    rates, secs_all = [], []
+    text = ""
+    for step in range(args.warmup + args.steps):
+        flops, secs, text = oracle_sample(n_video_tiles=24, n_prefix_rows=64, seed=CFG.seed + step)
+        if step >= args.warmup:
+            rates.append(flops / secs / 1e12)
+            secs_all.append(secs)
+    value = statistics.mean(rates)
+    cores = cpu_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs_all),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": text},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import block_sparse_video_gb300 as bsv
+
+    world, rank, local = dist_info()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    cfg = CFG
+    keep = cfg.keep[0]
+    peaks, peak_src = read_peaks()
+    bsv.load_library()  # fails loudly if the library is not built
+
+    q, k, v, g = make_inputs(cfg.batch, cfg.heads, cfg.len_text, cfg.len_audio, cfg.len_video,
+                             cfg.seed + rank, device=dev)
+    op = bsv.VSA(cfg.batch, cfg.heads, cfg.len_text, cfg.len_audio, cfg.len_video, keep, device=dev)
+    out = torch.empty_like(q)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fl = effective_flops(cfg, keep)
+
+    for _ in range(args.warmup):
+        op(q, k, v, g, out)
+    op.check()
+
+    steps = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.25)
+    for s in range(steps):
+        flush.zero_()
+        bsv.vsa_plan_set_stage_events(op.plan, ev[s])
+        starts[s].record(stream)
+        op(q, k, v, g, out)
+        ends[s].record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    barrier(world)
+    bsv.vsa_plan_set_stage_events(op.plan, None)
+    op.check()
+
+    step_ms = [starts[s].elapsed_time(ends[s]) for s in range(steps)]
+    stage_ms = [[ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(steps)] for i in range(3)]
+    local_ms = statistics.mean(step_ms)
+    ms = reduce_max(local_ms, world, dev)
+    total_flops = reduce_sum(fl["total"], world, dev)
+    value = total_flops / (ms * 1e-3) / 1e12
+
+    pool_ms, coarse_ms, fine_ms = (statistics.mean(x) for x in stage_ms)
+    fine_tflops = fl["fine"] / (fine_ms * 1e-3) / 1e12
+    sustained = peaks["bf16_tflops_sustained"]
+    burst = peaks["bf16_tflops"]
+    pool_gbs = pool_bytes(cfg) / (pool_ms * 1e-3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "fine_attn_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            with open(tpath) as f:
+                tr = json.load(f)
+            if tr.get("kernel_source_hash") == _source_hash():
+                traffic = tr.get("bytes_per_launch_10s")
+        except Exception:
+            traffic = None
+
+    # ---- end to end through the host-buffer entry point
+    e2e = None
+    if args.e2e_steps > 0:
+        hq, hk, hv, hg = [x.cpu().pin_memory() for x in (q, k, v, g)]
+        hout = torch.empty_like(hq).pin_memory()
+        del out, q, k, v, g
+        torch.cuda.empty_cache()
+        dbuf = torch.empty(bsv.vsa_plan_host_path_bytes(op.plan), dtype=torch.uint8, device=dev)
+        for _ in range(2):
+            bsv.vsa_forward_host(op.plan, hq, hk, hv, hg, hout, dbuf)
+        barrier(world)
+        times = []
+        for _ in range(args.e2e_steps):
+            t0 = time.perf_counter()
+            bsv.vsa_forward_host(op.plan, hq, hk, hv, hg, hout, dbuf)
+            times.append(time.perf_counter() - t0)
+        e2e_s = reduce_max(statistics.mean(times), world, dev)
+        tb = hq.numel() * hq.element_size()
+        e2e = {"value": total_flops / e2e_s / 1e12, "unit": UNIT, "ms_per_step": e2e_s * 1e3,
+               "h2d_bytes_per_step": 4 * tb, "d2h_bytes_per_step": tb,
+               "api": "vsa_forward_host (C ABI), pinned host buffers, synchronous"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        flops, secs, text = oracle_sample()
+        cpu = {"value": flops / secs / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+               "sample": text, "seconds": secs}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; no checkpoint)",
+            "config": workload_config(cfg, keep),
+            "ms_per_layer": ms,
+            "effective_flops_per_step": fl["total"],
+            "frac_of_bf16_peak": {"sustained": value / world / sustained, "burst": value / world / burst,
+                                  "source": peak_src},
+            "roofline": {"bound": "tensor", "kernel": "fine_attn_kernel", "achieved": fine_tflops,
+                         "peak": sustained, "unit": "TFLOP/s", "frac": fine_tflops / sustained,
+                         "traffic": traffic, "peak_kind": f"bf16 dense, sustained ({peak_src})",
+                         "frac_of_burst": fine_tflops / burst,
+                         "algorithmic_flops_per_launch": fl["fine"], "ms_per_launch": fine_ms},
+            "kernels": {
+                "pool_kernel": {"ms": pool_ms, "bytes": pool_bytes(cfg), "GB_s": pool_gbs,
+                                "frac_of_hbm": pool_gbs / peaks["hbm_gbs"]},
+                "coarse_topk_kernel": {"ms": coarse_ms, "flops": fl["coarse"],
+                                       "TFLOP_s": fl["coarse"] / (coarse_ms * 1e-3) / 1e12},
+                "fine_attn_kernel": {"ms": fine_ms, "flops": fl["fine"], "TFLOP_s": fine_tflops},
+            },
+            "clocks": clocks,
+            "e2e": e2e,
+            "gpu_launches": 3 * steps,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def _source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("fine_attn.cu", "ptx.cuh", "kernels.cuh"):
+        with open(os.path.join(ROOT, "block_sparse_video_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["10s", "5s", "medium"], default="10s",
+                    help="10s is the benchmark; the smaller ones serve profiler captures")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    world, _, _ = dist_info()
+    if world != args.gpus and not (world == 1 and args.gpus == 1):
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+    global CFG
+    CFG = CONFIGS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -14,7 +14,7 @@
 //   S^T[128 keys x 64 queries] = K_blk[128 x 128] . Q^T           (A, B K-major)
 //   O^T[128 dims x 64 queries] += V_blk^T[128 x 128 keys] . P^T   (A, B MN-major)
 // S^T and O^T live in tensor memory (TMEM lane = key, resp. head dim; column =
-// query). Each softmax thread owns one key lane for 32 query columns, so
+// query). Each softmax thread owns one key lane for 16 query columns, so
 // masking a ragged or absent key tile is a per-thread select. The online
 // softmax keeps, per query column, a reference m (log2 units) shared by every
 // lane; a block whose scores all stay below m + 8 (P <= 256) needs no cross-
@@ -22,34 +22,47 @@
 // exact block maximum across the 128 lanes, raises m, and rescales the row
 // sums and O^T. Row sums are per-lane partials, reduced once at the end.
 //
-// Warp roles (320 threads): warp 0 issues TMA loads (Q once; K and V blocks
-// into 3- and 2-stage rings); warp 1 owns TMEM and issues tcgen05.mma; warps
-// 2-5 and 6-9 are two softmax warpgroups (query columns 0-31 and 32-63) that
-// also run the epilogue. Every wait is bounded (see ptx.cuh).
+// Warp roles (640 threads): warp 0 issues the TMA loads of Q and of the K
+// blocks (3-stage ring), warp 19 those of the V blocks (2-stage ring), four
+// lanes each issuing one 8 KB box; warp 1 owns TMEM and issues the S^T
+// products, warp 18 the O^T products; warps 2-17 are four softmax warpgroups
+// (16 query columns each) that also run the epilogue. Spreading the columns
+// over 16 warps shortens each warp's per-block dependency chain. Every wait
+// is bounded (see ptx.cuh).
 #include "kernels.cuh"
 #include "ptx.cuh"
 
 namespace vsa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kSoftmaxWGs = 4;               // softmax warpgroups, each kCols query columns
+constexpr int kCols = 64 / kSoftmaxWGs;
+constexpr int kThreads = 32 * (4 + 4 * kSoftmaxWGs);  // 20 warps
+constexpr int kWarpProducer = 0;             // Q, then the K ring
+constexpr int kWarpMmaS = 1;                 // also owns the TMEM allocation
+constexpr int kWarpSoftmax0 = 2;             // warps 2 .. 2 + 4*kSoftmaxWGs - 1
+constexpr int kWarpMmaPV = kWarpSoftmax0 + 4 * kSoftmaxWGs;
+constexpr int kWarpProducerV = kWarpMmaPV + 1;  // the V ring
+static_assert(kCols == 16, "the softmax code below is written for 16 columns per warpgroup");
 constexpr int kNumK = 3;
 constexpr int kNumV = 2;
 constexpr uint32_t kQBytes = 64 * kHeadDim * 2;    // 16 KB
 constexpr uint32_t kKVBytes = 128 * kHeadDim * 2;  // 32 KB, one 128-key block
 constexpr uint32_t kPBytes = 128 * 64 * 2;         // 16 KB
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS1 = 64;  // S^T buffer b at column b * kColS1
-constexpr uint32_t kColO = 128;
+constexpr int kNumS = 3;                 // S^T buffers in TMEM
+constexpr int kNumP = 3;                 // P^T buffers in shared memory
+constexpr uint32_t kColS1 = 64;          // S^T buffer b at column b * kColS1
+constexpr uint32_t kColO = kNumS * kColS1;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P never exceeds 2^8
 
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
 constexpr uint32_t kOffV = kOffK + kNumK * kKVBytes;
 constexpr uint32_t kOffP = kOffV + kNumV * kKVBytes;
-constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffBar = kOffP + kNumP * kPBytes;
 constexpr uint32_t kOffRed = kOffBar + 256;
-constexpr uint32_t kOffSlot = kOffRed + 2 * 32 * 4 * 4;
+constexpr uint32_t kOffSlot = kOffRed + 64 * 4 * 4;  // [64 query columns][4 lane quarters] fp32
 constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;  // + 1024-byte alignment slack
 
 // barrier indices
@@ -59,11 +72,12 @@ constexpr int kBarKEmpty = kBarKFull + kNumK;
 constexpr int kBarVFull = kBarKEmpty + kNumK;
 constexpr int kBarVEmpty = kBarVFull + kNumV;
 constexpr int kBarSFull = kBarVEmpty + kNumV;
-constexpr int kBarSEmpty = kBarSFull + 2;
-constexpr int kBarPFull = kBarSEmpty + 2;
-constexpr int kBarPEmpty = kBarPFull + 2;
-constexpr int kNumBars = kBarPEmpty + 2;
+constexpr int kBarSEmpty = kBarSFull + kNumS;
+constexpr int kBarPFull = kBarSEmpty + kNumS;
+constexpr int kBarPEmpty = kBarPFull + kNumP;
+constexpr int kNumBars = kBarPEmpty + kNumP;
 static_assert(kNumBars * 8 <= 256, "barrier area");
+static_assert(kColO + 64 <= kTmemCols, "TMEM columns");
 
 struct FineParams {
   int B, H, P, Lv, N, T, TP, k;
@@ -123,22 +137,31 @@ __device__ __forceinline__ int kv_tile_id(const Item& it, int tp, int ti) {
   return it.list ? __ldg(it.list + (ti - tp)) : ti - tp;
 }
 
-// Reduce 32 per-lane column values across the warp; afterwards lane c holds the
-// reduction of column c. The input array is consumed.
-template <bool kMax>
-__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+// One halving step of the warp reduce-scatter: lanes with bit O set keep the
+// upper half of the live columns, the others the lower half, combined with the
+// half their partner (lane ^ O) gave away.
+template <bool kMax, int O, int N>
+__device__ __forceinline__ void reduce_scatter_step(float (&v)[N], int lane) {
+  const bool upper = (lane & O) != 0;
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < o; ++i) {
-      const float send = upper ? v[i] : v[i + o];
-      const float keep = upper ? v[i + o] : v[i];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, o);
-      v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
-    }
+  for (int i = 0; i < O; ++i) {
+    const float send = upper ? v[i] : v[i + O];
+    const float keep = upper ? v[i + O] : v[i];
+    const float recv = __shfl_xor_sync(0xffffffffu, send, O);
+    v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
   }
-  return v[0];
+}
+
+// Reduce 16 per-lane column values across the warp; afterwards lanes c and
+// c + 16 hold the reduction of column c. The input array is consumed.
+template <bool kMax>
+__device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
+  reduce_scatter_step<kMax, 8>(v, lane);
+  reduce_scatter_step<kMax, 4>(v, lane);
+  reduce_scatter_step<kMax, 2>(v, lane);
+  reduce_scatter_step<kMax, 1>(v, lane);
+  const float other = __shfl_xor_sync(0xffffffffu, v[0], 16);
+  return kMax ? fmaxf(v[0], other) : v[0] + other;
 }
 
 __device__ __forceinline__ bool warp_any(bool x) { return __any_sync(0xffffffffu, x); }
@@ -167,24 +190,29 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     mbar_init(bar(kBarQ), 1);
     for (int s = 0; s < kNumK; ++s) { mbar_init(bar(kBarKFull + s), 1); mbar_init(bar(kBarKEmpty + s), 1); }
     for (int s = 0; s < kNumV; ++s) { mbar_init(bar(kBarVFull + s), 1); mbar_init(bar(kBarVEmpty + s), 1); }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kNumS; ++s) {
       mbar_init(bar(kBarSFull + s), 1);
-      mbar_init(bar(kBarSEmpty + s), 8);
-      mbar_init(bar(kBarPFull + s), 8);
+      mbar_init(bar(kBarSEmpty + s), 4 * kSoftmaxWGs);
+    }
+    for (int s = 0; s < kNumP; ++s) {
+      mbar_init(bar(kBarPFull + s), 4 * kSoftmaxWGs);
       mbar_init(bar(kBarPEmpty + s), 1);
     }
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tslot), kTmemCols);
+  if (warp == kWarpMmaS) tmem_alloc(smem_u32(tslot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == kWarpProducer || warp == kWarpProducerV) {
+    // ------------------------------------------------------------ TMA producers
+    // Lanes 0-3 of each producer warp issue the four 8 KB boxes of a block (tile
+    // a/b x channel half): several issuing threads keep far more bytes in flight
+    // than one thread can.
     bool failed = abort_raised(err);
-    if (lane == 0 && !failed) {
+    if (warp == kWarpProducer && lane == 0 && !failed) {
       prefetch_tensor_map(&map_q);
       prefetch_tensor_map(&map_k);
       prefetch_tensor_map(&map_v);
@@ -214,221 +242,221 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       }
       return p.P + j * kTile;
     };
-    int prev_ra = 0, prev_rb = 0;
-    for (int step = 0; step <= nblk && !failed; ++step) {
-      int ra = 0, rb = 0;
-      if (step < nblk) {
-        ra = tile_row(2 * step);
-        rb = tile_row(2 * step + 1);
-        if (lane == 0) {
-          const int s = step % kNumK;
-          const uint32_t par = ((step / kNumK) & 1) ^ 1;
-          if (mbar_wait(bar(kBarKEmpty + s), par, err, 0x100u)) {
-            const uint32_t dst = sK + s * kKVBytes;
-            mbar_arrive_expect_tx(bar(kBarKFull + s), kKVBytes);
-            for (int c = 0; c < 2; ++c) {
-              tma_load_4d(dst + c * 16384, &map_k, 64 * c, it.h, ra, it.b, bar(kBarKFull + s));
-              tma_load_4d(dst + c * 16384 + 8192, &map_k, 64 * c, it.h, rb, it.b, bar(kBarKFull + s));
-            }
-          } else {
-            failed = true;
-          }
-        }
+    // K and V come from separate warps so that a full V ring never delays K.
+    const bool v_warp = warp == kWarpProducerV;
+    const CUtensorMap* map = v_warp ? &map_v : &map_k;
+    const uint32_t ring = v_warp ? sV : sK;
+    const int nstage = v_warp ? kNumV : kNumK;
+    const int bar_full = v_warp ? kBarVFull : kBarKFull;
+    const int bar_empty = v_warp ? kBarVEmpty : kBarKEmpty;
+    const int box_tile = (lane >> 1) & 1, box_half = lane & 1;  // this lane's box within a block
+    const uint32_t box_off = box_half * 16384 + box_tile * 8192;
+    for (int blk = 0; blk < nblk && !failed; ++blk) {
+      const int ra = tile_row(2 * blk);
+      const int rb = tile_row(2 * blk + 1);
+      const int s = blk % nstage;
+      bool ok = true;
+      if (lane == 0) {
+        ok = mbar_wait(bar(bar_empty + s), ((blk / nstage) & 1) ^ 1, err, v_warp ? 0x200u : 0x100u, 128);
+        if (ok) mbar_arrive_expect_tx(bar(bar_full + s), kKVBytes);
       }
-      if (step >= 1 && lane == 0 && !failed) {
-        const int vb = step - 1;
-        const int s = vb % kNumV;
-        const uint32_t par = ((vb / kNumV) & 1) ^ 1;
-        if (mbar_wait(bar(kBarVEmpty + s), par, err, 0x200u)) {
-          const uint32_t dst = sV + s * kKVBytes;
-          mbar_arrive_expect_tx(bar(kBarVFull + s), kKVBytes);
-          for (int c = 0; c < 2; ++c) {
-            tma_load_4d(dst + c * 16384, &map_v, 64 * c, it.h, prev_ra, it.b, bar(kBarVFull + s));
-            tma_load_4d(dst + c * 16384 + 8192, &map_v, 64 * c, it.h, prev_rb, it.b, bar(kBarVFull + s));
-          }
-        } else {
-          failed = true;
-        }
-      }
-      failed = __shfl_sync(0xffffffffu, failed, 0);
-      prev_ra = ra;
-      prev_rb = rb;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) { failed = true; break; }
+      if (lane < 4)
+        tma_load_4d(ring + s * kKVBytes + box_off, map, 64 * box_half, it.h, box_tile ? rb : ra, it.b,
+                    bar(bar_full + s));
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kWarpMmaS) {
+    // ------------------------------------------------------------ S^T = K Q^T issuer
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
-      const uint32_t id_o = idesc_bf16_f32(128, 64, 1, 1);
-      auto issue_pv = [&](int j) -> bool {
-        const int vs = j % kNumV, pb = j & 1;
-        if (!mbar_wait(bar(kBarVFull + vs), (j / kNumV) & 1, err, 0x300u)) return false;
-        if (!mbar_wait(bar(kBarPFull + pb), (j >> 1) & 1, err, 0x400u)) return false;
-        tc_fence_after();
-        const uint32_t va = sV + vs * kKVBytes, pa = sP + pb * kPBytes;
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          const uint64_t a = smem_desc_sw128(va + s * 2048, 16384, 1024);
-          const uint64_t b = smem_desc_sw128(pa + s * 2048, 8192, 1024);
-          umma_bf16(tbase + kColO, a, b, id_o, (j > 0 || s > 0) ? 1u : 0u);
-        }
-        umma_commit(bar(kBarVEmpty + vs));
-        umma_commit(bar(kBarPEmpty + pb));
-        return true;
-      };
-      bool ok = mbar_wait(bar(kBarQ), 0, err, 0x500u);
+      const uint64_t dk0 = smem_desc_sw128(sK, 16, 1024);
+      const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
+      bool ok = mbar_wait(bar(kBarQ), 0, err, 0x500u, 64);
       for (int i = 0; i < nblk && ok; ++i) {
-        const int ks = i % kNumK, sb = i & 1;
-        ok = mbar_wait(bar(kBarKFull + ks), (i / kNumK) & 1, err, 0x600u) &&
-             mbar_wait(bar(kBarSEmpty + sb), ((i >> 1) & 1) ^ 1, err, 0x700u);
+        const int ks = i % kNumK, sb = i % kNumS;
+        ok = mbar_wait(bar(kBarKFull + ks), (i / kNumK) & 1, err, 0x600u, 64) &&
+             mbar_wait(bar(kBarSEmpty + sb), ((i / kNumS) & 1) ^ 1, err, 0x700u, 64);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t ka = sK + ks * kKVBytes;
+        const uint64_t dk = dk0 + ((ks * kKVBytes) >> 4);
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-          const uint64_t a = smem_desc_sw128(ka + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
-          const uint64_t b = smem_desc_sw128(sQ + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024);
-          umma_bf16(tbase + sb * kColS1, a, b, id_s, s > 0 ? 1u : 0u);
+          const uint32_t koff = ((s >> 2) * 16384 + (s & 3) * 32) >> 4;
+          const uint32_t qoff = ((s >> 2) * 8192 + (s & 3) * 32) >> 4;
+          umma_bf16(tbase + sb * kColS1, dk + koff, dq0 + qoff, id_s, s > 0 ? 1u : 0u);
         }
         umma_commit(bar(kBarKEmpty + ks));
         umma_commit(bar(kBarSFull + sb));
-        if (i >= 1) ok = issue_pv(i - 1);
       }
-      if (ok) issue_pv(nblk - 1);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMmaPV) {
+    // ------------------------------------------------------------ O^T += V^T P^T issuer
+    if (lane == 0) {
+      const uint32_t id_o = idesc_bf16_f32(128, 64, 1, 1);
+      const uint64_t dv0 = smem_desc_sw128(sV, 16384, 1024);
+      const uint64_t dp0 = smem_desc_sw128(sP, 8192, 1024);
+      for (int j = 0; j < nblk; ++j) {
+        const int vs = j % kNumV, pb = j % kNumP;
+        if (!mbar_wait(bar(kBarVFull + vs), (j / kNumV) & 1, err, 0x300u, 32)) break;
+        if (!mbar_wait(bar(kBarPFull + pb), (j / kNumP) & 1, err, 0x400u, 32)) break;
+        tc_fence_after();
+        const uint64_t dv = dv0 + ((vs * kKVBytes) >> 4);
+        const uint64_t dp = dp0 + ((pb * kPBytes) >> 4);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          umma_bf16(tbase + kColO, dv + ((s * 2048) >> 4), dp + ((s * 2048) >> 4), id_o,
+                    (j > 0 || s > 0) ? 1u : 0u);
+        umma_commit(bar(kBarVEmpty + vs));
+        umma_commit(bar(kBarPEmpty + pb));
+      }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int wg = (warp - 2) / 4;          // query columns 32*wg .. 32*wg+31
-    const int q4 = warp % 4;                // TMEM lane quarter this warp may access
-    const int r = 32 * q4 + lane;           // key lane (softmax), head dim (epilogue)
+    const int wg = (warp - kWarpSoftmax0) / 4;  // query columns kCols*wg .. kCols*wg + kCols-1
+    const int q4 = warp % 4;                     // TMEM lane quarter this warp may access
+    const int r = 32 * q4 + lane;                // key lane (softmax), head dim (epilogue)
+    const int col0 = kCols * wg;
+    const int key_row = r & 63, key_slot = r >> 6;
     const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
     const uint32_t bar_id = 1 + wg;
     const float sl2 = p.scale_log2;
-    float m[32], l[32];
+    // Only two key tiles can be ragged: the last prefix tile, and video tile T-1,
+    // which (selections being ascending) can only be the item's last key tile.
+    const int prefix_tail = p.TP > 0 ? p.P - (p.TP - 1) * kTile : kTile;
+    const int video_tail = p.Lv - (p.T - 1) * kTile;
+    const bool last_is_ragged =
+        video_tail < kTile && (it.list == nullptr || __ldg(it.list + p.k - 1) == p.T - 1);
+    float nm[kCols], l[kCols];  // -reference (log2 units) and this lane's partial row sums, per column
 #pragma unroll
-    for (int c = 0; c < 32; ++c) { m[c] = -INFINITY; l[c] = 0.f; }
+    for (int c = 0; c < kCols; ++c) { nm[c] = INFINITY; l[c] = 0.f; }
     bool failed = false;
-    int j_cur = kv_tile_id(it, p.TP, r >> 6);
     for (int i = 0; i < nblk; ++i) {
-      const int sb = i & 1;
-      const int ti = 2 * i + (r >> 6);
-      const int j_nxt = kv_tile_id(it, p.TP, ti + 2);
-      const bool valid = (r & 63) < kv_tile_len(p, it, ti, j_cur);
-      j_cur = j_nxt;
+      const int sb = i % kNumS, pb = i % kNumP;
+      const int ti = 2 * i + key_slot;
+      bool valid = ti < it.n_kv;
+      if (ti == p.TP - 1) valid = key_row < prefix_tail;
+      if (ti == it.n_kv - 1 && last_is_ragged) valid = valid && key_row < video_tail;
 
-      failed = warp_any(failed || !mbar_wait(bar(kBarSFull + sb), (i >> 1) & 1, err, 0x800u));
-      float s[32];
+      failed = warp_any(failed || !mbar_wait(bar(kBarSFull + sb), (i / kNumS) & 1, err, 0x800u));
+      float s[kCols];
       if (!failed) {
         tc_fence_after();
-        uint32_t raw[32];
-        tmem_ld32(tbase + lane_off + sb * kColS1 + 32 * wg, raw);
+        uint32_t raw[kCols];
+        tmem_ld16(tbase + lane_off + sb * kColS1 + col0, raw);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(raw[c]);
+        for (int c = 0; c < kCols; ++c) s[c] = __uint_as_float(raw[c]);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarSEmpty + sb));
       } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) s[c] = 0.f;
+        for (int c = 0; c < kCols; ++c) s[c] = 0.f;
       }
-      float t[32];
-      float mx = -INFINITY;
+      if (!valid) {  // masked key lane (ragged or absent tile): contributes nothing
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        t[c] = valid ? fmaf(s[c], sl2, -m[c]) : -INFINITY;
-        mx = fmaxf(mx, t[c]);
+        for (int c = 0; c < kCols; ++c) s[c] = -INFINITY;
       }
-      if (named_bar_or(bar_id, 128, failed || mx > kRescaleThreshold)) {
+      // t = s * log2(e)/sqrt(128) - reference, two columns per instruction
+      float t[kCols];
+#pragma unroll
+      for (int c = 0; c < kCols; c += 2) fma_f32x2(t[c], t[c + 1], s[c], s[c + 1], sl2, sl2, nm[c], nm[c + 1]);
+      const float mxall = fmax3(fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmax3(t[6], t[7], t[8])),
+                                fmax3(t[9], t[10], t[11]), fmax3(fmax3(t[12], t[13], t[14]), t[15], -INFINITY));
+      if (named_bar_or(bar_id, 128, failed || mxall > kRescaleThreshold)) {
         if (named_bar_or(bar_id, 128, failed)) { failed = true; break; }
         // slow path: exact block maximum per query column across the 128 key lanes
-        float u[32];
+        float u[kCols];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) u[c] = valid ? s[c] * sl2 : -INFINITY;
-        const float wmax = reduce_scatter32<true>(u, lane);
-        red[(wg * 32 + lane) * 4 + q4] = wmax;
+        for (int c = 0; c < kCols; ++c) u[c] = s[c] * sl2;
+        const float wmax = reduce_scatter16<true>(u, lane);
+        if (lane < kCols) red[(wg * kCols + lane) * 4 + q4] = wmax;
         named_bar_sync(bar_id, 128);
-        float alpha[32];
+        float alpha[kCols];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float4 x = reinterpret_cast<const float4*>(red)[wg * 32 + c];
+        for (int c = 0; c < kCols; ++c) {
+          const float4 x = reinterpret_cast<const float4*>(red)[wg * kCols + c];
           const float bm = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
-          const float mn = fmaxf(m[c], bm);
-          alpha[c] = ex2_approx(m[c] - mn);
+          const float nmn = fminf(nm[c], -bm);
+          alpha[c] = ex2_approx(nmn - nm[c]);
           l[c] *= alpha[c];
-          m[c] = mn;
+          nm[c] = nmn;
         }
         if (i > 0) {
           // O^T must hold every PV product issued so far: wait for PV of block
-          // i-1 on its P-buffer barrier (PV of block i-3 is already known to be
-          // complete, so this parity wait cannot alias an older phase; tcgen05
-          // MMAs complete in issue order).
+          // i-1 on its P-buffer barrier (PV of block i-1-kNumP is already known
+          // to be complete, so this parity wait cannot alias an older phase;
+          // tcgen05 MMAs complete in issue order).
           const int pj = i - 1;
-          failed = warp_any(!mbar_wait(bar(kBarPEmpty + (pj & 1)), (pj >> 1) & 1, err, 0x900u));
+          failed = warp_any(!mbar_wait(bar(kBarPEmpty + pj % kNumP), (pj / kNumP) & 1, err, 0x900u));
           if (!failed) {
             tc_fence_after();
-            uint32_t o[32];
-            tmem_ld32(tbase + lane_off + kColO + 32 * wg, o);
+            uint32_t o[kCols];
+            tmem_ld16(tbase + lane_off + kColO + col0, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha[c]);
-            tmem_st32(tbase + lane_off + kColO + 32 * wg, o);
+            for (int c = 0; c < kCols; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha[c]);
+            tmem_st16(tbase + lane_off + kColO + col0, o);
             tmem_wait_st();
             tc_fence_before();
           }
         }
 #pragma unroll
-        for (int c = 0; c < 32; ++c) t[c] = valid ? fmaf(s[c], sl2, -m[c]) : -INFINITY;
+        for (int c = 0; c < kCols; c += 2)
+          fma_f32x2(t[c], t[c + 1], s[c], s[c + 1], sl2, sl2, nm[c], nm[c + 1]);
       }
-      uint32_t pk[16];
+      uint32_t pk[kCols / 2];
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
+      for (int c = 0; c < kCols; c += 2) {
         const float p0 = ex2_approx(t[c]), p1 = ex2_approx(t[c + 1]);
-        l[c] += p0;
-        l[c + 1] += p1;
+        add_f32x2(l[c], l[c + 1], l[c], l[c + 1], p0, p1);
         pk[c / 2] = pack_bf16x2(p0, p1);
       }
-      failed = warp_any(failed || !mbar_wait(bar(kBarPEmpty + sb), ((i >> 1) & 1) ^ 1, err, 0xA00u));
+      failed = warp_any(failed || !mbar_wait(bar(kBarPEmpty + pb), ((i / kNumP) & 1) ^ 1, err, 0xA00u));
       if (!failed) {
-        const uint32_t row = sP + sb * kPBytes + r * 128;
+        const uint32_t prow = sP + pb * kPBytes + r * 128;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const uint32_t chunk = static_cast<uint32_t>((4 * wg + cc) ^ (r & 7));
-          st_shared_v4(row + chunk * 16, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        for (int cc = 0; cc < kCols / 8; ++cc) {
+          const uint32_t chunk = static_cast<uint32_t>((col0 / 8 + cc) ^ (r & 7));
+          st_shared_v4(prow + chunk * 16, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarPFull + sb));
+        if (lane == 0) mbar_arrive(bar(kBarPFull + pb));
       }
     }
     // ---- epilogue: out = O / l (+ sigmoid(gate) * coarse on video rows)
     if (!named_bar_or(bar_id, 128, failed)) {
-      const float lw = reduce_scatter32<false>(l, lane);
-      red[(wg * 32 + lane) * 4 + q4] = lw;
+      const float lw = reduce_scatter16<false>(l, lane);
+      if (lane < kCols) red[(wg * kCols + lane) * 4 + q4] = lw;
       named_bar_sync(bar_id, 128);
       const int pj = nblk - 1;  // the last PV product (see the rescale above)
-      failed = warp_any(!mbar_wait(bar(kBarPEmpty + (pj & 1)), (pj >> 1) & 1, err, 0xB00u));
+      failed = warp_any(!mbar_wait(bar(kBarPEmpty + pj % kNumP), (pj / kNumP) & 1, err, 0xB00u));
       if (!failed) {
         tc_fence_after();
-        uint32_t o[32];
-        tmem_ld32(tbase + lane_off + kColO + 32 * wg, o);
+        uint32_t o[kCols];
+        tmem_ld16(tbase + lane_off + kColO + col0, o);
         tmem_wait_ld();
         const int d = r;
         float cz = 0.f;
         if (it.video)
           cz = __ldg(p.coarse + ((static_cast<size_t>(it.b) * p.H + it.h) * p.T + it.t) * kHeadDim + d);
-#pragma unroll 4
-        for (int c = 0; c < 32; ++c) {
-          const int qc = 32 * wg + c;
+        const size_t row_stride = static_cast<size_t>(p.H) * kHeadDim;
+        const size_t base = (static_cast<size_t>(it.b) * p.N + it.q_row0) * row_stride +
+                            static_cast<size_t>(it.h) * kHeadDim + d;
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) {
+          const int qc = col0 + c;
           if (qc < it.q_valid) {
-            const float4 x = reinterpret_cast<const float4*>(red)[wg * 32 + c];
+            const float4 x = reinterpret_cast<const float4*>(red)[wg * kCols + c];
             const float lsum = (x.x + x.y) + (x.z + x.w);
-            float val = __uint_as_float(o[c]) / lsum;
-            const size_t off =
-                ((static_cast<size_t>(it.b) * p.N + it.q_row0 + qc) * p.H + it.h) * kHeadDim + d;
+            float val = __fdividef(__uint_as_float(o[c]), lsum);
+            const size_t off = base + static_cast<size_t>(qc) * row_stride;
             if (it.video) {
               const float g = __bfloat162float(p.gate[off]);
-              val += cz / (1.0f + __expf(-g));
+              val += __fdividef(cz, 1.0f + __expf(-g));
             }
             p.out[off] = __float2bfloat16_rn(val);
           }
@@ -439,7 +467,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tbase, kTmemCols);
+  if (warp == kWarpMmaS) tmem_dealloc(tbase, kTmemCols);
 }
 
 }  // namespace

@@ -72,19 +72,43 @@ __device__ __forceinline__ void raise_error(unsigned int* words, unsigned int co
   __threadfence();
 }
 
+// try_wait with a suspend-time hint: the waiting thread sleeps (issuing
+// nothing) until the phase completes or the hint elapses.
+constexpr uint32_t kSuspendHintNs = 500000;
+
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of `bar` with parity `parity` to complete. Returns false
-// (after recording a timeout) if it does not within kWaitLimitNs, or at once
-// if the abort flag is already up.
+// (after recording a timeout) if it does not within kWaitLimitNs, or soon after
+// another CTA raised the abort flag.
+// `sleep_ns` > 0 backs off with __nanosleep between polls: for waiters that run
+// ahead of the critical path (loaders, the S issuer), so that their polling
+// does not take issue slots from the warps doing the arithmetic.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err,
-                                          unsigned int detail) {
+                                          unsigned int detail, uint32_t sleep_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  uint64_t t0 = 0;
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 64; ++i) {
       if (mbar_try_wait(bar, parity)) return true;
+      if (sleep_ns) __nanosleep(sleep_ns);
+    }
     if (abort_raised(err)) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    const uint64_t now = global_timer_ns();
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > kWaitLimitNs) {
       raise_error(err, kErrDeviceTimeout, detail);
       return false;
     }
@@ -206,6 +230,31 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+#define VSA_R16(r)                                                                              \
+  "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),           \
+      "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),    \
+      "=r"(r[14]), "=r"(r[15])
+#define VSA_W16(r)                                                                              \
+  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),       \
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+
+// Warp-collective: 16 consecutive 32-bit columns of lane (taddr lane field) + i.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : VSA_R16(r)
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      VSA_W16(r)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -230,6 +279,32 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool p
       : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
       : "memory");
   return out != 0;
+}
+
+// d = a * b + c on two lanes at once (packed fp32).
+__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, float b0,
+                                          float b1, float c0, float c1) {
+  asm("{\n.reg .b64 ra, rb, rc, rd;\n"
+      "mov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\nmov.b64 rc, {%6, %7};\n"
+      "fma.rn.f32x2 rd, ra, rb, rc;\nmov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// d = a + b on two lanes at once (packed fp32).
+__device__ __forceinline__ void add_f32x2(float& d0, float& d1, float a0, float a1, float b0,
+                                          float b1) {
+  asm("{\n.reg .b64 ra, rb, rd;\n"
+      "mov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\n"
+      "add.rn.f32x2 rd, ra, rb;\nmov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
