@@ -25,6 +25,7 @@ VSA_ERR_UNSUPPORTED = 2
 VSA_ERR_CUDA = 3
 VSA_ERR_DEVICE_TIMEOUT = 4
 VSA_ERR_INTERNAL = 5
+STATIC_WORKSPACE_BYTES = 32 * 1024 * 1024  # VSA_STATIC_WORKSPACE_BYTES in include/vsa.h
 
 
 class VsaError(RuntimeError):
@@ -67,6 +68,7 @@ def load_library(path: str = LIB_PATH):
         "vsa_debug_views": (i32, [vp, vp] + [ctypes.POINTER(vp)] * 5),
         "vsa_check": (i32, [vp, vp, vp]),
         "vsa_plan_set_stage_events": (i32, [vp, ctypes.POINTER(vp)]),
+        "vsa_forward_static_workspace": (i32, [vp, vp, vp, vp, vp, vp, vp]),
         "vsa_plan_destroy": (None, [vp]),
         "vsa_status_string": (ctypes.c_char_p, [i32]),
     }
@@ -155,6 +157,18 @@ def vsa_forward_host(plan, q, k, v, gate, out, device_buffer, stream=None):
                                            _ptr(device_buffer),
                                            device_buffer.numel() * device_buffer.element_size(),
                                            _stream_handle(stream)), "vsa_forward_host")
+
+
+def vsa_forward_static_workspace(plan, q, k, v, gate, out, stream=None):
+    """Forward that allocates nothing: the scratch is the library's own fixed-size
+    device array (VSA_STATIC_WORKSPACE_BYTES). For callers that cannot allocate
+    device memory. Calls that overlap on the GPU race on the shared array."""
+    status = load_library().vsa_forward_static_workspace(plan, _ptr(q), _ptr(k), _ptr(v), _ptr(gate),
+                                                         _ptr(out), _stream_handle(stream))
+    if status == VSA_ERR_UNSUPPORTED:
+        raise VsaError(status, "vsa_forward_static_workspace: the plan's workspace exceeds "
+                               f"{STATIC_WORKSPACE_BYTES} bytes")
+    _check(status, "vsa_forward_static_workspace")
 
 
 def vsa_check(plan, workspace, stream=None):
@@ -249,4 +263,5 @@ __all__ = [
     "VSA", "VsaError", "load_library", "header_functions", "vsa_plan_create", "vsa_plan_info",
     "vsa_forward", "vsa_forward_host", "vsa_plan_host_path_bytes", "vsa_debug_views", "vsa_check",
     "vsa_plan_set_stage_events", "vsa_plan_destroy", "vsa_status_string",
+    "vsa_forward_static_workspace",
 ]

@@ -1,0 +1,17 @@
+// The host-side plan behind the opaque vsa_plan_t handle of include/vsa.h.
+#pragma once
+#include <cstddef>
+#include <cuda_runtime.h>
+
+#include "kernels.cuh"
+#include "vsa.h"
+
+struct vsa_plan {
+  vsa_shape_t shape;
+  int device;
+  vsa::Geometry g;
+  size_t off_err, off_pq, off_pk, off_pv, off_coarse, off_idx, ws_bytes;
+  size_t tensor_bytes;  // one bf16 [B, N, H, 128] tensor
+  cudaEvent_t events[4];
+  bool have_events;
+};

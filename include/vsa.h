@@ -96,8 +96,7 @@ vsa_status_t vsa_plan_info(vsa_plan_t plan, int64_t* n_tiles, int64_t* k, size_t
  *   stream        : cudaStream_t to launch on (NULL = legacy default stream)
  * Enqueues three kernels (tile pool; coarse attention + top-k; fine attention
  * with the gated combination fused into its epilogue) and returns without
- * synchronising. It allocates nothing and reads no device data on the host, so
- * it can be captured into a CUDA graph. */
+ * synchronising. It allocates nothing and reads no device data on the host. */
 vsa_status_t vsa_forward(vsa_plan_t plan, const void* q, const void* k, const void* v,
                          const void* gate, void* out, void* workspace, size_t workspace_bytes,
                          void* stream);
@@ -131,6 +130,34 @@ vsa_status_t vsa_check(vsa_plan_t plan, void* workspace, void* stream);
  * the forward's stream. The four cudaEvent_t handles are owned by the caller;
  * pass NULL to stop recording. */
 vsa_status_t vsa_plan_set_stage_events(vsa_plan_t plan, void* const* events);
+
+/* Size of the library-owned workspace used by vsa_forward_static_workspace:
+ * 32 MiB, enough for one GPU's head share of a 5 s request (14 heads, 36,288
+ * video tokens) or anything whose workspace_bytes (vsa_plan_info) fits. */
+#define VSA_STATIC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+
+/* The forward for callers that cannot allocate device memory (a serving engine
+ * that budgets all device memory at start-up, a plugin interface without an
+ * allocator, a latency-critical path that must not call cudaMalloc). The
+ * paper has no counterpart to this entry point.
+ *   q, k, v, gate, out, stream: as for vsa_forward; the caller still owns them.
+ * The scratch is a file-scope device array of VSA_STATIC_WORKSPACE_BYTES inside
+ * the library; every GPU that loads the library holds it until the process
+ * exits. The call allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library routine).
+ * Returns VSA_ERR_UNSUPPORTED, without launching, if the plan's workspace_bytes
+ * exceed VSA_STATIC_WORKSPACE_BYTES.
+ * The first call for a plan on a given device resolves the array's device
+ * address (cudaGetSymbolAddress, once per device); make that first call before
+ * any stream capture.
+ * All calls share the one array, which keeps the previous call's contents (the
+ * forward clears what must start at zero and overwrites the rest): calls whose
+ * work overlaps on the GPU (different streams, or host threads, without
+ * ordering between them) race on it. Device-side wait timeouts land in the
+ * array's error words and are not reported by this entry point. */
+vsa_status_t vsa_forward_static_workspace(vsa_plan_t plan, const void* q, const void* k,
+                                          const void* v, const void* gate, void* out,
+                                          void* stream);
 
 void vsa_plan_destroy(vsa_plan_t plan);
 
