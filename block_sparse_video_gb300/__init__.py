@@ -69,6 +69,7 @@ def load_library(path: str = LIB_PATH):
         "vsa_check": (i32, [vp, vp, vp]),
         "vsa_plan_set_stage_events": (i32, [vp, ctypes.POINTER(vp)]),
         "vsa_forward_static_workspace": (i32, [vp, vp, vp, vp, vp, vp, vp]),
+        "vsa_diag_wait_timeout": (i32, [vp, vp, ctypes.c_int, vp]),
         "vsa_plan_destroy": (None, [vp]),
         "vsa_status_string": (ctypes.c_char_p, [i32]),
     }
@@ -171,6 +172,12 @@ def vsa_forward_static_workspace(plan, q, k, v, gate, out, stream=None):
     _check(status, "vsa_forward_static_workspace")
 
 
+def vsa_diag_wait_timeout(plan, workspace, n_ctas=1, stream=None):
+    """Launch the diagnostic kernel whose bounded waits must run out (see vsa.h)."""
+    _check(load_library().vsa_diag_wait_timeout(plan, _ptr(workspace), int(n_ctas), _stream_handle(stream)),
+           "vsa_diag_wait_timeout")
+
+
 def vsa_check(plan, workspace, stream=None):
     """Synchronise and raise VsaError if a bounded wait inside a kernel gave up."""
     _check(load_library().vsa_check(plan, _ptr(workspace), _stream_handle(stream)), "vsa_check")
@@ -263,5 +270,5 @@ __all__ = [
     "VSA", "VsaError", "load_library", "header_functions", "vsa_plan_create", "vsa_plan_info",
     "vsa_forward", "vsa_forward_host", "vsa_plan_host_path_bytes", "vsa_debug_views", "vsa_check",
     "vsa_plan_set_stage_events", "vsa_plan_destroy", "vsa_status_string",
-    "vsa_forward_static_workspace",
+    "vsa_forward_static_workspace", "vsa_diag_wait_timeout",
 ]

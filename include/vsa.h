@@ -131,6 +131,15 @@ vsa_status_t vsa_check(vsa_plan_t plan, void* workspace, void* stream);
  * pass NULL to stop recording. */
 vsa_status_t vsa_plan_set_stage_events(vsa_plan_t plan, void* const* events);
 
+/* Diagnostics: launch `n_ctas` CTAs that each wait on a barrier nothing ever
+ * completes, using the same bounded wait as the forward's kernels, with the
+ * error words of `workspace` (a workspace of this plan). The first wait gives up
+ * after its time limit (2 s) and records VSA_ERR_DEVICE_TIMEOUT; the other CTAs
+ * observe the abort flag and return. vsa_check(plan, workspace, stream) then
+ * reports VSA_ERR_DEVICE_TIMEOUT. Exercises failure detection without any GPU
+ * fault; returns without synchronising. */
+vsa_status_t vsa_diag_wait_timeout(vsa_plan_t plan, void* workspace, int n_ctas, void* stream);
+
 /* Size of the library-owned workspace used by vsa_forward_static_workspace:
  * 32 MiB, enough for one GPU's head share of a 5 s request (14 heads, 36,288
  * video tokens) or anything whose workspace_bytes (vsa_plan_info) fits. */
