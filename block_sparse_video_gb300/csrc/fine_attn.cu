@@ -54,7 +54,8 @@ constexpr int kNumS = 3;                 // S^T buffers in TMEM
 constexpr int kNumP = 3;                 // P^T buffers in shared memory
 constexpr uint32_t kColS1 = 64;          // S^T buffer b at column b * kColS1
 constexpr uint32_t kColO = kNumS * kColS1;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: P never exceeds 2^8
+constexpr float kRescaleThreshold = 8.0f;  // exact mode: rescale when P would exceed 2^8
+constexpr float kFastLimit = 60.0f;         // fast mode: P stays below 2^60, far from fp32/bf16 overflow
 
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
@@ -186,7 +187,23 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
   const Item it = decode_item(p, blockIdx.x);
   const int nblk = (it.n_kv + 1) / 2;
 
+  volatile uint32_t* redo_flag = tslot + 1;  // set when the fast pass must be redone exactly
+  if (warp == kWarpMmaS) tmem_alloc(smem_u32(tslot), kTmemCols);
+
+  for (int pass = 0; pass < 2; ++pass) {
+  // Pass 0 is the fast mode: after the first block, the per-column softmax
+  // reference stays fixed and blocks need no warpgroup vote. It is valid while
+  // no score exceeds the reference by more than 2^kFastLimit (P, the row sums
+  // and O then stay finite, and exact in relative terms). A thread that sees a
+  // larger excess flags the item, and the CTA reruns it in pass 1 with the
+  // exact per-block rescaling.
+  const bool exact = pass > 0;
   if (tid == 0) {
+    if (pass > 0) {
+      for (int i = 0; i < kNumBars; ++i) mbar_inval(bar(i));
+    } else {
+      *redo_flag = 0u;
+    }
     mbar_init(bar(kBarQ), 1);
     for (int s = 0; s < kNumK; ++s) { mbar_init(bar(kBarKFull + s), 1); mbar_init(bar(kBarKEmpty + s), 1); }
     for (int s = 0; s < kNumV; ++s) { mbar_init(bar(kBarVFull + s), 1); mbar_init(bar(kBarVEmpty + s), 1); }
@@ -200,7 +217,6 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     }
     fence_barrier_init();
   }
-  if (warp == kWarpMmaS) tmem_alloc(smem_u32(tslot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -331,7 +347,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     float nm[kCols], l[kCols];  // -reference (log2 units) and this lane's partial row sums, per column
 #pragma unroll
     for (int c = 0; c < kCols; ++c) { nm[c] = INFINITY; l[c] = 0.f; }
-    bool failed = false;
+    bool failed = false, overflow = false;
     for (int i = 0; i < nblk; ++i) {
       const int sb = i % kNumS, pb = i % kNumP;
       const int ti = 2 * i + key_slot;
@@ -365,7 +381,13 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       for (int c = 0; c < kCols; c += 2) fma_f32x2(t[c], t[c + 1], s[c], s[c + 1], sl2, sl2, nm[c], nm[c + 1]);
       const float mxall = fmax3(fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmax3(t[6], t[7], t[8])),
                                 fmax3(t[9], t[10], t[11]), fmax3(fmax3(t[12], t[13], t[14]), t[15], -INFINITY));
-      if (named_bar_or(bar_id, 128, failed || mxall > kRescaleThreshold)) {
+      bool slow = false;
+      if (exact || i == 0) {
+        slow = named_bar_or(bar_id, 128, failed || mxall > kRescaleThreshold);
+      } else {
+        overflow = overflow || mxall > kFastLimit;  // caught after the item; P stays finite meanwhile
+      }
+      if (slow) {
         if (named_bar_or(bar_id, 128, failed)) { failed = true; break; }
         // slow path: exact block maximum per query column across the 128 key lanes
         float u[kCols];
@@ -428,6 +450,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       }
     }
     // ---- epilogue: out = O / l (+ sigmoid(gate) * coarse on video rows)
+    if (named_bar_or(bar_id, 128, overflow && !failed)) *redo_flag = 1u;  // rerun in exact mode
     if (!named_bar_or(bar_id, 128, failed)) {
       const float lw = reduce_scatter16<false>(l, lane);
       if (lane < kCols) red[(wg * kCols + lane) * 4 + q4] = lw;
@@ -467,7 +490,10 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMmaS) tmem_dealloc(tbase, kTmemCols);
+  if (*redo_flag == 0u) break;  // uniform: read after the barrier by every thread
+  }  // pass
+
+  if (warp == kWarpMmaS) tmem_dealloc(*tslot, kTmemCols);
 }
 
 }  // namespace

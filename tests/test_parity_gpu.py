@@ -16,7 +16,7 @@ import torch
 import block_sparse_video_gb300 as bsv
 from block_sparse_video_gb300.synthetic import CONFIGS, bf16_bits, make_config_inputs, make_inputs
 from oracle import vsa_oracle as vo
-from tests.vsa_parity import assert_errors, compare_head, full_check, run_gpu, to_f64
+from tests.vsa_parity import assert_errors, check_inputs, compare_head, full_check, run_gpu, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -137,3 +137,15 @@ def test_stage_events_time_each_kernel(cuda_ok):
     bsv.vsa_plan_set_stage_events(op.plan, None)
     times = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
     assert all(t > 0 for t in times)
+
+
+@pytest.mark.parametrize("level", [6.0, 16.0])
+def test_large_score_jump_after_first_block(cuda_ok, level):
+    """One video key tile scores far above everything in the first key block
+    (2^94 and 2^261 in softmax units): the fast pass's fixed reference cannot
+    hold it, so the kernel must rerun those items with exact rescaling."""
+    lt, la, lv = 40, 24, 1024
+    q, k, v, g = make_inputs(1, 2, lt, la, lv, 31, device="cuda")
+    q.fill_(1.0)
+    k[:, lt + la + 5 * 64: lt + la + 6 * 64] = level
+    check_inputs(q, k, v, g, lt, la, lv, 0.2, f"score jump {level}")

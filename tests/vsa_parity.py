@@ -103,3 +103,14 @@ def full_check(batch, heads, len_text, len_audio, len_video, keep, seed, device=
     stats = [compare_head(*bits, views, o, b, h, len_text + len_audio, len_video, keep)
              for b in range(batch) for h in range(heads)]
     return assert_errors(stats, f"B{batch} H{heads} {len_text}+{len_audio}+{len_video} f={keep}")
+
+
+def check_inputs(q, k, v, g, len_text, len_audio, len_video, keep, label):
+    """Full parity check on caller-built inputs (small shapes)."""
+    _, out, views = run_gpu(q, k, v, g, len_text, len_audio, len_video, keep)
+    bits = [bf16_bits(x.cpu()) for x in (q, k, v, g)]
+    o = to_f64(out)
+    b_count, _, h_count, _ = q.shape
+    stats = [compare_head(*bits, views, o, b, h, len_text + len_audio, len_video, keep)
+             for b in range(b_count) for h in range(h_count)]
+    return assert_errors(stats, label)
