@@ -55,7 +55,7 @@ constexpr int kNumP = 3;                 // P^T buffers in shared memory
 constexpr uint32_t kColS1 = 64;          // S^T buffer b at column b * kColS1
 constexpr uint32_t kColO = kNumS * kColS1;
 constexpr float kRescaleThreshold = 8.0f;  // exact mode: rescale when P would exceed 2^8
-constexpr float kFastLimit = 60.0f;         // fast mode: P stays below 2^60, far from fp32/bf16 overflow
+constexpr float kFastLimitSum = 18446744073709551616.0f;  // 2^64: fast-pass bound on P (and on each row sum)
 
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
@@ -79,6 +79,7 @@ constexpr int kBarPEmpty = kBarPFull + kNumP;
 constexpr int kNumBars = kBarPEmpty + kNumP;
 static_assert(kNumBars * 8 <= 256, "barrier area");
 static_assert(kColO + 64 <= kTmemCols, "TMEM columns");
+static_assert(kNumS == kNumP, "the softmax loop walks the S^T and P^T rings with one slot counter");
 
 struct FineParams {
   int B, H, P, Lv, N, T, TP, k;
@@ -193,10 +194,10 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
   for (int pass = 0; pass < 2; ++pass) {
   // Pass 0 is the fast mode: after the first block, the per-column softmax
   // reference stays fixed and blocks need no warpgroup vote. It is valid while
-  // no score exceeds the reference by more than 2^kFastLimit (P, the row sums
-  // and O then stay finite, and exact in relative terms). A thread that sees a
-  // larger excess flags the item, and the CTA reruns it in pass 1 with the
-  // exact per-block rescaling.
+  // every P = 2^(score - reference) stays below kFastLimitSum (P, the row sums
+  // and O then stay finite, and exact in relative terms). A thread whose row
+  // sums end at or above that bound flags the item, and the CTA reruns it in
+  // pass 1 with the exact per-block rescaling.
   const bool exact = pass > 0;
   if (tid == 0) {
     if (pass > 0) {
@@ -344,29 +345,39 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     const int video_tail = p.Lv - (p.T - 1) * kTile;
     const bool last_is_ragged =
         video_tail < kTile && (it.list == nullptr || __ldg(it.list + p.k - 1) == p.T - 1);
-    float nm[kCols], l[kCols];  // -reference (log2 units) and this lane's partial row sums, per column
+    // Per column pair: -reference (log2 units) and this lane's partial row sums.
+    float2 nm2[kCols / 2], l2[kCols / 2];
 #pragma unroll
-    for (int c = 0; c < kCols; ++c) { nm[c] = INFINITY; l[c] = 0.f; }
-    bool failed = false, overflow = false;
-    for (int i = 0; i < nblk; ++i) {
-      const int sb = i % kNumS, pb = i % kNumP;
+    for (int j = 0; j < kCols / 2; ++j) {
+      nm2[j] = make_float2(INFINITY, INFINITY);
+      l2[j] = make_float2(0.f, 0.f);
+    }
+    const float2 sl2v = make_float2(sl2, sl2);
+    // Blocks that may hold masked key lanes: the one with the ragged last prefix
+    // tile, and the last block (an absent second tile, or ragged video tile T-1).
+    const int ragged_prefix_blk = (p.TP > 0 && prefix_tail < kTile) ? (p.TP - 1) / 2 : -1;
+    bool failed = false;
+    // ---- general block: masking, and (exact pass or first block) the exact
+    // per-column block maximum with rescaling. st / ph: S^T and P^T ring slot
+    // of block i and its phase parity (the two rings have equal depth).
+    auto general_block = [&](const int i, const int st, const uint32_t ph) {
       const int ti = 2 * i + key_slot;
       bool valid = ti < it.n_kv;
       if (ti == p.TP - 1) valid = key_row < prefix_tail;
       if (ti == it.n_kv - 1 && last_is_ragged) valid = valid && key_row < video_tail;
 
-      failed = warp_any(failed || !mbar_wait(bar(kBarSFull + sb), (i / kNumS) & 1, err, 0x800u));
+      failed = warp_any(failed || !mbar_wait(bar(kBarSFull + st), ph, err, 0x800u));
       float s[kCols];
       if (!failed) {
         tc_fence_after();
         uint32_t raw[kCols];
-        tmem_ld16(tbase + lane_off + sb * kColS1 + col0, raw);
+        tmem_ld16(tbase + lane_off + st * kColS1 + col0, raw);
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < kCols; ++c) s[c] = __uint_as_float(raw[c]);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarSEmpty + sb));
+        if (lane == 0) mbar_arrive(bar(kBarSEmpty + st));
       } else {
 #pragma unroll
         for (int c = 0; c < kCols; ++c) s[c] = 0.f;
@@ -375,20 +386,22 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
 #pragma unroll
         for (int c = 0; c < kCols; ++c) s[c] = -INFINITY;
       }
-      // t = s * log2(e)/sqrt(128) - reference, two columns per instruction
+      // t = s * log2(e)/sqrt(128) - reference
       float t[kCols];
 #pragma unroll
-      for (int c = 0; c < kCols; c += 2) fma_f32x2(t[c], t[c + 1], s[c], s[c + 1], sl2, sl2, nm[c], nm[c + 1]);
-      const float mxall = fmax3(fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmax3(t[6], t[7], t[8])),
-                                fmax3(t[9], t[10], t[11]), fmax3(fmax3(t[12], t[13], t[14]), t[15], -INFINITY));
+      for (int j = 0; j < kCols / 2; ++j) {
+        const float2 tt = __ffma2_rn(make_float2(s[2 * j], s[2 * j + 1]), sl2v, nm2[j]);
+        t[2 * j] = tt.x;
+        t[2 * j + 1] = tt.y;
+      }
       bool slow = false;
       if (exact || i == 0) {
+        const float mxall = fmax3(fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmax3(t[6], t[7], t[8])),
+                                  fmax3(t[9], t[10], t[11]), fmax3(fmax3(t[12], t[13], t[14]), t[15], -INFINITY));
         slow = named_bar_or(bar_id, 128, failed || mxall > kRescaleThreshold);
-      } else {
-        overflow = overflow || mxall > kFastLimit;  // caught after the item; P stays finite meanwhile
       }
       if (slow) {
-        if (named_bar_or(bar_id, 128, failed)) { failed = true; break; }
+        if (named_bar_or(bar_id, 128, failed)) { failed = true; return; }
         // slow path: exact block maximum per query column across the 128 key lanes
         float u[kCols];
 #pragma unroll
@@ -398,21 +411,25 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         named_bar_sync(bar_id, 128);
         float alpha[kCols];
 #pragma unroll
-        for (int c = 0; c < kCols; ++c) {
-          const float4 x = reinterpret_cast<const float4*>(red)[wg * kCols + c];
-          const float bm = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
-          const float nmn = fminf(nm[c], -bm);
-          alpha[c] = ex2_approx(nmn - nm[c]);
-          l[c] *= alpha[c];
-          nm[c] = nmn;
+        for (int j = 0; j < kCols / 2; ++j) {
+          const float4 x0 = reinterpret_cast<const float4*>(red)[wg * kCols + 2 * j];
+          const float4 x1 = reinterpret_cast<const float4*>(red)[wg * kCols + 2 * j + 1];
+          const float bm0 = fmaxf(fmaxf(x0.x, x0.y), fmaxf(x0.z, x0.w));
+          const float bm1 = fmaxf(fmaxf(x1.x, x1.y), fmaxf(x1.z, x1.w));
+          const float n0 = fminf(nm2[j].x, -bm0), n1 = fminf(nm2[j].y, -bm1);
+          alpha[2 * j] = ex2_approx(n0 - nm2[j].x);
+          alpha[2 * j + 1] = ex2_approx(n1 - nm2[j].y);
+          l2[j] = make_float2(l2[j].x * alpha[2 * j], l2[j].y * alpha[2 * j + 1]);
+          nm2[j] = make_float2(n0, n1);
         }
         if (i > 0) {
           // O^T must hold every PV product issued so far: wait for PV of block
           // i-1 on its P-buffer barrier (PV of block i-1-kNumP is already known
           // to be complete, so this parity wait cannot alias an older phase;
           // tcgen05 MMAs complete in issue order).
-          const int pj = i - 1;
-          failed = warp_any(!mbar_wait(bar(kBarPEmpty + pj % kNumP), (pj / kNumP) & 1, err, 0x900u));
+          const int pst = st == 0 ? kNumP - 1 : st - 1;
+          const uint32_t pph = st == 0 ? ph ^ 1u : ph;
+          failed = warp_any(!mbar_wait(bar(kBarPEmpty + pst), pph, err, 0x900u));
           if (!failed) {
             tc_fence_after();
             uint32_t o[kCols];
@@ -426,19 +443,22 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
           }
         }
 #pragma unroll
-        for (int c = 0; c < kCols; c += 2)
-          fma_f32x2(t[c], t[c + 1], s[c], s[c + 1], sl2, sl2, nm[c], nm[c + 1]);
+        for (int j = 0; j < kCols / 2; ++j) {
+          const float2 tt = __ffma2_rn(make_float2(s[2 * j], s[2 * j + 1]), sl2v, nm2[j]);
+          t[2 * j] = tt.x;
+          t[2 * j + 1] = tt.y;
+        }
       }
       uint32_t pk[kCols / 2];
 #pragma unroll
-      for (int c = 0; c < kCols; c += 2) {
-        const float p0 = ex2_approx(t[c]), p1 = ex2_approx(t[c + 1]);
-        add_f32x2(l[c], l[c + 1], l[c], l[c + 1], p0, p1);
-        pk[c / 2] = pack_bf16x2(p0, p1);
+      for (int j = 0; j < kCols / 2; ++j) {
+        const float p0 = ex2_approx(t[2 * j]), p1 = ex2_approx(t[2 * j + 1]);
+        l2[j] = __fadd2_rn(l2[j], make_float2(p0, p1));
+        pk[j] = pack_bf16x2(p0, p1);
       }
-      failed = warp_any(failed || !mbar_wait(bar(kBarPEmpty + pb), ((i / kNumP) & 1) ^ 1, err, 0xA00u));
+      failed = warp_any(failed || !mbar_wait(bar(kBarPEmpty + st), ph ^ 1u, err, 0xA00u));
       if (!failed) {
-        const uint32_t prow = sP + pb * kPBytes + r * 128;
+        const uint32_t prow = sP + st * kPBytes + r * 128;
 #pragma unroll
         for (int cc = 0; cc < kCols / 8; ++cc) {
           const uint32_t chunk = static_cast<uint32_t>((col0 / 8 + cc) ^ (r & 7));
@@ -446,8 +466,72 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarPFull + pb));
+        if (lane == 0) mbar_arrive(bar(kBarPFull + st));
       }
+    };
+    // ---- fast-pass block: no masked lanes, fixed reference, no cross-lane work.
+    // Returns false once a wait has failed.
+    auto fast_block = [&](const int st, const uint32_t ph) -> bool {
+      if (warp_any(!mbar_wait(bar(kBarSFull + st), ph, err, 0x800u))) return false;
+      tc_fence_after();
+      uint32_t raw[kCols];
+      tmem_ld16(tbase + lane_off + st * kColS1 + col0, raw);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarSEmpty + st));
+      uint32_t pk[kCols / 2];
+#pragma unroll
+      for (int j = 0; j < kCols / 2; ++j) {
+        const float2 t = __ffma2_rn(make_float2(__uint_as_float(raw[2 * j]), __uint_as_float(raw[2 * j + 1])),
+                                    sl2v, nm2[j]);
+        const float p0 = ex2_approx(t.x), p1 = ex2_approx(t.y);
+        l2[j] = __fadd2_rn(l2[j], make_float2(p0, p1));
+        pk[j] = pack_bf16x2(p0, p1);
+      }
+      if (warp_any(!mbar_wait(bar(kBarPEmpty + st), ph ^ 1u, err, 0xA00u))) return false;
+      const uint32_t prow = sP + st * kPBytes + r * 128;
+#pragma unroll
+      for (int cc = 0; cc < kCols / 8; ++cc) {
+        const uint32_t chunk = static_cast<uint32_t>((col0 / 8 + cc) ^ (r & 7));
+        st_shared_v4(prow + chunk * 16, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarPFull + st));
+      return true;
+    };
+    if (exact) {
+      for (int i = 0; i < nblk && !failed; ++i) general_block(i, i % kNumS, (i / kNumS) & 1);
+    } else {
+      general_block(0, 0, 0u);
+      // fast blocks 1 .. nblk-2, the ragged-prefix block (if any) excepted
+      int st = 1 % kNumS;
+      uint32_t ph = 0;
+      for (int i = 1; i < nblk - 1 && !failed; ++i) {
+        if (i == ragged_prefix_blk) {
+          general_block(i, st, ph);
+        } else if (!fast_block(st, ph)) {
+          failed = true;
+        }
+        if (++st == kNumS) { st = 0; ph ^= 1u; }
+      }
+      if (nblk > 1 && !failed) general_block(nblk - 1, (nblk - 1) % kNumS, ((nblk - 1) / kNumS) & 1);
+    }
+    // The fast pass is valid while every P stayed below 2^kFastLimit: P >= 0, so
+    // one larger P (or an overflow to inf) leaves a partial row sum at or above
+    // that bound (a NaN fails the comparison too).
+    bool overflow = false;
+    if (!exact) {
+#pragma unroll
+      for (int j = 0; j < kCols / 2; ++j)
+        overflow = overflow || !(l2[j].x < kFastLimitSum) || !(l2[j].y < kFastLimitSum);
+    }
+    float l[kCols];
+#pragma unroll
+    for (int j = 0; j < kCols / 2; ++j) {
+      l[2 * j] = l2[j].x;
+      l[2 * j + 1] = l2[j].y;
     }
     // ---- epilogue: out = O / l (+ sigmoid(gate) * coarse on video rows)
     if (named_bar_or(bar_id, 128, overflow && !failed)) *redo_flag = 1u;  // rerun in exact mode
