@@ -501,8 +501,29 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       if (lane == 0) mbar_arrive(bar(kBarPFull + st));
       return true;
     };
+    // The epilogue's gate and coarse inputs come from HBM: all of them are
+    // requested together, right after the last block, so that their latency
+    // overlaps the drain of the last O^T product (loading them inside the store
+    // loop serialised one HBM round trip per column).
+    const size_t row_stride = static_cast<size_t>(p.H) * kHeadDim;
+    const size_t out_base = (static_cast<size_t>(it.b) * p.N + it.q_row0) * row_stride +
+                            static_cast<size_t>(it.h) * kHeadDim + r;
+    float gv[kCols];
+    float cz = 0.f;
+    auto prefetch_gate = [&]() {
+#pragma unroll
+      for (int c = 0; c < kCols; ++c) gv[c] = 0.f;
+      if (it.video) {
+        cz = __ldg(p.coarse + ((static_cast<size_t>(it.b) * p.H + it.h) * p.T + it.t) * kHeadDim + r);
+#pragma unroll
+        for (int c = 0; c < kCols; ++c)
+          if (col0 + c < it.q_valid)
+            gv[c] = __bfloat162float(__ldg(p.gate + out_base + static_cast<size_t>(col0 + c) * row_stride));
+      }
+    };
     if (exact) {
       for (int i = 0; i < nblk && !failed; ++i) general_block(i, i % kNumS, (i / kNumS) & 1);
+      prefetch_gate();
     } else {
       general_block(0, 0, 0u);
       // fast blocks 1 .. nblk-2, the ragged-prefix block (if any) excepted
@@ -517,6 +538,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         if (++st == kNumS) { st = 0; ph ^= 1u; }
       }
       if (nblk > 1 && !failed) general_block(nblk - 1, (nblk - 1) % kNumS, ((nblk - 1) / kNumS) & 1);
+      prefetch_gate();
     }
     // The fast pass is valid while every P stayed below 2^kFastLimit: P >= 0, so
     // one larger P (or an overflow to inf) leaves a partial row sum at or above
@@ -546,13 +568,6 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         uint32_t o[kCols];
         tmem_ld16(tbase + lane_off + kColO + col0, o);
         tmem_wait_ld();
-        const int d = r;
-        float cz = 0.f;
-        if (it.video)
-          cz = __ldg(p.coarse + ((static_cast<size_t>(it.b) * p.H + it.h) * p.T + it.t) * kHeadDim + d);
-        const size_t row_stride = static_cast<size_t>(p.H) * kHeadDim;
-        const size_t base = (static_cast<size_t>(it.b) * p.N + it.q_row0) * row_stride +
-                            static_cast<size_t>(it.h) * kHeadDim + d;
 #pragma unroll
         for (int c = 0; c < kCols; ++c) {
           const int qc = col0 + c;
@@ -560,12 +575,8 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             const float4 x = reinterpret_cast<const float4*>(red)[wg * kCols + c];
             const float lsum = (x.x + x.y) + (x.z + x.w);
             float val = __fdividef(__uint_as_float(o[c]), lsum);
-            const size_t off = base + static_cast<size_t>(qc) * row_stride;
-            if (it.video) {
-              const float g = __bfloat162float(p.gate[off]);
-              val += __fdividef(cz, 1.0f + __expf(-g));
-            }
-            p.out[off] = __float2bfloat16_rn(val);
+            if (it.video) val += __fdividef(cz, 1.0f + __expf(-gv[c]));
+            p.out[out_base + static_cast<size_t>(qc) * row_stride] = __float2bfloat16_rn(val);
           }
         }
       }
