@@ -83,7 +83,6 @@ static_assert(kNumS == kNumP, "the softmax loop walks the S^T and P^T rings with
 
 struct FineParams {
   int B, H, P, Lv, N, T, TP, k;
-  int n_prefix_items;
   float scale_log2;
   const __nv_bfloat16* gate;
   __nv_bfloat16* out;
@@ -100,43 +99,33 @@ struct Item {
   const int32_t* list;  // selected video tiles, or null: every video tile in order
 };
 
+// Items are ordered head by head: for each (batch, head), its TP prefix query
+// tiles (the long, dense items) and then its T video query tiles. The CTAs in
+// flight at any time then read the K/V of one or two heads, which stay resident
+// in L2; taking all prefix items first would stream every head's K/V at once.
 __device__ __forceinline__ Item decode_item(const FineParams& p, int item) {
   Item it;
-  if (item < p.n_prefix_items) {
+  const int per_head = p.TP + p.T;
+  const int bh = item / per_head;
+  const int local = item - bh * per_head;
+  it.b = bh / p.H;
+  it.h = bh - it.b * p.H;
+  if (local < p.TP) {
     it.video = false;
-    it.b = item / (p.H * p.TP);
-    const int rem = item % (p.H * p.TP);
-    it.h = rem / p.TP;
-    it.t = rem % p.TP;
+    it.t = local;
     it.q_row0 = it.t * kTile;
     it.q_valid = min(kTile, p.P - it.q_row0);
     it.n_kv = p.TP + p.T;
     it.list = nullptr;
   } else {
-    const int v = item - p.n_prefix_items;
     it.video = true;
-    it.b = v / (p.H * p.T);
-    const int rem = v % (p.H * p.T);
-    it.h = rem / p.T;
-    it.t = rem % p.T;
+    it.t = local - p.TP;
     it.q_row0 = p.P + it.t * kTile;
     it.q_valid = min(kTile, p.Lv - it.t * kTile);
     it.n_kv = p.TP + p.k;
     it.list = p.tile_index + ((static_cast<size_t>(it.b) * p.H + it.h) * p.T + it.t) * p.k;
   }
   return it;
-}
-
-// Valid keys of key tile `ti` of an item whose video tile id is `jv`.
-__device__ __forceinline__ int kv_tile_len(const FineParams& p, const Item& it, int ti, int jv) {
-  if (ti >= it.n_kv) return 0;
-  if (ti < p.TP) return min(kTile, p.P - ti * kTile);
-  return min(kTile, p.Lv - jv * kTile);
-}
-
-__device__ __forceinline__ int kv_tile_id(const Item& it, int tp, int ti) {
-  if (ti < tp || ti >= it.n_kv) return 0;
-  return it.list ? __ldg(it.list + (ti - tp)) : ti - tp;
 }
 
 // One halving step of the warp reduce-scatter: lanes with bit O set keep the
@@ -599,7 +588,6 @@ cudaError_t launch_fine(const Geometry& g, const CUtensorMap& map_q, const CUten
                         const CUtensorMap& map_v, const FineArgs& a, cudaStream_t stream) {
   FineParams p;
   p.B = g.B; p.H = g.H; p.P = g.P; p.Lv = g.Lv; p.N = g.N; p.T = g.T; p.TP = g.TP; p.k = g.k;
-  p.n_prefix_items = g.B * g.H * g.TP;
   p.scale_log2 = 1.4426950408889634f * 0.08838834764831845f;
   p.gate = a.gate;
   p.out = a.out;
