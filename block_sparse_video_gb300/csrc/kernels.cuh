@@ -38,15 +38,21 @@ cudaError_t launch_coarse_topk(const Geometry& g, const float* pooled_q, const f
 // Fine attention: prefix query tiles over every key, video query tiles over
 // the prefix plus their selected video tiles; epilogue adds sigmoid(gate) *
 // coarse on video rows and writes bf16 out.
+// Launches two persistent kernels of num_sms CTAs (at most one per item): the
+// fast one over every item, then the exact one over the items the fast one
+// appended to the redo list.
 struct FineArgs {
   const __nv_bfloat16* gate;
   __nv_bfloat16* out;
   const float* coarse;
   const int32_t* tile_index;
-  unsigned int* err;  // 3 error words in the workspace
+  unsigned int* err;   // 3 error words in the workspace
+  int* redo_count;     // zero before the launch
+  int* redo_list;      // int32 [B * H * (TP + T)]
+  int* work_counters;  // 2 counters, zero before the launch
 };
 size_t fine_smem_bytes();
 cudaError_t launch_fine(const Geometry& g, const CUtensorMap& map_q, const CUtensorMap& map_k,
-                        const CUtensorMap& map_v, const FineArgs& a, cudaStream_t stream);
+                        const CUtensorMap& map_v, const FineArgs& a, int num_sms, cudaStream_t stream);
 
 }  // namespace vsa

@@ -10,7 +10,8 @@ struct vsa_plan {
   vsa_shape_t shape;
   int device;
   vsa::Geometry g;
-  size_t off_err, off_pq, off_pk, off_pv, off_coarse, off_idx, ws_bytes;
+  size_t off_err, off_pq, off_pk, off_pv, off_coarse, off_idx, off_redo, ws_bytes;
+  int num_sms;          // SM count of `device`, read on the first forward
   size_t tensor_bytes;  // one bf16 [B, N, H, 128] tensor
   cudaEvent_t events[4];
   bool have_events;

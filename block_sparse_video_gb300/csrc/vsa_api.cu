@@ -141,6 +141,7 @@ vsa_status_t vsa_plan_create(const vsa_shape_t* shape, int device, vsa_plan_t* o
   p->off_pv = off;   off += align_up(pooled);
   p->off_coarse = off; off += align_up(pooled);
   p->off_idx = off;  off += align_up(idx);
+  p->off_redo = off; off += align_up(static_cast<size_t>(g.B) * g.H * (g.TP + g.T) * sizeof(int32_t));
   p->ws_bytes = off;
   p->tensor_bytes = static_cast<size_t>(g.B) * g.N * g.H * vsa::kHeadDim * 2;
   *out = p;
@@ -198,7 +199,11 @@ vsa_status_t vsa_forward(vsa_plan_t plan, const void* q, const void* k, const vo
   float* coarse = reinterpret_cast<float*>(ws + plan->off_coarse);
   int32_t* idx = reinterpret_cast<int32_t*>(ws + plan->off_idx);
 
-  if (cudaMemsetAsync(err, 0, 16, st) != cudaSuccess) return VSA_ERR_CUDA;
+  if (plan->num_sms == 0 &&
+      cudaDeviceGetAttribute(&plan->num_sms, cudaDevAttrMultiProcessorCount, plan->device) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  // error words 0-2, redo count (word 4), the fine kernels' work counters (words 5, 6)
+  if (cudaMemsetAsync(err, 0, 32, st) != cudaSuccess) return VSA_ERR_CUDA;
   vsa_status_t rs = record(plan, 0, st);
   if (rs != VSA_OK) return rs;
   if (vsa::launch_pool(g, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
@@ -213,7 +218,10 @@ vsa_status_t vsa_forward(vsa_plan_t plan, const void* q, const void* k, const vo
   a.coarse = coarse;
   a.tile_index = idx;
   a.err = err;
-  if (vsa::launch_fine(g, mq, mk, mv, a, st) != cudaSuccess) return VSA_ERR_CUDA;
+  a.redo_count = reinterpret_cast<int*>(err + 4);
+  a.redo_list = reinterpret_cast<int32_t*>(ws + plan->off_redo);
+  a.work_counters = reinterpret_cast<int*>(err + 5);
+  if (vsa::launch_fine(g, mq, mk, mv, a, plan->num_sms, st) != cudaSuccess) return VSA_ERR_CUDA;
   return record(plan, 3, st);
 }
 
