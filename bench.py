@@ -57,7 +57,9 @@ def workload_config(cfg=None, keep=None):
                      f"({t} tiles of 64, k={k}, keep {keep})"),
         "batch": cfg.batch, "heads": cfg.heads, "head_dim": 128, "len_text": cfg.len_text,
         "len_audio": cfg.len_audio, "len_video": cfg.len_video, "video_tiles": t, "kept_tiles": k,
-        "seed": cfg.seed, "l2": "flushed between timed steps (512 MB write); inputs 4.3 GB > L2",
+        "seed": cfg.seed,
+        "l2": (f"flushed between timed steps (512 MB write); inputs "
+               f"{4 * cfg.batch * (cfg.prefix + cfg.len_video) * cfg.heads * 128 * 2 / 1e9:.2f} GB"),
         "parallelism": "one full problem per GPU (weak scaling)",
     }
 
@@ -84,6 +86,24 @@ def effective_flops(cfg=None, keep=None, tile_index=None):
     fine = 4 * d * (video_pairs + prefix_pairs)
     coarse = 4 * d * t * t * cfg.batch * cfg.heads
     return {"fine": float(fine), "coarse": float(coarse), "total": float(fine + coarse)}
+
+
+def kv_stream_bytes(cfg=None, keep=None):
+    """K and V bytes the fine kernel moves from L2 into shared memory: every
+    item (64-query tile) loads its key tiles in 128-key blocks (an odd count is
+    padded with an all-zero tile that is loaded too)."""
+    cfg = CFG if cfg is None else cfg
+    keep = cfg.keep[0] if keep is None else keep
+    t = cfg.n_video_tiles
+    tp = -(-cfg.prefix // 64)
+    k = max(1, min(t, int(np.floor(keep * t + 0.5))))
+    blocks = cfg.batch * cfg.heads * (t * ((tp + k + 1) // 2) + tp * ((tp + t + 1) // 2))
+    return float(blocks * 2 * 128 * 128 * 2)
+
+
+# kernels launched by one forward: tile pool, coarse attention + top-k, the
+# fine-attention fast kernel and its exact redo pass
+LAUNCHES_PER_FORWARD = 4
 
 
 def pool_bytes(cfg=None):
@@ -366,11 +386,13 @@ def run_ours(args):
                                 "frac_of_hbm": pool_gbs / peaks["hbm_gbs"]},
                 "coarse_topk_kernel": {"ms": coarse_ms, "flops": fl["coarse"],
                                        "TFLOP_s": fl["coarse"] / (coarse_ms * 1e-3) / 1e12},
-                "fine_attn_kernel": {"ms": fine_ms, "flops": fl["fine"], "TFLOP_s": fine_tflops},
+                "fine_attn_kernel": {"ms": fine_ms, "flops": fl["fine"], "TFLOP_s": fine_tflops,
+                                     "kv_l2_to_smem_bytes": kv_stream_bytes(cfg, keep),
+                                     "kv_l2_to_smem_TB_s": kv_stream_bytes(cfg, keep) / (fine_ms * 1e-3) / 1e12},
             },
             "clocks": clocks,
             "e2e": e2e,
-            "gpu_launches": 3 * steps,
+            "gpu_launches": LAUNCHES_PER_FORWARD * steps,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line))

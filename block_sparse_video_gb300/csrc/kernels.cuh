@@ -1,4 +1,4 @@
-// Internal interface between the C-ABI host code and the three kernels.
+// Internal interface between the C-ABI host code and the kernels.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
