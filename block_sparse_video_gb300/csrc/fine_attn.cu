@@ -38,8 +38,9 @@
 // four lanes each issuing one 8 KB box; warp 1 owns TMEM, loads Q (one buffer,
 // reloaded once the item's last S^T product has completed) and issues the S^T
 // products, warp 18 the O^T products (two TMEM accumulators, alternating by
-// item); warps 2-17 are four softmax warpgroups (16 query columns each) that
-// also run the epilogue. Every wait is bounded (see ptx.cuh); a named barrier
+// item), each MMA warp converged with one elected lane issuing; warps 2-17
+// are four softmax warpgroups (16 query columns each) that also run the
+// epilogue. Every wait is bounded (see ptx.cuh); a named barrier
 // is always reached by all of its threads.
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -332,91 +333,85 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     }
   } else if (warp == kWarpMmaS) {
     // ------------------------------------------------------------ Q loads, S^T = K Q^T issuer
+    // The whole warp runs the loop (warp-uniform descriptors); one elected lane
+    // issues the products and commits, lane 0 the Q loads.
     bool ok = true;
     int item = read_item(0, ok);
-    if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
-      const uint64_t dk0 = smem_desc_sw128(sK, 16, 1024);
-      const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
-      auto load_q = [&](int itm) {
+    const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
+    const uint64_t dk0 = smem_desc_sw128(sK, 16, 1024);
+    const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
+    auto load_q = [&](int itm) {
+      if (lane == 0) {
         const Item qi = decode_item(p, itm);
         mbar_arrive_expect_tx(bar(kBarQFull), kQBytes);
         for (int c = 0; c < 2; ++c)
           tma_load_4d(sQ + c * 8192, &map_q, 64 * c, qi.h, qi.q_row0, qi.b, bar(kBarQFull));
-      };
-      if (ok && item >= 0) load_q(item);
-      uint32_t g = 0;  // blocks issued so far, over all items
-      for (int n = 0; ok && item >= 0; ++n) {
-        const Item it = decode_item(p, item);
-        const int nblk = (it.n_kv + 1) / 2;
-        ok = mbar_wait(bar(kBarQFull), n & 1, err, 0x500u, 64);
-        for (int i = 0; i < nblk && ok; ++i, ++g) {
-          const int ks = g % kNumK, sb = g % kNumS;
-          ok = mbar_wait(bar(kBarKFull + ks), (g / kNumK) & 1, err, 0x600u, 64) &&
-               mbar_wait(bar(kBarSEmpty + sb), ((g / kNumS) & 1) ^ 1, err, 0x700u, 64);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t dk = dk0 + ((ks * kKVBytes) >> 4);
+      }
+      __syncwarp();
+    };
+    if (ok && item >= 0) load_q(item);
+    uint32_t g = 0;  // blocks issued so far, over all items
+    for (int n = 0; ok && item >= 0; ++n) {
+      const Item it = decode_item(p, item);
+      const int nblk = (it.n_kv + 1) / 2;
+      ok = mbar_wait_warp(bar(kBarQFull), n & 1, err, 0x500u, 64);
+      for (int i = 0; i < nblk && ok; ++i, ++g) {
+        const int ks = g % kNumK, sb = g % kNumS;
+        ok = mbar_wait_warp(bar(kBarKFull + ks), (g / kNumK) & 1, err, 0x600u, 64) &&
+             mbar_wait_warp(bar(kBarSEmpty + sb), ((g / kNumS) & 1) ^ 1, err, 0x700u, 64);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t dk = dk0 + ((ks * kKVBytes) >> 4);
 #pragma unroll
-          for (int s = 0; s < 8; ++s) {
-            const uint32_t koff = ((s >> 2) * 16384 + (s & 3) * 32) >> 4;
-            const uint32_t qoff = ((s >> 2) * 8192 + (s & 3) * 32) >> 4;
-            umma_bf16(tbase + sb * kColS1, dk + koff, dq0 + qoff, id_s, s > 0 ? 1u : 0u);
-          }
-          umma_commit(bar(kBarKEmpty + ks));
-          umma_commit(bar(kBarSFull + sb));
+        for (int s = 0; s < 8; ++s) {
+          const uint32_t koff = ((s >> 2) * 16384 + (s & 3) * 32) >> 4;
+          const uint32_t qoff = ((s >> 2) * 8192 + (s & 3) * 32) >> 4;
+          umma_bf16_elect(tbase + sb * kColS1, dk + koff, dq0 + qoff, id_s, s > 0 ? 1u : 0u);
         }
-        if (!ok) break;
-        // Q stays in use until the item's last S^T product completes
-        umma_commit(bar(kBarQEmpty));
-        // next item (lane 0 only here: the ring read is done by hand)
-        const int s = (n + 1) % kItemSlots;
-        ok = mbar_wait(bar(kBarItemFull + s), ((n + 1) / kItemSlots) & 1, err, 0xC00u, 64);
-        if (!ok) break;
-        item = items[s];
-        mbar_arrive(bar(kBarItemEmpty + s));
-        if (item >= 0) {
-          ok = mbar_wait(bar(kBarQEmpty), n & 1, err, 0x510u, 64);
-          if (ok) load_q(item);
-        }
+        umma_commit_elect(bar(kBarKEmpty + ks));
+        umma_commit_elect(bar(kBarSFull + sb));
+      }
+      if (!ok) break;
+      // Q stays in use until the item's last S^T product completes
+      umma_commit_elect(bar(kBarQEmpty));
+      item = read_item(n + 1, ok);
+      if (ok && item >= 0) {
+        ok = mbar_wait_warp(bar(kBarQEmpty), n & 1, err, 0x510u, 64);
+        if (ok) load_q(item);
       }
     }
-    __syncwarp();
   } else if (warp == kWarpMmaPV) {
     // ------------------------------------------------------------ O^T += V^T P^T issuer
+    // converged warp, elected lane issues (as for S^T)
     bool ok = true;
     uint32_t g = 0;  // blocks issued so far, over all items
+    const uint32_t id_o = idesc_bf16_f32(128, 64, 1, 1);
+    const uint64_t dv0 = smem_desc_sw128(sV, 16384, 1024);
+    const uint64_t dp0 = smem_desc_sw128(sP, 8192, 1024);
     for (int n = 0; ok; ++n) {
       const int item = read_item(n, ok);
       if (!ok || item < 0) break;
-      if (lane == 0) {
-        const Item it = decode_item(p, item);
-        const int nblk = (it.n_kv + 1) / 2;
-        const uint32_t ob = n % kNumO;
-        // accumulator ob was last read by the epilogue of item n - kNumO
-        if (n >= kNumO) ok = mbar_wait(bar(kBarOEmpty + ob), ((n - kNumO) / kNumO) & 1, err, 0x310u, 32);
-        const uint32_t id_o = idesc_bf16_f32(128, 64, 1, 1);
-        const uint64_t dv0 = smem_desc_sw128(sV, 16384, 1024);
-        const uint64_t dp0 = smem_desc_sw128(sP, 8192, 1024);
-        for (int j = 0; j < nblk && ok; ++j, ++g) {
-          const int vs = g % kNumV, pb = g % kNumP;
-          ok = mbar_wait(bar(kBarVFull + vs), (g / kNumV) & 1, err, 0x300u, 32) &&
-               mbar_wait(bar(kBarPFull + pb), (g / kNumP) & 1, err, 0x400u, 32);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t dv = dv0 + ((vs * kKVBytes) >> 4);
-          const uint64_t dp = dp0 + ((pb * kPBytes) >> 4);
+      const Item it = decode_item(p, item);
+      const int nblk = (it.n_kv + 1) / 2;
+      const uint32_t ob = n % kNumO;
+      // accumulator ob was last read by the epilogue of item n - kNumO
+      if (n >= kNumO) ok = mbar_wait_warp(bar(kBarOEmpty + ob), ((n - kNumO) / kNumO) & 1, err, 0x310u, 32);
+      for (int j = 0; j < nblk && ok; ++j, ++g) {
+        const int vs = g % kNumV, pb = g % kNumP;
+        ok = mbar_wait_warp(bar(kBarVFull + vs), (g / kNumV) & 1, err, 0x300u, 32) &&
+             mbar_wait_warp(bar(kBarPFull + pb), (g / kNumP) & 1, err, 0x400u, 32);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t dv = dv0 + ((vs * kKVBytes) >> 4);
+        const uint64_t dp = dp0 + ((pb * kPBytes) >> 4);
 #pragma unroll
-          for (int s = 0; s < 8; ++s)
-            umma_bf16(tbase + kColO + ob * 64, dv + ((s * 2048) >> 4), dp + ((s * 2048) >> 4), id_o,
-                      (j > 0 || s > 0) ? 1u : 0u);
-          umma_commit(bar(kBarVEmpty + vs));
-          umma_commit(bar(kBarPEmpty + pb));
-        }
+        for (int s = 0; s < 8; ++s)
+          umma_bf16_elect(tbase + kColO + ob * 64, dv + ((s * 2048) >> 4), dp + ((s * 2048) >> 4), id_o,
+                          (j > 0 || s > 0) ? 1u : 0u);
+        umma_commit_elect(bar(kBarVEmpty + vs));
+        umma_commit_elect(bar(kBarPEmpty + pb));
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
     }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     const int wg = (warp - kWarpSoftmax0) / 4;  // query columns kCols*wg .. kCols*wg + kCols-1

@@ -119,6 +119,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
   }
 }
 
+// mbar_wait for a converged warp: one warp-wide test on the fast path; when the
+// phase is not complete yet, every lane runs the bounded wait and the warp
+// agrees on the outcome (false if any lane gave up).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, unsigned int* err,
+                                               unsigned int detail, uint32_t sleep_ns = 0) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const bool ok = mbar_wait(bar, parity, err, detail, sleep_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- async proxy
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -195,10 +205,35 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// The same product issued from a converged warp: elect.sync picks one lane
+// (the lowest, so always the same lane of a full warp) inside the asm block.
+// Keeping the issuing loop warp-uniform keeps its descriptor arithmetic in
+// uniform registers: measured on GB300, a loop of these issues one M=128, N=64
+// MMA per ~49 cycles (the tensor pipe's rate) where the same loop run by lane 0
+// alone needs ~110.
+__device__ __forceinline__ void umma_bf16_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Make `bar` track completion of every tcgen05 op this thread issued so far.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// umma_commit from a converged warp, by the lane elect.sync picks (the lane
+// umma_bf16_elect issues from).
+__device__ __forceinline__ void umma_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar)
       : "memory");
 }
 
