@@ -189,7 +189,8 @@ __device__ __forceinline__ bool warp_any(bool x) { return __any_sync(0xffffffffu
 template <bool kExact>
 __global__ void __launch_bounds__(kThreads, 1)
 fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                 const __grid_constant__ CUtensorMap map_v, const FineParams p) {
+                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_g,
+                 const FineParams p) {
   const int n_work = kExact ? *reinterpret_cast<const volatile int*>(p.redo_count) : p.n_items;
   if (n_work <= 0) return;  // uniform: nothing to do (the exact kernel's usual case)
 
@@ -295,6 +296,19 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       if (!ok || item < 0) break;
       const Item it = decode_item(p, item);
       const int nblk = (it.n_kv + 1) / 2;
+      if (!v_warp && lane == 0) {
+        // Into L2 ahead of use: the item's Q tile (loaded once its S^T products
+        // start) and, for a video item, its gate tile and coarse row (read by
+        // the epilogue, an item's duration later).
+        tma_prefetch_l2_4d(&map_q, 0, it.h, it.q_row0, it.b);
+        tma_prefetch_l2_4d(&map_q, 64, it.h, it.q_row0, it.b);
+        if (it.video) {
+          tma_prefetch_l2_4d(&map_g, 0, it.h, it.q_row0, it.b);
+          tma_prefetch_l2_4d(&map_g, 64, it.h, it.q_row0, it.b);
+          bulk_prefetch_l2(p.coarse + ((static_cast<size_t>(it.b) * p.H + it.h) * p.T + it.t) * kHeadDim,
+                           kHeadDim * sizeof(float));
+        }
+      }
       // window of 32 selected tile ids (video items), prefetched one window ahead
       int wbase = 0;
       int win = 0, win_next = 0;
@@ -599,10 +613,9 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         if (lane == 0) mbar_arrive(bar(kBarPFull + pt));
         return true;
       };
-      // The epilogue's gate and coarse inputs come from HBM: all of them are
-      // requested together, right after the last block, so that their latency
-      // overlaps the drain of the last O^T product (loading them inside the store
-      // loop serialised one HBM round trip per column).
+      // The epilogue's gate and coarse inputs were prefetched into L2 when the
+      // item was fetched; all of them are requested together (loading them
+      // inside the store loop serialised one round trip per column).
       const size_t out_base = (static_cast<size_t>(it.b) * p.N + it.q_row0) * row_stride +
                               static_cast<size_t>(it.h) * kHeadDim + r;
       float gv[kCols];
@@ -641,7 +654,6 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         }
         if (nblk > 1 && !failed) general_block(nblk - 1, gs + nblk - 1);
       }
-      prefetch_gate();
       // The fast mode is valid while every P stayed below kFastLimitSum: P >= 0,
       // so one larger P (or an overflow to inf) leaves a partial row sum at or
       // above that bound (a NaN fails the comparison too).
@@ -666,6 +678,9 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       const float lw = reduce_scatter16<false>(l, lane);
       if (lane < kCols) red[(wg * kCols + lane) * 4 + q4] = lw;
       named_bar_sync(bar_id, 128);
+      // after the named barriers (which wait for a warp's outstanding loads),
+      // so that these L2 reads overlap the drain of the last O^T product
+      prefetch_gate();
       const uint32_t gl = gs + nblk - 1;  // the item's last PV product (see the rescale above)
       failed = warp_any(!mbar_wait(bar(kBarPEmpty + gl % kNumP), (gl / kNumP) & 1, err, 0xB00u));
       if (!failed) {
@@ -704,7 +719,8 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
 size_t fine_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_fine(const Geometry& g, const CUtensorMap& map_q, const CUtensorMap& map_k,
-                        const CUtensorMap& map_v, const FineArgs& a, int num_sms, cudaStream_t stream) {
+                        const CUtensorMap& map_v, const CUtensorMap& map_gate, const FineArgs& a, int num_sms,
+                        cudaStream_t stream) {
   FineParams p;
   p.B = g.B; p.H = g.H; p.P = g.P; p.Lv = g.Lv; p.N = g.N; p.T = g.T; p.TP = g.TP; p.k = g.k;
   p.n_items = g.B * g.H * (g.TP + g.T);
@@ -724,12 +740,12 @@ cudaError_t launch_fine(const Geometry& g, const CUtensorMap& map_q, const CUten
                            static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   p.work_counter = a.work_counters;
-  fine_attn_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(map_q, map_k, map_v, p);
+  fine_attn_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(map_q, map_k, map_v, map_gate, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // Items whose fast-mode softmax left its range: recomputed with exact
   // rescaling (an empty list costs one launch whose CTAs return at once).
   p.work_counter = a.work_counters + 1;
-  fine_attn_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(map_q, map_k, map_v, p);
+  fine_attn_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(map_q, map_k, map_v, map_gate, p);
   return cudaGetLastError();
 }
 

@@ -53,6 +53,7 @@ struct FineArgs {
 };
 size_t fine_smem_bytes();
 cudaError_t launch_fine(const Geometry& g, const CUtensorMap& map_q, const CUtensorMap& map_k,
-                        const CUtensorMap& map_v, const FineArgs& a, int num_sms, cudaStream_t stream);
+                        const CUtensorMap& map_v, const CUtensorMap& map_gate, const FineArgs& a, int num_sms,
+                        cudaStream_t stream);
 
 }  // namespace vsa

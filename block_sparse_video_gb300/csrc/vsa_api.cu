@@ -187,8 +187,9 @@ vsa_status_t vsa_forward(vsa_plan_t plan, const void* q, const void* k, const vo
   DeviceGuard guard(plan->device);
   if (!guard.ok) return VSA_ERR_CUDA;
   const vsa::Geometry& g = plan->g;
-  CUtensorMap mq, mk, mv;
-  if (!encode_bnhd(&mq, q, g) || !encode_bnhd(&mk, k, g) || !encode_bnhd(&mv, v, g))
+  CUtensorMap mq, mk, mv, mg;
+  if (!encode_bnhd(&mq, q, g) || !encode_bnhd(&mk, k, g) || !encode_bnhd(&mv, v, g) ||
+      !encode_bnhd(&mg, gate, g))
     return VSA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -221,7 +222,7 @@ vsa_status_t vsa_forward(vsa_plan_t plan, const void* q, const void* k, const vo
   a.redo_count = reinterpret_cast<int*>(err + 4);
   a.redo_list = reinterpret_cast<int32_t*>(ws + plan->off_redo);
   a.work_counters = reinterpret_cast<int*>(err + 5);
-  if (vsa::launch_fine(g, mq, mk, mv, a, plan->num_sms, st) != cudaSuccess) return VSA_ERR_CUDA;
+  if (vsa::launch_fine(g, mq, mk, mv, mg, a, plan->num_sms, st) != cudaSuccess) return VSA_ERR_CUDA;
   return record(plan, 3, st);
 }
 
