@@ -309,31 +309,24 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                            kHeadDim * sizeof(float));
         }
       }
-      // window of 32 selected tile ids (video items), prefetched one window ahead
-      int wbase = 0;
-      int win = 0, win_next = 0;
-      if (it.list) {
-        win = lane < p.k ? __ldg(it.list + lane) : 0;
-        win_next = 32 + lane < p.k ? __ldg(it.list + 32 + lane) : 0;
-      }
+      // Token row of key tile ti of this item (p.N for an absent tile: the TMA
+      // box is then fully out of bounds and reads as zeros).
       auto tile_row = [&](int ti) -> int {
-        if (ti >= it.n_kv) return p.N;  // absent: fully out of bounds, TMA fills zeros
+        if (ti >= it.n_kv) return p.N;
         if (ti < p.TP) return ti * kTile;
-        const int pos = ti - p.TP;
-        int j = pos;
-        if (it.list) {
-          while (pos >= wbase + 32) {
-            wbase += 32;
-            win = win_next;
-            win_next = wbase + 32 + lane < p.k ? __ldg(it.list + wbase + 32 + lane) : 0;
-          }
-          j = __shfl_sync(0xffffffffu, win, pos - wbase);
-        }
-        return p.P + j * kTile;
+        return p.P + (it.list ? __ldg(it.list + (ti - p.TP)) : ti - p.TP) * kTile;
       };
+      // Rows are worked out 32 blocks at a time, lane l taking block base + l,
+      // so that each block only needs two shuffles here (this warp's loop is on
+      // the critical path).
+      int row_a = 0, row_b = 0;
       for (int blk = 0; blk < nblk; ++blk, ++g) {
-        const int ra = tile_row(2 * blk);
-        const int rb = tile_row(2 * blk + 1);
+        if ((blk & 31) == 0) {
+          row_a = tile_row(2 * (blk + lane));
+          row_b = tile_row(2 * (blk + lane) + 1);
+        }
+        const int ra = __shfl_sync(0xffffffffu, row_a, blk & 31);
+        const int rb = __shfl_sync(0xffffffffu, row_b, blk & 31);
         const int s = g % nstage;
         if (lane == 0) {
           ok = mbar_wait(bar(bar_empty + s), ((g / nstage) & 1) ^ 1, err, v_warp ? 0x200u : 0x100u, 128);
