@@ -272,7 +272,8 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     const int bar_empty = v_warp ? kBarVEmpty : kBarKEmpty;
     const int box_tile = (lane >> 1) & 1, box_half = lane & 1;  // this lane's box within a block
     const uint32_t box_off = box_half * 16384 + box_tile * 8192;
-    uint32_t g = 0;  // blocks loaded so far, over all items
+    int slot = 0;        // ring slot of the next block (counting over all items)
+    uint32_t phase = 0;  // parity of that slot's use
     for (int n = 0; ok; ++n) {
       int item;
       if (!v_warp) {
@@ -320,22 +321,28 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       // so that each block only needs two shuffles here (this warp's loop is on
       // the critical path).
       int row_a = 0, row_b = 0;
-      for (int blk = 0; blk < nblk; ++blk, ++g) {
+      for (int blk = 0; blk < nblk; ++blk) {
         if ((blk & 31) == 0) {
           row_a = tile_row(2 * (blk + lane));
           row_b = tile_row(2 * (blk + lane) + 1);
         }
         const int ra = __shfl_sync(0xffffffffu, row_a, blk & 31);
         const int rb = __shfl_sync(0xffffffffu, row_b, blk & 31);
-        const int s = g % nstage;
-        if (lane == 0) {
-          ok = mbar_wait(bar(bar_empty + s), ((g / nstage) & 1) ^ 1, err, v_warp ? 0x200u : 0x100u, 128);
-          if (ok) mbar_arrive_expect_tx(bar(bar_full + s), kKVBytes);
+        // Each issuing lane waits for the slot itself (no broadcast round trip);
+        // lane 0 arms the full barrier. A box may land before the arming: the
+        // transaction count may run negative until the arrive, and the phase
+        // cannot complete before it.
+        bool lane_ok = true;
+        if (lane < 4) {
+          lane_ok = mbar_wait(bar(bar_empty + slot), phase ^ 1u, err, v_warp ? 0x200u : 0x100u);
+          if (lane_ok) {
+            if (lane == 0) mbar_arrive_expect_tx(bar(bar_full + slot), kKVBytes);
+            tma_load_4d(ring + slot * kKVBytes + box_off, map, 64 * box_half, it.h, box_tile ? rb : ra, it.b,
+                        bar(bar_full + slot));
+          }
         }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) { ok = false; break; }
-        if (lane < 4)
-          tma_load_4d(ring + s * kKVBytes + box_off, map, 64 * box_half, it.h, box_tile ? rb : ra, it.b,
-                      bar(bar_full + s));
+        if (!__all_sync(0xffffffffu, lane_ok)) { ok = false; break; }
+        if (++slot == nstage) { slot = 0; phase ^= 1u; }
       }
     }
   } else if (warp == kWarpMmaS) {
