@@ -11,9 +11,11 @@
 // A CTA owns R query tiles of one (b, h) and keeps their R x T score rows in
 // shared memory. Pooled K (then V) tiles stream through a padded smem chunk of
 // 64 rows. Selection is a warp-per-row radix select over the order-preserving
-// integer image of the fp32 scores, followed by an in-order compaction that
-// writes the selected tile ids ascending. No atomics: results are
-// deterministic.
+// integer image of the fp32 scores: four passes of 8-bit digits, each a
+// 256-bin shared-memory histogram of the keys that still match the digits
+// fixed so far, then an in-order compaction that writes the selected tile ids
+// ascending. Results are deterministic: the histograms are counts, and the
+// compaction follows tile order.
 #include "kernels.cuh"
 
 namespace vsa {
@@ -24,6 +26,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = 64;        // pooled tiles staged per step
 constexpr int kPad = kHeadDim + 4;  // padded smem row (floats): conflict-free float4 reads
 constexpr size_t kSmemBudget = 220 * 1024;
+constexpr int kBins = 256;          // radix-select histogram, one per warp
 
 // Order-preserving map from fp32 to uint32 (larger float -> larger key);
 // -0 and +0 map to the same key.
@@ -55,6 +58,7 @@ coarse_topk_kernel(const float* __restrict__ pooled_q, const float* __restrict__
   float* sq = S + R * tpad;           // [R][kPad] pooled queries
   float* sx = sq + R * kPad;          // [kChunk][kPad] pooled K or V chunk
   float* sl = sx + kChunk * kPad;     // [R] softmax denominators
+  int* hist = reinterpret_cast<int*>(sl + R);  // [kWarps][kBins] radix histograms
 
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const int t0 = blockIdx.x * R;
@@ -102,18 +106,54 @@ coarse_topk_kernel(const float* __restrict__ pooled_q, const float* __restrict__
     float* row = S + r * tpad;
     const int t = t0 + r;
     if (t < T) {
-      uint32_t thr = 0u;
-      for (int bit = 31; bit >= 0; --bit) {
-        const uint32_t cand = thr | (1u << bit);
-        int cnt = 0;
-        for (int j = lane; j < T; j += 32) cnt += order_key(row[j]) >= cand ? 1 : 0;
-        cnt = __reduce_add_sync(full, cnt);
-        if (cnt >= k) thr = cand;
+      // radix select, 8 bits per pass from the top: prefix holds the digits of
+      // the k-th largest key fixed so far, rem how many keys above it are
+      // still to be taken among those that match the prefix
+      int* h = hist + warp * kBins;
+      uint32_t prefix = 0u, pmask = 0u;
+      int rem = k;
+#pragma unroll 1
+      for (int shift = 24; shift >= 0; shift -= 8) {
+#pragma unroll
+        for (int b = lane; b < kBins; b += 32) h[b] = 0;
+        __syncwarp();
+        for (int j = lane; j < T; j += 32) {
+          const uint32_t key = order_key(row[j]);
+          if ((key & pmask) == prefix) atomicAdd(&h[(key >> shift) & 0xFFu], 1);
+        }
+        __syncwarp();
+        // lane l owns bins 255 - 8l .. 248 - 8l (descending); find the bin where
+        // the count from the top first reaches rem
+        int c[8], lsum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { c[i] = h[255 - 8 * lane - i]; lsum += c[i]; }
+        int incl = lsum;  // inclusive prefix over lanes 0..lane
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(full, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int excl = incl - lsum;
+        const unsigned hit = __ballot_sync(full, excl < rem && incl >= rem);
+        const int src = __ffs(hit) - 1;
+        int digit = 0, above = 0;
+        if (lane == src) {
+          int run = excl;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (run + c[i] >= rem) { digit = 255 - 8 * lane - i; above = run; break; }
+            run += c[i];
+          }
+        }
+        digit = __shfl_sync(full, digit, src);
+        above = __shfl_sync(full, above, src);
+        prefix |= static_cast<uint32_t>(digit) << shift;
+        pmask |= 0xFFu << shift;
+        rem -= above;
+        __syncwarp();
       }
-      int gt = 0;
-      for (int j = lane; j < T; j += 32) gt += order_key(row[j]) > thr ? 1 : 0;
-      gt = __reduce_add_sync(full, gt);
-      const int need_eq = k - gt;
+      const uint32_t thr = prefix;  // the k-th largest key
+      const int need_eq = rem;      // how many keys equal to thr are taken (lowest tile ids first)
       int written = 0, eq_seen = 0;
       int32_t* dst = tile_index + (bh * T + t) * static_cast<size_t>(k);
       for (int base = 0; base < T; base += 32) {
@@ -182,7 +222,7 @@ coarse_topk_kernel(const float* __restrict__ pooled_q, const float* __restrict__
 int pick_rows(int tpad) {
   for (int r = 32; r >= 8; r /= 2) {
     const size_t bytes = (static_cast<size_t>(r) * tpad + static_cast<size_t>(r) * kPad +
-                          static_cast<size_t>(kChunk) * kPad + r) * sizeof(float);
+                          static_cast<size_t>(kChunk) * kPad + r + kWarps * kBins) * sizeof(float);
     if (bytes <= kSmemBudget) return r;
   }
   return 0;
@@ -196,7 +236,7 @@ size_t coarse_smem_bytes(const Geometry& g, int* rows_per_cta) {
   if (rows_per_cta) *rows_per_cta = r;
   if (r == 0) return 0;
   return (static_cast<size_t>(r) * tpad + static_cast<size_t>(r) * kPad +
-          static_cast<size_t>(kChunk) * kPad + r) * sizeof(float);
+          static_cast<size_t>(kChunk) * kPad + r + kWarps * kBins) * sizeof(float);
 }
 
 cudaError_t launch_coarse_topk(const Geometry& g, const float* pooled_q, const float* pooled_k,
