@@ -88,11 +88,13 @@ constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;  // + 1024-byte alignment 
 // barrier indices
 constexpr int kBarQFull = 0;
 constexpr int kBarQEmpty = 1;
+// A K slot is released by the S-full barrier of the block that read it (the
+// same commit, so no separate barrier), a V slot by the P-empty barrier of its
+// block: one commit per MMA group. Each loader waits on those barriers in
+// block order, so none of its parity waits can fall two phases behind.
 constexpr int kBarKFull = 2;
-constexpr int kBarKEmpty = kBarKFull + kNumK;
-constexpr int kBarVFull = kBarKEmpty + kNumK;
-constexpr int kBarVEmpty = kBarVFull + kNumV;
-constexpr int kBarSFull = kBarVEmpty + kNumV;
+constexpr int kBarVFull = kBarKFull + kNumK;
+constexpr int kBarSFull = kBarVFull + kNumV;
 constexpr int kBarSEmpty = kBarSFull + kNumS;
 constexpr int kBarPFull = kBarSEmpty + kNumS;
 constexpr int kBarPEmpty = kBarPFull + kNumP;
@@ -101,6 +103,7 @@ constexpr int kBarItemFull = kBarOEmpty + kNumO;
 constexpr int kBarItemEmpty = kBarItemFull + kItemSlots;
 constexpr int kNumBars = kBarItemEmpty + kItemSlots;
 static_assert(kNumBars * 8 <= 512, "barrier area");
+static_assert(kNumK == kNumS, "K slot g % kNumK is released through S-full barrier g % kNumS");
 static_assert(kColO + kNumO * 64 <= kTmemCols, "TMEM columns");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
@@ -213,8 +216,8 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
   if (tid == 0) {
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 1);
-    for (int s = 0; s < kNumK; ++s) { mbar_init(bar(kBarKFull + s), 1); mbar_init(bar(kBarKEmpty + s), 1); }
-    for (int s = 0; s < kNumV; ++s) { mbar_init(bar(kBarVFull + s), 1); mbar_init(bar(kBarVEmpty + s), 1); }
+    for (int s = 0; s < kNumK; ++s) mbar_init(bar(kBarKFull + s), 1);
+    for (int s = 0; s < kNumV; ++s) mbar_init(bar(kBarVFull + s), 1);
     for (int s = 0; s < kNumS; ++s) {
       mbar_init(bar(kBarSFull + s), 1);
       mbar_init(bar(kBarSEmpty + s), kSoftmaxWarps);
@@ -269,11 +272,11 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     const uint32_t ring = v_warp ? sV : sK;
     const int nstage = v_warp ? kNumV : kNumK;
     const int bar_full = v_warp ? kBarVFull : kBarKFull;
-    const int bar_empty = v_warp ? kBarVEmpty : kBarKEmpty;
     const int box_tile = (lane >> 1) & 1, box_half = lane & 1;  // this lane's box within a block
     const uint32_t box_off = box_half * 16384 + box_tile * 8192;
     int slot = 0;        // ring slot of the next block (counting over all items)
     uint32_t phase = 0;  // parity of that slot's use
+    uint32_t g = 0;      // blocks loaded so far, over all items
     for (int n = 0; ok; ++n) {
       int item;
       if (!v_warp) {
@@ -332,9 +335,21 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         // lane 0 arms the full barrier. A box may land before the arming: the
         // transaction count may run negative until the arrive, and the phase
         // cannot complete before it.
+        // The slot's previous block must have been read: K slot (block g - 3) via
+        // S-full of that block (same slot index, parity phase ^ 1: a fresh
+        // barrier passes the first kNumK blocks), V slot (block g - 2) via
+        // P-empty of that block.
+        int rel_bar = kBarSFull + slot;
+        uint32_t rel_par = phase ^ 1u;
+        if (v_warp) {
+          const uint32_t gp = g - kNumV;  // wraps for the first kNumV blocks, which wait for nothing
+          rel_bar = kBarPEmpty + gp % kNumP;
+          rel_par = (gp / kNumP) & 1u;
+        }
         bool lane_ok = true;
         if (lane < 4) {
-          lane_ok = mbar_wait(bar(bar_empty + slot), phase ^ 1u, err, v_warp ? 0x200u : 0x100u);
+          if (!v_warp || g >= static_cast<uint32_t>(kNumV))
+            lane_ok = mbar_wait(bar(rel_bar), rel_par, err, v_warp ? 0x200u : 0x100u);
           if (lane_ok) {
             if (lane == 0) mbar_arrive_expect_tx(bar(bar_full + slot), kKVBytes);
             tma_load_4d(ring + slot * kKVBytes + box_off, map, 64 * box_half, it.h, box_tile ? rb : ra, it.b,
@@ -343,6 +358,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         }
         if (!__all_sync(0xffffffffu, lane_ok)) { ok = false; break; }
         if (++slot == nstage) { slot = 0; phase ^= 1u; }
+        ++g;
       }
     }
   } else if (warp == kWarpMmaS) {
@@ -382,8 +398,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
           const uint32_t qoff = ((s >> 2) * 8192 + (s & 3) * 32) >> 4;
           umma_bf16_elect(tbase + sb * kColS1, dk + koff, dq0 + qoff, id_s, s > 0 ? 1u : 0u);
         }
-        umma_commit_elect(bar(kBarKEmpty + ks));
-        umma_commit_elect(bar(kBarSFull + sb));
+        umma_commit_elect(bar(kBarSFull + sb));  // also releases K slot ks
       }
       if (!ok) break;
       // Q stays in use until the item's last S^T product completes
@@ -422,8 +437,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         for (int s = 0; s < 8; ++s)
           umma_bf16_elect(tbase + kColO + ob * 64, dv + ((s * 2048) >> 4), dp + ((s * 2048) >> 4), id_o,
                           (j > 0 || s > 0) ? 1u : 0u);
-        umma_commit_elect(bar(kBarVEmpty + vs));
-        umma_commit_elect(bar(kBarPEmpty + pb));
+        umma_commit_elect(bar(kBarPEmpty + pb));  // also releases V slot vs
       }
     }
   } else {
