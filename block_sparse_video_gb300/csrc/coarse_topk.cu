@@ -5,17 +5,20 @@
 //   s[t][j] = pooled_q[t] . pooled_k[j] / sqrt(128)         over all T video tiles
 //   selection(t) = the k largest s[t][j], ties to the lower j, ascending
 //   coarse[t] = sum_j softmax_j(s[t][.]) * pooled_v[j]
-// The scores live only in shared memory. Everything is fp32 FFMA: the
-// selection is an integer decision taken in fp32.
+// The scores live only in shared memory.
 //
 // A CTA owns R query tiles of one (b, h) and keeps their R x T score rows in
 // shared memory. Pooled K (then V) tiles stream through a padded smem chunk of
-// 64 rows. Selection is a warp-per-row radix select over the order-preserving
-// integer image of the fp32 scores: four passes of 8-bit digits, each a
-// 256-bin shared-memory histogram of the keys that still match the digits
-// fixed so far, then an in-order compaction that writes the selected tile ids
-// ascending. Results are deterministic: the histograms are counts, and the
-// compaction follows tile order.
+// 64 rows. Both products run on the tensor cores (mma.sync m16n8k8, tf32) with
+// each fp32 operand split into a tf32 head and a tf32 remainder: a*b is taken
+// as hi*hi + hi*lo + lo*hi, which leaves out only the lo*lo term (relative size
+// ~2^-22), so the scores carry fp32-level error and the selection is an integer
+// decision taken on them. Selection is a warp-per-row radix select over the
+// order-preserving integer image of the fp32 scores: four passes of 8-bit
+// digits, each a 256-bin shared-memory histogram of the keys that still match
+// the digits fixed so far, then an in-order compaction that writes the selected
+// tile ids ascending. Results are deterministic: the histograms are counts, and
+// the compaction follows tile order.
 #include "kernels.cuh"
 
 namespace vsa {
@@ -23,10 +26,11 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 64;        // pooled tiles staged per step
-constexpr int kPad = kHeadDim + 4;  // padded smem row (floats): conflict-free float4 reads
+constexpr int kChunk = 64;            // pooled tiles staged per step
+constexpr int kQPad = kHeadDim + 4;   // q rows and K chunk rows (floats): conflict-free fragment loads
+constexpr int kVPad = kHeadDim + 8;   // V chunk rows
 constexpr size_t kSmemBudget = 220 * 1024;
-constexpr int kBins = 256;          // radix-select histogram, one per warp
+constexpr int kBins = 256;            // radix-select histogram, one per warp
 
 // Order-preserving map from fp32 to uint32 (larger float -> larger key);
 // -0 and +0 map to the same key.
@@ -36,16 +40,56 @@ __device__ __forceinline__ uint32_t order_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ void load_rows(float* dst, const float* src, int first, int count,
-                                          int rows) {
+__device__ __forceinline__ void load_rows(float* dst, const float* src, int first, int count, int rows,
+                                          int pad) {
   // rows [first, first + rows) of a [count, 128] fp32 array into padded smem; zero past count
   for (int e = threadIdx.x; e < rows * (kHeadDim / 4); e += kThreads) {
     const int r = e / (kHeadDim / 4), c4 = e % (kHeadDim / 4);
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
     if (first + r < count)
       x = __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(first + r) * kHeadDim) + c4);
-    *reinterpret_cast<float4*>(dst + r * kPad + 4 * c4) = x;
+    *reinterpret_cast<float4*>(dst + r * pad + 4 * c4) = x;
   }
+}
+
+// x = hi + lo with hi and lo tf32 values (hi rounded to nearest)
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+  const float r = x - __uint_as_float(hi);
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// c += a b for a 16x8 (A) by 8x8 (B) step, from split operands (small terms first)
+__device__ __forceinline__ void mma_split(float (&c)[4], const uint32_t (&ahi)[4], const uint32_t (&alo)[4],
+                                          uint32_t bhi0, uint32_t bhi1, uint32_t blo0, uint32_t blo1) {
+  mma_tf32(c, alo, bhi0, bhi1);
+  mma_tf32(c, ahi, blo0, blo1);
+  mma_tf32(c, ahi, bhi0, bhi1);
+}
+
+// Fragment layouts of m16n8k8 (lane = 4 g + t4): A (16 x 8, row-major) holds
+// (g, t4), (g + 8, t4), (g, t4 + 4), (g + 8, t4 + 4); B (8 x 8, k x n) holds
+// (t4, g), (t4 + 4, g); C (16 x 8) holds (g, 2 t4), (g, 2 t4 + 1), (g + 8, 2 t4),
+// (g + 8, 2 t4 + 1).
+__device__ __forceinline__ void load_a_split(const float* base, int stride, int rows_valid, int g, int t4,
+                                             uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+  // base points at row 0, column t4-aligned step start; rows >= rows_valid read as zero
+  const float x0 = g < rows_valid ? base[g * stride + t4] : 0.f;
+  const float x1 = g + 8 < rows_valid ? base[(g + 8) * stride + t4] : 0.f;
+  const float x2 = g < rows_valid ? base[g * stride + t4 + 4] : 0.f;
+  const float x3 = g + 8 < rows_valid ? base[(g + 8) * stride + t4 + 4] : 0.f;
+  split_tf32(x0, hi[0], lo[0]);
+  split_tf32(x1, hi[1], lo[1]);
+  split_tf32(x2, hi[2], lo[2]);
+  split_tf32(x3, hi[3], lo[3]);
 }
 
 template <int R>
@@ -53,49 +97,58 @@ __global__ void __launch_bounds__(kThreads, 1)
 coarse_topk_kernel(const float* __restrict__ pooled_q, const float* __restrict__ pooled_k,
                    const float* __restrict__ pooled_v, float* __restrict__ coarse,
                    int32_t* __restrict__ tile_index, int T, int k, int tpad) {
+  constexpr int MT = R >= 16 ? R / 16 : 1;  // m16 row tiles (R = 8 leaves rows 8-15 empty)
+  const int sstride = tpad + 4;             // score row stride: conflict-free A-fragment reads
   extern __shared__ __align__(16) float smem[];
-  float* S = smem;                    // [R][tpad] scores, then probabilities
-  float* sq = S + R * tpad;           // [R][kPad] pooled queries
-  float* sx = sq + R * kPad;          // [kChunk][kPad] pooled K or V chunk
-  float* sl = sx + kChunk * kPad;     // [R] softmax denominators
+  float* S = smem;                          // [R][sstride] scores, then probabilities
+  float* sq = S + R * sstride;              // [16 MT][kQPad] pooled queries
+  float* sx = sq + 16 * MT * kQPad;         // [kChunk][kVPad] pooled K (row stride kQPad) or V chunk
+  float* sl = sx + kChunk * kVPad;          // [R] softmax denominators
   int* hist = reinterpret_cast<int*>(sl + R);  // [kWarps][kBins] radix histograms
 
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  const int g = lane >> 2, t4 = lane & 3;
   const int t0 = blockIdx.x * R;
   const size_t bh = blockIdx.y;
   const float* gq = pooled_q + bh * T * kHeadDim;
   const float* gk = pooled_k + bh * T * kHeadDim;
   const float* gv = pooled_v + bh * T * kHeadDim;
   const float scale = 0.08838834764831845f;  // 1/sqrt(128)
+  const int rows = min(R, T - t0);           // query tiles of this CTA
 
-  load_rows(sq, gq, t0, T, R);
+  load_rows(sq, gq, t0, t0 + rows, 16 * MT, kQPad);
 
-  // ---- scores: thread -> one query row, KPT keys of each chunk
-  constexpr int TPR = kThreads / R;   // threads per query row
-  constexpr int KPT = kChunk / TPR;   // keys per thread per chunk
-  const int my_r = tid / TPR, my_k = tid % TPR;
+  // ---- scores: warp w computes key columns 8w .. 8w + 7 of each chunk for all rows
   for (int c0 = 0; c0 < tpad; c0 += kChunk) {
     __syncthreads();
-    load_rows(sx, gk, c0, T, kChunk);
+    load_rows(sx, gk, c0, T, kChunk, kQPad);
     __syncthreads();
-    float acc[KPT];
+    float acc[MT][4];
 #pragma unroll
-    for (int i = 0; i < KPT; ++i) acc[i] = 0.f;
-    const float* qrow = sq + my_r * kPad;
+    for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+    const float* kb = sx + (8 * warp + g) * kQPad;
 #pragma unroll 4
-    for (int d = 0; d < kHeadDim; d += 4) {
-      const float4 a = *reinterpret_cast<const float4*>(qrow + d);
+    for (int kk = 0; kk < kHeadDim; kk += 8) {
+      uint32_t bh0, bl0, bh1, bl1;
+      split_tf32(kb[kk + t4], bh0, bl0);
+      split_tf32(kb[kk + t4 + 4], bh1, bl1);
 #pragma unroll
-      for (int i = 0; i < KPT; ++i) {
-        const float4 b = *reinterpret_cast<const float4*>(sx + (my_k + TPR * i) * kPad + d);
-        acc[i] = fmaf(a.x, b.x, acc[i]);
-        acc[i] = fmaf(a.y, b.y, acc[i]);
-        acc[i] = fmaf(a.z, b.z, acc[i]);
-        acc[i] = fmaf(a.w, b.w, acc[i]);
+      for (int m = 0; m < MT; ++m) {
+        uint32_t ah[4], al[4];
+        load_a_split(sq + 16 * m * kQPad + kk, kQPad, 16, g, t4, ah, al);
+        mma_split(acc[m], ah, al, bh0, bh1, bl0, bl1);
       }
     }
+    const int col = c0 + 8 * warp + 2 * t4;
 #pragma unroll
-    for (int i = 0; i < KPT; ++i) S[my_r * tpad + c0 + my_k + TPR * i] = acc[i] * scale;
+    for (int m = 0; m < MT; ++m) {
+      const int r0 = 16 * m + g;
+      if (r0 < R)
+        *reinterpret_cast<float2*>(S + r0 * sstride + col) = make_float2(acc[m][0] * scale, acc[m][1] * scale);
+      if (r0 + 8 < R)
+        *reinterpret_cast<float2*>(S + (r0 + 8) * sstride + col) =
+            make_float2(acc[m][2] * scale, acc[m][3] * scale);
+    }
   }
   __syncthreads();
 
@@ -103,7 +156,7 @@ coarse_topk_kernel(const float* __restrict__ pooled_q, const float* __restrict__
   const unsigned full = 0xffffffffu;
   const unsigned lt_mask = (1u << lane) - 1u;
   for (int r = warp; r < R; r += kWarps) {
-    float* row = S + r * tpad;
+    float* row = S + r * sstride;
     const int t = t0 + r;
     if (t < T) {
       // radix select, 8 bits per pass from the top: prefix holds the digits of
@@ -183,48 +236,59 @@ coarse_topk_kernel(const float* __restrict__ pooled_q, const float* __restrict__
     if (lane == 0) sl[r] = l;
   }
 
-  // ---- coarse[t] = sum_j p[t][j] * pooled_v[j] / l[t]
-  constexpr int RPT = R / kWarps;  // query rows per thread
-  const int d4 = lane;             // dims 4*d4 .. 4*d4+3
-  float4 acc[RPT];
+  // ---- coarse[t] = sum_j p[t][j] * pooled_v[j] / l[t]; warp w owns dims 16w .. 16w + 15
+  float o[MT][2][4];
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) o[m][nt][0] = o[m][nt][1] = o[m][nt][2] = o[m][nt][3] = 0.f;
   for (int c0 = 0; c0 < tpad; c0 += kChunk) {
     __syncthreads();
-    load_rows(sx, gv, c0, T, kChunk);
+    load_rows(sx, gv, c0, T, kChunk, kVPad);
     __syncthreads();
-#pragma unroll 4
-    for (int j = 0; j < kChunk; ++j) {
-      const float4 vv = *reinterpret_cast<const float4*>(sx + j * kPad + 4 * d4);
+#pragma unroll 2
+    for (int kk = 0; kk < kChunk; kk += 8) {
+      uint32_t bh[2][2], bl[2][2];
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) {
-        const float p = S[(warp * RPT + i) * tpad + c0 + j];
-        acc[i].x = fmaf(p, vv.x, acc[i].x);
-        acc[i].y = fmaf(p, vv.y, acc[i].y);
-        acc[i].z = fmaf(p, vv.z, acc[i].z);
-        acc[i].w = fmaf(p, vv.w, acc[i].w);
+      for (int nt = 0; nt < 2; ++nt) {
+        const int n = 16 * warp + 8 * nt + g;
+        split_tf32(sx[(kk + t4) * kVPad + n], bh[nt][0], bl[nt][0]);
+        split_tf32(sx[(kk + t4 + 4) * kVPad + n], bh[nt][1], bl[nt][1]);
+      }
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        uint32_t ah[4], al[4];
+        load_a_split(S + 16 * m * sstride + c0 + kk, sstride, R - 16 * m, g, t4, ah, al);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) mma_split(o[m][nt], ah, al, bh[nt][0], bh[nt][1], bl[nt][0], bl[nt][1]);
       }
     }
   }
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    const int r = warp * RPT + i;
-    const int t = t0 + r;
-    if (t < T) {
-      const float inv = 1.0f / sl[r];
-      float4 o = acc[i];
-      o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
-      reinterpret_cast<float4*>(coarse + (bh * T + t) * kHeadDim)[d4] = o;
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int r = 16 * m + g + 8 * half;
+      if (r < rows) {
+        const float inv = 1.0f / sl[r];
+        float* dst = coarse + (bh * T + t0 + r) * kHeadDim;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+          *reinterpret_cast<float2*>(dst + 16 * warp + 8 * nt + 2 * t4) =
+              make_float2(o[m][nt][2 * half] * inv, o[m][nt][2 * half + 1] * inv);
+      }
     }
-  }
+}
+
+size_t smem_for(int r, int tpad) {
+  const int mt = r >= 16 ? r / 16 : 1;
+  return (static_cast<size_t>(r) * (tpad + 4) + static_cast<size_t>(16 * mt) * kQPad +
+          static_cast<size_t>(kChunk) * kVPad + r + kWarps * kBins) * sizeof(float);
 }
 
 int pick_rows(int tpad) {
-  for (int r = 32; r >= 8; r /= 2) {
-    const size_t bytes = (static_cast<size_t>(r) * tpad + static_cast<size_t>(r) * kPad +
-                          static_cast<size_t>(kChunk) * kPad + r + kWarps * kBins) * sizeof(float);
-    if (bytes <= kSmemBudget) return r;
-  }
+  for (int r = 32; r >= 8; r /= 2)
+    if (smem_for(r, tpad) <= kSmemBudget) return r;
   return 0;
 }
 
@@ -235,8 +299,7 @@ size_t coarse_smem_bytes(const Geometry& g, int* rows_per_cta) {
   const int r = pick_rows(tpad);
   if (rows_per_cta) *rows_per_cta = r;
   if (r == 0) return 0;
-  return (static_cast<size_t>(r) * tpad + static_cast<size_t>(r) * kPad +
-          static_cast<size_t>(kChunk) * kPad + r + kWarps * kBins) * sizeof(float);
+  return smem_for(r, tpad);
 }
 
 cudaError_t launch_coarse_topk(const Geometry& g, const float* pooled_q, const float* pooled_k,
