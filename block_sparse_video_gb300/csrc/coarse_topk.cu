@@ -24,7 +24,7 @@
 namespace vsa {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = 64;            // pooled tiles staged per step
 constexpr int kQPad = kHeadDim + 4;   // q rows and K chunk rows (floats): conflict-free fragment loads
@@ -75,6 +75,32 @@ __device__ __forceinline__ void mma_split(float (&c)[4], const uint32_t (&ahi)[4
   mma_tf32(c, ahi, bhi0, bhi1);
 }
 
+// Next K or V chunk, fetched into registers (one float4 per thread and step)
+// while the current chunk is in use, then stored into the padded smem rows.
+constexpr int kChunkF4PerThread = kChunk * (kHeadDim / 4) / kThreads;
+static_assert(kChunkF4PerThread * kThreads == kChunk * (kHeadDim / 4), "chunk staging");
+
+__device__ __forceinline__ void fetch_chunk(float4 (&pre)[kChunkF4PerThread], const float* src, int first,
+                                            int count) {
+#pragma unroll
+  for (int i = 0; i < kChunkF4PerThread; ++i) {
+    const int e = threadIdx.x + i * kThreads;
+    const int r = e / (kHeadDim / 4), c4 = e % (kHeadDim / 4);
+    pre[i] = first + r < count
+                 ? __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(first + r) * kHeadDim) + c4)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+__device__ __forceinline__ void stash_chunk(float* dst, const float4 (&pre)[kChunkF4PerThread], int pad) {
+#pragma unroll
+  for (int i = 0; i < kChunkF4PerThread; ++i) {
+    const int e = threadIdx.x + i * kThreads;
+    const int r = e / (kHeadDim / 4), c4 = e % (kHeadDim / 4);
+    *reinterpret_cast<float4*>(dst + r * pad + 4 * c4) = pre[i];
+  }
+}
+
 // Fragment layouts of m16n8k8 (lane = 4 g + t4): A (16 x 8, row-major) holds
 // (g, t4), (g + 8, t4), (g, t4 + 4), (g + 8, t4 + 4); B (8 x 8, k x n) holds
 // (t4, g), (t4 + 4, g); C (16 x 8) holds (g, 2 t4), (g, 2 t4 + 1), (g + 8, 2 t4),
@@ -118,38 +144,36 @@ coarse_topk_kernel(const float* __restrict__ pooled_q, const float* __restrict__
 
   load_rows(sq, gq, t0, t0 + rows, 16 * MT, kQPad);
 
-  // ---- scores: warp w computes key columns 8w .. 8w + 7 of each chunk for all rows
+  // ---- scores: warp w computes key columns 8 (w % 8) .. + 7 of each chunk for
+  // row tile w / 8 (warps of a row tile that does not exist idle here)
+  float4 pre[kChunkF4PerThread];
+  fetch_chunk(pre, gk, 0, T);
+  const int s_nt = warp % 8, s_m = warp / 8;
   for (int c0 = 0; c0 < tpad; c0 += kChunk) {
     __syncthreads();
-    load_rows(sx, gk, c0, T, kChunk, kQPad);
+    stash_chunk(sx, pre, kQPad);
     __syncthreads();
-    float acc[MT][4];
-#pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
-    const float* kb = sx + (8 * warp + g) * kQPad;
+    if (c0 + kChunk < tpad) fetch_chunk(pre, gk, c0 + kChunk, T);  // in flight during the products
+    if (s_m < MT) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const float* kb = sx + (8 * s_nt + g) * kQPad;
 #pragma unroll 4
-    for (int kk = 0; kk < kHeadDim; kk += 8) {
-      uint32_t bh0, bl0, bh1, bl1;
-      split_tf32(kb[kk + t4], bh0, bl0);
-      split_tf32(kb[kk + t4 + 4], bh1, bl1);
-#pragma unroll
-      for (int m = 0; m < MT; ++m) {
+      for (int kk = 0; kk < kHeadDim; kk += 8) {
+        uint32_t bh0, bl0, bh1, bl1;
+        split_tf32(kb[kk + t4], bh0, bl0);
+        split_tf32(kb[kk + t4 + 4], bh1, bl1);
         uint32_t ah[4], al[4];
-        load_a_split(sq + 16 * m * kQPad + kk, kQPad, 16, g, t4, ah, al);
-        mma_split(acc[m], ah, al, bh0, bh1, bl0, bl1);
+        load_a_split(sq + 16 * s_m * kQPad + kk, kQPad, 16, g, t4, ah, al);
+        mma_split(acc, ah, al, bh0, bh1, bl0, bl1);
       }
-    }
-    const int col = c0 + 8 * warp + 2 * t4;
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      const int r0 = 16 * m + g;
-      if (r0 < R)
-        *reinterpret_cast<float2*>(S + r0 * sstride + col) = make_float2(acc[m][0] * scale, acc[m][1] * scale);
+      const int col = c0 + 8 * s_nt + 2 * t4;
+      const int r0 = 16 * s_m + g;
+      if (r0 < R) *reinterpret_cast<float2*>(S + r0 * sstride + col) = make_float2(acc[0] * scale, acc[1] * scale);
       if (r0 + 8 < R)
-        *reinterpret_cast<float2*>(S + (r0 + 8) * sstride + col) =
-            make_float2(acc[m][2] * scale, acc[m][3] * scale);
+        *reinterpret_cast<float2*>(S + (r0 + 8) * sstride + col) = make_float2(acc[2] * scale, acc[3] * scale);
     }
   }
+  fetch_chunk(pre, gv, 0, T);  // first V chunk, in flight during the selection
   __syncthreads();
 
   // ---- per row: radix select of the k-th largest key, ordered compaction, softmax
@@ -236,31 +260,27 @@ coarse_topk_kernel(const float* __restrict__ pooled_q, const float* __restrict__
     if (lane == 0) sl[r] = l;
   }
 
-  // ---- coarse[t] = sum_j p[t][j] * pooled_v[j] / l[t]; warp w owns dims 16w .. 16w + 15
-  float o[MT][2][4];
+  // ---- coarse[t] = sum_j p[t][j] * pooled_v[j] / l[t]; warp w owns dims 8w .. 8w + 7
+  static_assert(kWarps * 8 == kHeadDim, "one 8-dim column tile per warp");
+  float o[MT][4];
 #pragma unroll
-  for (int m = 0; m < MT; ++m)
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) o[m][nt][0] = o[m][nt][1] = o[m][nt][2] = o[m][nt][3] = 0.f;
+  for (int m = 0; m < MT; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
   for (int c0 = 0; c0 < tpad; c0 += kChunk) {
     __syncthreads();
-    load_rows(sx, gv, c0, T, kChunk, kVPad);
+    stash_chunk(sx, pre, kVPad);
     __syncthreads();
+    if (c0 + kChunk < tpad) fetch_chunk(pre, gv, c0 + kChunk, T);
 #pragma unroll 2
     for (int kk = 0; kk < kChunk; kk += 8) {
-      uint32_t bh[2][2], bl[2][2];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int n = 16 * warp + 8 * nt + g;
-        split_tf32(sx[(kk + t4) * kVPad + n], bh[nt][0], bl[nt][0]);
-        split_tf32(sx[(kk + t4 + 4) * kVPad + n], bh[nt][1], bl[nt][1]);
-      }
+      const int n = 8 * warp + g;
+      uint32_t bh0, bl0, bh1, bl1;
+      split_tf32(sx[(kk + t4) * kVPad + n], bh0, bl0);
+      split_tf32(sx[(kk + t4 + 4) * kVPad + n], bh1, bl1);
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
         uint32_t ah[4], al[4];
         load_a_split(S + 16 * m * sstride + c0 + kk, sstride, R - 16 * m, g, t4, ah, al);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) mma_split(o[m][nt], ah, al, bh[nt][0], bh[nt][1], bl[nt][0], bl[nt][1]);
+        mma_split(o[m], ah, al, bh0, bh1, bl0, bl1);
       }
     }
   }
@@ -272,10 +292,7 @@ coarse_topk_kernel(const float* __restrict__ pooled_q, const float* __restrict__
       if (r < rows) {
         const float inv = 1.0f / sl[r];
         float* dst = coarse + (bh * T + t0 + r) * kHeadDim;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-          *reinterpret_cast<float2*>(dst + 16 * warp + 8 * nt + 2 * t4) =
-              make_float2(o[m][nt][2 * half] * inv, o[m][nt][2 * half + 1] * inv);
+        *reinterpret_cast<float2*>(dst + 8 * warp + 2 * t4) = make_float2(o[m][2 * half] * inv, o[m][2 * half + 1] * inv);
       }
     }
 }
