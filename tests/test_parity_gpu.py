@@ -103,6 +103,16 @@ def test_long_video_smaller_coarse_tiles(cuda_ok):
     assert_errors(stats, "long video")
 
 
+def test_very_long_video_eight_coarse_tiles(cuda_ok):
+    """T = 2,600 video tiles (the last one ragged): the coarse kernel keeps 8
+    query tiles per CTA and runs its tensor-core tiles with half the rows empty.
+    Every pooled statistic, selection and coarse row of both heads is checked."""
+    lv = 64 * 2600 - 30
+    q, k, v, g = make_inputs(1, 2, 40, 24, lv, 23, device="cuda")
+    stats = _sampled(q, k, v, g, 40, 24, lv, 0.2, [(0, 0), (0, 1)], 16, {(0, 0)}, 23)
+    assert_errors(stats, "very long video")
+
+
 def test_deterministic(cuda_ok):
     c = CONFIGS["medium"]
     q, k, v, g = make_config_inputs(c, device="cuda")
