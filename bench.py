@@ -111,6 +111,71 @@ def pool_bytes(cfg=None):
     return 3 * cfg.batch * cfg.len_video * cfg.heads * 128 * 2 + 3 * cfg.batch * cfg.heads * cfg.n_video_tiles * 128 * 4
 
 
+# fused preprocessing workload: the projections of a 10 s request arrive in a
+# capacity-padded buffer of 78,080 rows (the page's preallocated size for that
+# request); RoPE covers 96 of the 128 channels of each head
+PRE_ROWS_IN = 78080
+ROPE_DIM = 96
+
+
+def preprocess_bytes(cfg=None, rope_dim=ROPE_DIM):
+    """Algorithmic HBM bytes of one preprocessing launch: the N valid projection
+    rows of Q/K/V/gate read once, the four packed tensors written, the RoPE
+    tables read once, and the pooled Q/K/V written (padding rows are never read)."""
+    cfg = CFG if cfg is None else cfg
+    rows = cfg.batch * cfg.seq * cfg.heads * 128 * 2
+    return 8 * rows + cfg.seq * rope_dim * 4 + 3 * cfg.batch * cfg.heads * cfg.n_video_tiles * 128 * 4
+
+
+def measure_preprocess(op, cfg, dev, stream, flush, steps, warmup, peaks, world):
+    """Time vsa_preprocess alone (device events, L2 flushed before each launch)
+    and the fused chain vsa_preprocess + vsa_forward_preprocessed."""
+    import block_sparse_video_gb300 as bsv
+    from block_sparse_video_gb300.synthetic import make_norm_weights, make_projections, make_rope_tables
+
+    rows_in = max(PRE_ROWS_IN, cfg.seq)
+    proj = make_projections(cfg.batch, rows_in, cfg.heads, cfg.seed + 100, device=dev)
+    wq, wk = (w.to(dev) for w in make_norm_weights(cfg.heads, cfg.seed + 101))
+    cos, sin = (t.to(dev) for t in make_rope_tables(cfg.len_text, cfg.len_audio, cfg.len_video, ROPE_DIM))
+    outs = [torch.empty(op.shape, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    fwd_out = torch.empty(op.shape, dtype=torch.bfloat16, device=dev)
+    ins = [proj[:, :, i] for i in range(4)]
+    args = bsv.vsa_preprocess_args_t(
+        ins[0].data_ptr(), ins[1].data_ptr(), ins[2].data_ptr(), ins[3].data_ptr(), rows_in,
+        ins[0].stride(1), None, wq.data_ptr(), wk.data_ptr(), 1e-6, ROPE_DIM, 1, cos.data_ptr(),
+        sin.data_ptr(), *[x.data_ptr() for x in outs])
+    for _ in range(warmup):
+        bsv.vsa_preprocess(op.plan, args, op.workspace)
+    op.check()
+    s0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    s1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        s0[i].record(stream)
+        bsv.vsa_preprocess(op.plan, args, op.workspace)
+        s1[i].record(stream)
+    torch.cuda.synchronize(dev)
+    op.check()
+    pre_ms = reduce_max(statistics.mean(a.elapsed_time(b) for a, b in zip(s0, s1)), world, dev)
+    for i in range(steps):
+        flush.zero_()
+        s0[i].record(stream)
+        bsv.vsa_preprocess(op.plan, args, op.workspace)
+        bsv.vsa_forward_preprocessed(op.plan, *outs, fwd_out, op.workspace)
+        s1[i].record(stream)
+    torch.cuda.synchronize(dev)
+    op.check()
+    chain_ms = reduce_max(statistics.mean(a.elapsed_time(b) for a, b in zip(s0, s1)), world, dev)
+    nbytes = preprocess_bytes(cfg)
+    gbs = nbytes / (pre_ms * 1e-3) / 1e9
+    del proj, outs, fwd_out
+    return {"ms": pre_ms, "bytes": nbytes, "GB_s": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+            "bound": "hbm", "rows_in": rows_in, "rope_dim": ROPE_DIM,
+            "launches_timed": steps,
+            "fused_chain_ms": chain_ms,
+            "fused_chain": "vsa_preprocess + vsa_forward_preprocessed (coarse + top-k, fine fast, fine exact)"}
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -338,6 +403,11 @@ def run_ours(args):
         except Exception:
             traffic = None
 
+    # ---- fused preprocessing, measured on its own (not part of the forward step above)
+    pre = None
+    if not args.no_preprocess:
+        pre = measure_preprocess(op, cfg, dev, stream, flush, steps, args.warmup, peaks, world)
+
     # ---- end to end through the host-buffer entry point
     e2e = None
     if args.e2e_steps > 0:
@@ -389,6 +459,7 @@ def run_ours(args):
                 "fine_attn_kernel": {"ms": fine_ms, "flops": fl["fine"], "TFLOP_s": fine_tflops,
                                      "kv_l2_to_smem_bytes": kv_stream_bytes(cfg, keep),
                                      "kv_l2_to_smem_TB_s": kv_stream_bytes(cfg, keep) / (fine_ms * 1e-3) / 1e12},
+                "preprocess_kernel": pre,
             },
             "clocks": clocks,
             "e2e": e2e,
@@ -418,6 +489,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-preprocess", action="store_true",
+                    help="skip the separate fused-preprocessing measurement")
     ap.add_argument("--workload", choices=["10s", "5s", "medium"], default="10s",
                     help="10s is the benchmark; the smaller ones serve profiler captures")
     args = ap.parse_args(argv)

@@ -46,6 +46,29 @@ class vsa_shape_t(ctypes.Structure):
     ]
 
 
+class vsa_preprocess_args_t(ctypes.Structure):
+    _fields_ = [
+        ("q_in", ctypes.c_void_p),
+        ("k_in", ctypes.c_void_p),
+        ("v_in", ctypes.c_void_p),
+        ("gate_in", ctypes.c_void_p),
+        ("rows_in", ctypes.c_int64),
+        ("row_stride", ctypes.c_int64),
+        ("src_row", ctypes.c_void_p),
+        ("q_norm_weight", ctypes.c_void_p),
+        ("k_norm_weight", ctypes.c_void_p),
+        ("eps", ctypes.c_float),
+        ("rope_dim", ctypes.c_int32),
+        ("rope_interleaved", ctypes.c_int32),
+        ("rope_cos", ctypes.c_void_p),
+        ("rope_sin", ctypes.c_void_p),
+        ("q_out", ctypes.c_void_p),
+        ("k_out", ctypes.c_void_p),
+        ("v_out", ctypes.c_void_p),
+        ("gate_out", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -63,6 +86,8 @@ def load_library(path: str = LIB_PATH):
         "vsa_plan_create": (i32, [ctypes.POINTER(vsa_shape_t), ctypes.c_int, ctypes.POINTER(vp)]),
         "vsa_plan_info": (i32, [vp, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(sz)]),
         "vsa_forward": (i32, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "vsa_preprocess": (i32, [vp, ctypes.POINTER(vsa_preprocess_args_t), vp, sz, vp]),
+        "vsa_forward_preprocessed": (i32, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "vsa_plan_host_path_bytes": (i32, [vp, ctypes.POINTER(sz)]),
         "vsa_forward_host": (i32, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "vsa_debug_views": (i32, [vp, vp] + [ctypes.POINTER(vp)] * 5),
@@ -150,6 +175,21 @@ def vsa_forward(plan, q, k, v, gate, out, workspace, stream=None):
     _check(load_library().vsa_forward(plan, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out),
                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _stream_handle(stream)), "vsa_forward")
+
+
+def vsa_preprocess(plan, args, workspace, stream=None):
+    """Enqueue the fused preprocessing; ``args`` is a filled vsa_preprocess_args_t."""
+    _check(load_library().vsa_preprocess(plan, ctypes.byref(args), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(),
+                                         _stream_handle(stream)), "vsa_preprocess")
+
+
+def vsa_forward_preprocessed(plan, q, k, v, gate, out, workspace, stream=None):
+    """Enqueue the forward over inputs packed by vsa_preprocess into ``workspace``."""
+    _check(load_library().vsa_forward_preprocessed(plan, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out),
+                                                   _ptr(workspace),
+                                                   workspace.numel() * workspace.element_size(),
+                                                   _stream_handle(stream)), "vsa_forward_preprocessed")
 
 
 def vsa_forward_host(plan, q, k, v, gate, out, device_buffer, stream=None):
@@ -253,6 +293,62 @@ class VSA:
 
     __call__ = forward
 
+    def preprocess(self, q_in, k_in, v_in, gate_in, q_norm_weight, k_norm_weight, rope_cos=None,
+                   rope_sin=None, rope_dim=0, rope_interleaved=True, eps=1e-6, src_row=None, out=None,
+                   stream=None):
+        """Fused preprocessing of projection rows into packed (q, k, v, gate).
+
+        q_in .. gate_in: bf16 [B, rows_in, H, 128] views sharing one row stride
+        (e.g. slices of a merged [B, rows_in, 4, H, 128] projection), channels
+        contiguous. q/k_norm_weight: fp32 [H, 128]. rope_cos/sin: fp32
+        [N, rope_dim / 2]. src_row: int32 [B, N] or None. out: optional tuple
+        of four bf16 [B, N, H, 128] tensors. The pooled statistics stay in this
+        object's workspace for forward_preprocessed.
+        """
+        ins = (q_in, k_in, v_in, gate_in)
+        b, h = self.batch, self.num_heads
+        for name, x in zip(("q_in", "k_in", "v_in", "gate_in"), ins):
+            if (x.dtype != torch.bfloat16 or x.dim() != 4 or x.shape[0] != b or x.shape[2] != h
+                    or x.shape[3] != 128 or x.stride(3) != 1 or x.stride(2) != 128 or x.device != self.device):
+                raise ValueError(f"{name}: expected bf16 [B, rows_in, H, 128] with contiguous heads on {self.device}")
+            if x.shape[1:] != q_in.shape[1:] or x.stride()[:2] != q_in.stride()[:2]:
+                raise ValueError("the four projections must share shape and strides")
+        rows_in, row_stride = q_in.shape[1], q_in.stride(1)
+        if b > 1 and q_in.stride(0) != rows_in * row_stride:
+            raise ValueError("batches must be rows_in * row_stride elements apart")
+        for name, w in (("q_norm_weight", q_norm_weight), ("k_norm_weight", k_norm_weight)):
+            if w.dtype != torch.float32 or tuple(w.shape) != (h, 128) or not w.is_contiguous():
+                raise ValueError(f"{name}: expected contiguous fp32 [{h}, 128]")
+        if rope_dim:
+            for name, t in (("rope_cos", rope_cos), ("rope_sin", rope_sin)):
+                if (t is None or t.dtype != torch.float32 or tuple(t.shape) != (self.seq, rope_dim // 2)
+                        or not t.is_contiguous()):
+                    raise ValueError(f"{name}: expected contiguous fp32 [{self.seq}, {rope_dim // 2}]")
+        if src_row is not None and (src_row.dtype != torch.int32 or tuple(src_row.shape) != (b, self.seq)
+                                    or not src_row.is_contiguous()):
+            raise ValueError(f"src_row: expected contiguous int32 [{b}, {self.seq}]")
+        if out is None:
+            out = tuple(torch.empty(self.shape, dtype=torch.bfloat16, device=self.device) for _ in range(4))
+        for name, x in zip(("q", "k", "v", "gate"), out):
+            _check_tensor(x, name, self.shape, self.device)
+        args = vsa_preprocess_args_t(
+            _ptr(q_in), _ptr(k_in), _ptr(v_in), _ptr(gate_in), rows_in, row_stride, _ptr(src_row),
+            _ptr(q_norm_weight), _ptr(k_norm_weight), float(eps), int(rope_dim), 1 if rope_interleaved else 0,
+            _ptr(rope_cos) if rope_dim else None, _ptr(rope_sin) if rope_dim else None,
+            *[_ptr(x) for x in out])
+        vsa_preprocess(self.plan, args, self.workspace, stream)
+        return out
+
+    def forward_preprocessed(self, q, k, v, gate, out=None, stream=None):
+        """The forward over tensors packed by ``preprocess`` (same workspace, same stream)."""
+        for name, x in (("q", q), ("k", k), ("v", v), ("gate", gate)):
+            _check_tensor(x, name, self.shape, self.device)
+        if out is None:
+            out = torch.empty(self.shape, dtype=torch.bfloat16, device=self.device)
+        _check_tensor(out, "out", self.shape, self.device)
+        vsa_forward_preprocessed(self.plan, q, k, v, gate, out, self.workspace, stream)
+        return out
+
     def check(self, stream=None):
         vsa_check(self.plan, self.workspace, stream)
 
@@ -268,7 +364,8 @@ class VSA:
 
 __all__ = [
     "VSA", "VsaError", "load_library", "header_functions", "vsa_plan_create", "vsa_plan_info",
-    "vsa_forward", "vsa_forward_host", "vsa_plan_host_path_bytes", "vsa_debug_views", "vsa_check",
+    "vsa_forward", "vsa_forward_host", "vsa_preprocess", "vsa_forward_preprocessed",
+    "vsa_preprocess_args_t", "vsa_plan_host_path_bytes", "vsa_debug_views", "vsa_check",
     "vsa_plan_set_stage_events", "vsa_plan_destroy", "vsa_status_string",
     "vsa_forward_static_workspace", "vsa_diag_wait_timeout",
 ]

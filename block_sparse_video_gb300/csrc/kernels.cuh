@@ -28,6 +28,26 @@ cudaError_t launch_pool(const Geometry& g, const __nv_bfloat16* q, const __nv_bf
                         const __nv_bfloat16* v, float* pooled_q, float* pooled_k,
                         float* pooled_v, cudaStream_t stream);
 
+// Fused attention preprocessing: Q/K RMSNorm, partial RoPE, packing of the
+// projection rows into [B, N, H, 128], gate copy and the Q/K/V tile pooling.
+struct PreprocessArgs {
+  const __nv_bfloat16* in[4];  // q, k, v, gate projections: row r of batch b at in + (b*rows_in + r)*row_stride
+  long long rows_in;           // projection rows per batch
+  long long row_stride;        // elements between projection rows
+  const int32_t* src_row;      // int32 [B, N] or null (row n)
+  const float* q_norm_weight;  // fp32 [H, 128]
+  const float* k_norm_weight;
+  float eps;
+  int rope_dim;                // multiple of 16 in [0, 128]
+  int rope_interleaved;        // pairs (2i, 2i+1) if nonzero, else (i, i + rope_dim/2)
+  const float* rope_cos;       // fp32 [N, rope_dim/2]
+  const float* rope_sin;
+  __nv_bfloat16* out[4];       // packed q, k, v, gate, bf16 [B, N, H, 128]
+  float* pooled[3];            // fp32 [B, H, T, 128]
+  unsigned int* err;           // error words; word 7 records the first bad map entry (token + 1)
+};
+cudaError_t launch_preprocess(const Geometry& g, const PreprocessArgs& a, cudaStream_t stream);
+
 // Coarse attention over pooled tiles fused with the top-k tile selection.
 // coarse fp32 [B, H, T, 128]; tile_index int32 [B, H, T, k] ascending.
 size_t coarse_smem_bytes(const Geometry& g, int* rows_per_cta);

@@ -170,9 +170,16 @@ vsa_status_t vsa_plan_set_stage_events(vsa_plan_t plan, void* const* events) {
   return VSA_OK;
 }
 
-vsa_status_t vsa_forward(vsa_plan_t plan, const void* q, const void* k, const void* v,
-                         const void* gate, void* out, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The forward behind vsa_forward (pool_ready = false: clears every counter and
+// error word, then pools Q/K/V) and vsa_forward_preprocessed (pool_ready = true:
+// the pooled statistics and word 7 come from vsa_preprocess and are kept).
+vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const void* v, const void* gate,
+                          void* out, void* workspace, size_t workspace_bytes, void* stream,
+                          bool pool_ready) {
   if (!plan || !q || !k || !v || !gate || !out || !workspace) return VSA_ERR_INVALID_ARG;
   if (workspace_bytes < plan->ws_bytes || !aligned(workspace, kAlign)) return VSA_ERR_INVALID_ARG;
   const void* ins[4] = {q, k, v, gate};
@@ -203,11 +210,13 @@ vsa_status_t vsa_forward(vsa_plan_t plan, const void* q, const void* k, const vo
   if (plan->num_sms == 0 &&
       cudaDeviceGetAttribute(&plan->num_sms, cudaDevAttrMultiProcessorCount, plan->device) != cudaSuccess)
     return VSA_ERR_CUDA;
-  // error words 0-2, redo count (word 4), the fine kernels' work counters (words 5, 6)
-  if (cudaMemsetAsync(err, 0, 32, st) != cudaSuccess) return VSA_ERR_CUDA;
+  // error words 0-2, redo count (word 4), the fine kernels' work counters (words 5, 6) and,
+  // unless the preprocessing just wrote it, its bad-map-entry word (7)
+  if (cudaMemsetAsync(err, 0, pool_ready ? 28 : 32, st) != cudaSuccess) return VSA_ERR_CUDA;
   vsa_status_t rs = record(plan, 0, st);
   if (rs != VSA_OK) return rs;
-  if (vsa::launch_pool(g, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+  if (!pool_ready &&
+      vsa::launch_pool(g, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
                        static_cast<const __nv_bfloat16*>(v), pq, pk, pv, st) != cudaSuccess)
     return VSA_ERR_CUDA;
   if ((rs = record(plan, 1, st)) != VSA_OK) return rs;
@@ -224,6 +233,88 @@ vsa_status_t vsa_forward(vsa_plan_t plan, const void* q, const void* k, const vo
   a.work_counters = reinterpret_cast<int*>(err + 5);
   if (vsa::launch_fine(g, mq, mk, mv, mg, a, plan->num_sms, st) != cudaSuccess) return VSA_ERR_CUDA;
   return record(plan, 3, st);
+}
+
+// Bytes spanned by one projection input: B * rows_in rows of row_stride elements,
+// the last one read up to its H * 128 channels.
+size_t projection_span(const vsa::Geometry& g, int64_t rows_in, int64_t row_stride) {
+  return (static_cast<size_t>(g.B) * rows_in - 1) * static_cast<size_t>(row_stride) * 2 +
+         static_cast<size_t>(g.H) * vsa::kHeadDim * 2;
+}
+
+}  // namespace
+
+extern "C" {
+
+vsa_status_t vsa_forward(vsa_plan_t plan, const void* q, const void* k, const void* v,
+                         const void* gate, void* out, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  return forward_impl(plan, q, k, v, gate, out, workspace, workspace_bytes, stream, false);
+}
+
+vsa_status_t vsa_forward_preprocessed(vsa_plan_t plan, const void* q, const void* k, const void* v,
+                                      const void* gate, void* out, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  return forward_impl(plan, q, k, v, gate, out, workspace, workspace_bytes, stream, true);
+}
+
+vsa_status_t vsa_preprocess(vsa_plan_t plan, const vsa_preprocess_args_t* args, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (!plan || !args || !workspace) return VSA_ERR_INVALID_ARG;
+  const vsa_preprocess_args_t& x = *args;
+  const vsa::Geometry& g = plan->g;
+  if (workspace_bytes < plan->ws_bytes || !aligned(workspace, kAlign)) return VSA_ERR_INVALID_ARG;
+  const void* ins[4] = {x.q_in, x.k_in, x.v_in, x.gate_in};
+  void* outs[4] = {x.q_out, x.k_out, x.v_out, x.gate_out};
+  if (x.rows_in < 1 || x.row_stride < static_cast<int64_t>(g.H) * vsa::kHeadDim || x.row_stride % 8 != 0)
+    return VSA_ERR_INVALID_ARG;
+  if (!x.src_row && x.rows_in < g.N) return VSA_ERR_INVALID_ARG;
+  if (x.rows_in > kMaxTokens * 4 || x.row_stride > (int64_t(1) << 24)) return VSA_ERR_UNSUPPORTED;
+  if (x.src_row && !aligned(x.src_row, 4)) return VSA_ERR_INVALID_ARG;
+  if (!x.q_norm_weight || !x.k_norm_weight || !aligned(x.q_norm_weight, 4) || !aligned(x.k_norm_weight, 4))
+    return VSA_ERR_INVALID_ARG;
+  if (!(std::isfinite(x.eps) && x.eps > 0.f)) return VSA_ERR_INVALID_ARG;
+  if (x.rope_dim < 0 || x.rope_dim > vsa::kHeadDim || x.rope_dim % 16 != 0) return VSA_ERR_INVALID_ARG;
+  if (x.rope_dim > 0 && (!x.rope_cos || !x.rope_sin || !aligned(x.rope_cos, 16) || !aligned(x.rope_sin, 16)))
+    return VSA_ERR_INVALID_ARG;
+  const size_t span = projection_span(g, x.rows_in, x.row_stride);
+  const size_t tb = plan->tensor_bytes;
+  for (int i = 0; i < 4; ++i) {
+    if (!ins[i] || !outs[i] || !aligned(ins[i], 16) || !aligned(outs[i], 16)) return VSA_ERR_INVALID_ARG;
+    if (overlaps(outs[i], tb, workspace, plan->ws_bytes)) return VSA_ERR_INVALID_ARG;
+    for (int j = 0; j < 4; ++j) {
+      if (overlaps(outs[i], tb, ins[j], span)) return VSA_ERR_INVALID_ARG;
+      if (j > i && overlaps(outs[i], tb, outs[j], tb)) return VSA_ERR_INVALID_ARG;
+    }
+  }
+
+  DeviceGuard guard(plan->device);
+  if (!guard.ok) return VSA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  unsigned int* err = reinterpret_cast<unsigned int*>(ws + plan->off_err);
+  // a preprocessing starts a new call sequence: every error word and counter starts at zero
+  if (cudaMemsetAsync(err, 0, 32, st) != cudaSuccess) return VSA_ERR_CUDA;
+  vsa::PreprocessArgs a;
+  for (int i = 0; i < 4; ++i) {
+    a.in[i] = static_cast<const __nv_bfloat16*>(ins[i]);
+    a.out[i] = static_cast<__nv_bfloat16*>(outs[i]);
+  }
+  a.rows_in = x.rows_in;
+  a.row_stride = x.row_stride;
+  a.src_row = x.src_row;
+  a.q_norm_weight = x.q_norm_weight;
+  a.k_norm_weight = x.k_norm_weight;
+  a.eps = x.eps;
+  a.rope_dim = x.rope_dim;
+  a.rope_interleaved = x.rope_interleaved;
+  a.rope_cos = x.rope_cos;
+  a.rope_sin = x.rope_sin;
+  a.pooled[0] = reinterpret_cast<float*>(ws + plan->off_pq);
+  a.pooled[1] = reinterpret_cast<float*>(ws + plan->off_pk);
+  a.pooled[2] = reinterpret_cast<float*>(ws + plan->off_pv);
+  a.err = err;
+  return vsa::launch_preprocess(g, a, st) == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
 vsa_status_t vsa_plan_host_path_bytes(vsa_plan_t plan, size_t* bytes) {
@@ -276,13 +367,14 @@ vsa_status_t vsa_check(vsa_plan_t plan, void* workspace, void* stream) {
   if (!guard.ok) return VSA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return VSA_ERR_CUDA;
-  unsigned int words[3] = {0, 0, 0};
+  unsigned int words[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   if (cudaMemcpy(words, static_cast<uint8_t*>(workspace) + plan->off_err, sizeof(words),
                  cudaMemcpyDeviceToHost) != cudaSuccess)
     return VSA_ERR_CUDA;
-  if (words[0] == 0) return VSA_OK;
   if (words[0] == static_cast<unsigned int>(VSA_ERR_DEVICE_TIMEOUT)) return VSA_ERR_DEVICE_TIMEOUT;
-  return VSA_ERR_INTERNAL;
+  if (words[0] != 0) return VSA_ERR_INTERNAL;
+  if (words[7] != 0) return VSA_ERR_INVALID_ARG;  // a preprocessing map entry outside its buffer
+  return VSA_OK;
 }
 
 void vsa_plan_destroy(vsa_plan_t plan) { delete plan; }

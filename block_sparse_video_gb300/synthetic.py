@@ -111,3 +111,72 @@ def bf16_bits(t: torch.Tensor):
     """The raw bf16 bit patterns of a CPU tensor as a numpy uint16 array (no conversion)."""
     assert t.dtype == torch.bfloat16
     return t.contiguous().view(torch.int16).numpy().view("uint16")
+
+
+# ---------------------------------------------------------------- preprocessing inputs
+#
+# Recipe for the fused-preprocessing inputs (the projections before Q/K norm and
+# RoPE, as "Fused attention preprocessing" receives them):
+# * one merged bf16 projection buffer [B, rows_in, 4, H, 128] (Q, K, V, gate
+#   side by side in each row, as one merged projection writes them), values
+#   N(0, 1) times a per-(row, tensor, head) scale exp(N(0, 0.5^2)), so rows
+#   differ in RMS. rows_in is a capacity that may exceed the token count;
+# * RMSNorm weights 1 + N(0, 0.1^2), fp32 [H, 128], one set for Q and one for K;
+# * RoPE tables for 3-D positions: video token v sits at (frame, y, x) of a
+#   24 x 42 latent grid per frame (1,008 tokens a frame: 72 frames are the
+#   72,576 tokens of a 10 s request at 1344 x 768). Text and audio token n sit
+#   at (n, 0, 0). The rope_dim / 2 angles split evenly over the three axes,
+#   with frequencies 10000^(-j / per_axis);
+# * a row map: a random injective choice of projection rows for the tokens.
+
+FRAME_GRID = (24, 42)
+
+
+def make_projections(batch, rows_in, heads, seed, device="cpu", head_dim=HEAD_DIM):
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    x = torch.randn((batch, rows_in, 4, heads, head_dim), generator=gen, device=device, dtype=torch.float32)
+    scale = torch.exp(0.5 * torch.randn((batch, rows_in, 4, heads, 1), generator=gen, device=device,
+                                        dtype=torch.float32))
+    return (x * scale).to(torch.bfloat16)
+
+
+def make_norm_weights(heads, seed, head_dim=HEAD_DIM):
+    gen = torch.Generator()
+    gen.manual_seed(int(seed))
+    w = 1.0 + 0.1 * torch.randn((2, heads, head_dim), generator=gen, dtype=torch.float32)
+    return w[0].contiguous(), w[1].contiguous()
+
+
+def rope_positions(len_text, len_audio, len_video):
+    """int64 [N, 3] (frame, y, x) position of each token, segments text | audio | video."""
+    prefix = len_text + len_audio
+    pos = torch.zeros((prefix + len_video, 3), dtype=torch.int64)
+    pos[:prefix, 0] = torch.arange(prefix)
+    v = torch.arange(len_video)
+    per_frame = FRAME_GRID[0] * FRAME_GRID[1]
+    pos[prefix:, 0] = v // per_frame
+    pos[prefix:, 1] = (v % per_frame) // FRAME_GRID[1]
+    pos[prefix:, 2] = v % FRAME_GRID[1]
+    return pos
+
+
+def make_rope_tables(len_text, len_audio, len_video, rope_dim):
+    """fp32 (cos, sin), each [N, rope_dim / 2], for the 3-D positions above."""
+    half = rope_dim // 2
+    pos = rope_positions(len_text, len_audio, len_video).to(torch.float64)
+    per_axis = [half // 3 + (1 if a < half % 3 else 0) for a in range(3)]
+    angles = []
+    for axis, m in enumerate(per_axis):
+        freq = 10000.0 ** (-torch.arange(m, dtype=torch.float64) / max(m, 1))
+        angles.append(pos[:, axis:axis + 1] * freq[None])
+    th = torch.cat(angles, dim=1) if half else torch.zeros((pos.shape[0], 0), dtype=torch.float64)
+    return torch.cos(th).to(torch.float32).contiguous(), torch.sin(th).to(torch.float32).contiguous()
+
+
+def make_row_map(batch, n_tokens, rows_in, seed):
+    """int32 [B, N]: distinct projection rows, a random choice per batch."""
+    gen = torch.Generator()
+    gen.manual_seed(int(seed))
+    return torch.stack([torch.randperm(rows_in, generator=gen)[:n_tokens] for _ in range(batch)]).to(torch.int32)

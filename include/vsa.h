@@ -104,6 +104,73 @@ vsa_status_t vsa_forward(vsa_plan_t plan, const void* q, const void* k, const vo
                          const void* gate, void* out, void* workspace, size_t workspace_bytes,
                          void* stream);
 
+/* Fused attention preprocessing ("UniServe: serving FastH3 at its fastest",
+ * section "Fused attention preprocessing"; section "The Kernel Layer" gives the
+ * rotary width of 96 channels and the rounding of the normalised value before
+ * RoPE). One pass over the projected Q/K/V/gate rows does the following:
+ *   - packs each attention token's row into the [batch, N, num_heads, 128]
+ *     layout the forward reads;
+ *   - applies RMSNorm to Q and K, per token and head over the head's 128
+ *     channels: y = x / sqrt(mean(x^2) + eps) * weight[head][channel];
+ *   - rounds the result to bf16 and rotates channels [0, rope_dim) of every
+ *     head: the pair (a, b) at token n becomes (a cos - b sin, a sin + b cos),
+ *     with cos and sin from the tables; the result is rounded to bf16 (RNE);
+ *   - copies V and the gate;
+ *   - writes the FP32 tile means of the packed Q, K and V (over each video
+ *     tile's valid tokens) into the workspace, where vsa_forward_preprocessed
+ *     reads them.
+ * Padding rows of the projection buffer are never read unless the map points
+ * at them. */
+typedef struct {
+  /* Projections, device, bf16. Channel c of head h of projection row r of
+   * batch b is at ptr + (b * rows_in + r) * row_stride + h * 128 + c (elements).
+   * 16-byte aligned. The four may share one buffer (e.g. one merged projection
+   * with row_stride = 4 * num_heads * 128). */
+  const void* q_in;
+  const void* k_in;
+  const void* v_in;
+  const void* gate_in;
+  int64_t rows_in;    /* projection rows per batch (capacity, may include padding), >= 1 */
+  int64_t row_stride; /* elements between projection rows: >= num_heads * 128, multiple of 8 */
+  /* Device int32 [batch, N]: the projection row of attention token n (segments
+   * text | audio | video). NULL means row n (then rows_in >= N). An entry outside
+   * [0, rows_in) gives a zero row, and vsa_check reports VSA_ERR_INVALID_ARG. */
+  const int32_t* src_row;
+  const float* q_norm_weight; /* device fp32 [num_heads, 128] */
+  const float* k_norm_weight; /* device fp32 [num_heads, 128] */
+  float eps;                  /* > 0 */
+  int32_t rope_dim;           /* rotated channels per head: multiple of 16 in [0, 128] */
+  int32_t rope_interleaved;   /* nonzero: pairs (2i, 2i+1); zero: pairs (i, i + rope_dim/2) */
+  /* Device fp32 [N, rope_dim / 2], 16-byte aligned: cos and sin of the angle
+   * of pair i at attention token n (any 1-D or 3-D position encoding). Unused
+   * when rope_dim = 0. */
+  const float* rope_cos;
+  const float* rope_sin;
+  /* Outputs, device bf16 [batch, N, num_heads, 128], 16-byte aligned. They must
+   * not overlap one another, any input or the workspace. */
+  void* q_out;
+  void* k_out;
+  void* v_out;
+  void* gate_out;
+} vsa_preprocess_args_t;
+
+/* Enqueue the fused preprocessing on `stream`. `workspace` is this plan's
+ * forward workspace (vsa_plan_info): the pooled statistics go there, and its
+ * error words are cleared first. Argument
+ * errors are returned synchronously and nothing is launched. Allocates nothing,
+ * does not synchronise and reads no device data on the host, so it is
+ * capture-safe. */
+vsa_status_t vsa_preprocess(vsa_plan_t plan, const vsa_preprocess_args_t* args, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* vsa_forward for inputs packed by vsa_preprocess into the same workspace on
+ * the same stream: skips the tile pool (the pooled statistics are already in
+ * the workspace) and keeps the preprocessing's error report for vsa_check.
+ * Three kernels; otherwise as vsa_forward. */
+vsa_status_t vsa_forward_preprocessed(vsa_plan_t plan, const void* q, const void* k, const void* v,
+                                      const void* gate, void* out, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
 /* Same forward on HOST buffers (q, k, v, gate read, out written, all bf16
  * [batch, N, num_heads, 128]; pinned memory makes the copies asynchronous).
  * `device_buffer` (>= host_path_bytes from vsa_plan_host_path_bytes, 256-byte
@@ -124,7 +191,8 @@ vsa_status_t vsa_debug_views(vsa_plan_t plan, void* workspace, const float** poo
                              const int32_t** tile_index, const float** coarse);
 
 /* Synchronise `stream` and report the device error words of `workspace`:
- * VSA_OK, or VSA_ERR_DEVICE_TIMEOUT if a bounded wait gave up. */
+ * VSA_OK; VSA_ERR_DEVICE_TIMEOUT if a bounded wait gave up; VSA_ERR_INVALID_ARG
+ * if the last vsa_preprocess met a map entry outside its projection buffer. */
 vsa_status_t vsa_check(vsa_plan_t plan, void* workspace, void* stream);
 
 /* Optional per-kernel timing. When `events` is non-NULL, each vsa_forward

@@ -96,3 +96,55 @@ def test_status_strings(lib):
     for s in range(6):
         assert bsv.vsa_status_string(s)
     assert "timed out" in bsv.vsa_status_string(bsv.VSA_ERR_DEVICE_TIMEOUT)
+
+
+def _pre_args(**kw):
+    """A vsa_preprocess_args_t with well-formed fake device addresses (never
+    dereferenced: every case below is rejected on the host)."""
+    g = 1 << 32
+    a = dict(q_in=1 * g, k_in=1 * g + 256, v_in=1 * g + 512, gate_in=1 * g + 768, rows_in=2000,
+             row_stride=4 * 2 * 128, src_row=None, q_norm_weight=3 * g, k_norm_weight=3 * g + 4096,
+             eps=1e-6, rope_dim=96, rope_interleaved=1, rope_cos=4 * g, rope_sin=5 * g,
+             q_out=6 * g, k_out=7 * g, v_out=8 * g, gate_out=9 * g)
+    a.update(kw)
+    return bsv.vsa_preprocess_args_t(**a)
+
+
+def test_preprocess_rejects_bad_arguments_without_launching(lib):
+    plan = bsv.vsa_plan_create(1, 2, 64, 64, 1024, 0.2)  # N = 1152
+    try:
+        _, _, ws = bsv.vsa_plan_info(plan)
+        wsp = ctypes.c_void_p(10 << 32)
+
+        def st(**kw):
+            return lib.vsa_preprocess(plan, ctypes.byref(_pre_args(**kw)), wsp, ws, None)
+
+        bad = [
+            dict(rows_in=1000),                    # no map and fewer rows than tokens
+            dict(rows_in=0, src_row=11 << 32),
+            dict(row_stride=2 * 128 - 8),          # shorter than one row of all heads
+            dict(row_stride=4 * 2 * 128 + 4),      # not a multiple of 8 elements
+            dict(eps=0.0), dict(eps=float("nan")),
+            dict(rope_dim=90), dict(rope_dim=144), dict(rope_dim=-16),
+            dict(rope_cos=None),
+            dict(rope_sin=(5 << 32) + 4),          # misaligned table
+            dict(q_norm_weight=None),
+            dict(k_in=(1 << 32) + 8),              # misaligned input
+            dict(v_out=None),
+            dict(gate_out=6 << 32),                # two outputs alias
+            dict(q_out=(1 << 32) + 1024),          # output inside the input rows
+            dict(src_row=(11 << 32) + 2),          # misaligned map
+        ]
+        for kw in bad:
+            assert st(**kw) == bsv.VSA_ERR_INVALID_ARG, kw
+        assert st(row_stride=1 << 25) == bsv.VSA_ERR_UNSUPPORTED
+        assert lib.vsa_preprocess(plan, None, wsp, ws, None) == bsv.VSA_ERR_INVALID_ARG
+        assert lib.vsa_preprocess(plan, ctypes.byref(_pre_args()), wsp, ws - 1, None) == bsv.VSA_ERR_INVALID_ARG
+        # an output overlapping the workspace
+        assert lib.vsa_preprocess(plan, ctypes.byref(_pre_args(k_out=10 << 32)), wsp, ws,
+                                  None) == bsv.VSA_ERR_INVALID_ARG
+        f = lib.vsa_forward_preprocessed
+        fake = ctypes.c_void_p(1 << 20)
+        assert f(plan, None, fake, fake, fake, fake, fake, ws, None) == bsv.VSA_ERR_INVALID_ARG
+    finally:
+        bsv.vsa_plan_destroy(plan)
