@@ -176,6 +176,58 @@ def measure_preprocess(op, cfg, dev, stream, flush, steps, warmup, peaks, world)
             "fused_chain": "vsa_preprocess + vsa_forward_preprocessed (coarse + top-k, fine fast, fine exact)"}
 
 
+# SubBlock-routed forwards measured beside the VSA forward (the page's profiles)
+SUBBLOCK_SPARSITY = (0.75, 0.8)
+
+
+def subblock_keep(t, sparsity):
+    """Kept key tiles: at most floor(s T) dropped, rounded up to a multiple of 8."""
+    need = t - int(np.floor(sparsity * t))
+    return min(t, 8 * (-(-need // 8)))
+
+
+def subblock_flops(cfg, sparsity):
+    """Fine FLOPs of the SubBlock pattern (4*D per attended pair; the 10 s video is
+    tile-aligned) and the router's sub-block logits (2*D per sub-block pair)."""
+    d, p, lv, t = 128, cfg.prefix, cfg.len_video, cfg.n_video_tiles
+    k = subblock_keep(t, sparsity)
+    bh = cfg.batch * cfg.heads
+    fine = 4 * d * bh * (lv * (p + 64 * k) + p * (p + lv))
+    router = 2 * d * bh * (4 * t) ** 2
+    return k, float(fine), float(router)
+
+
+def measure_subblock(q, k, v, cfg, dev, stream, flush, steps, warmup, peaks, world, sparsity):
+    """Time one SubBlock-routed forward per step (sub-block pool, router, fine fast
+    and exact passes) with per-stage device events, L2 flushed before each step."""
+    import block_sparse_video_gb300 as bsv
+    op = bsv.SubBlock(cfg.batch, cfg.heads, cfg.len_text, cfg.len_audio, cfg.len_video, sparsity, device=dev)
+    out = torch.empty_like(q)
+    for _ in range(warmup):
+        op(q, k, v, out=out)
+    op.check()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        bsv.vsa_plan_set_stage_events(op.plan, ev[i])
+        op(q, k, v, out=out)
+    torch.cuda.synchronize(dev)
+    bsv.vsa_plan_set_stage_events(op.plan, None)
+    op.check()
+    stage = [reduce_max(statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev), world, dev) for j in range(3)]
+    total = reduce_max(statistics.mean(e[0].elapsed_time(e[3]) for e in ev), world, dev)
+    kk, fine_fl, router_fl = subblock_flops(cfg, sparsity)
+    sustained = peaks["bf16_tflops_sustained"]
+    del out, op
+    return {"sparsity": sparsity, "kept_tiles": kk, "ms": total, "subpool_ms": stage[0],
+            "router_ms": stage[1], "fine_ms": stage[2],
+            "fine_TFLOP_s": fine_fl / (stage[2] * 1e-3) / 1e12,
+            "fine_frac_of_bf16_sustained": fine_fl / (stage[2] * 1e-3) / 1e12 / sustained,
+            "effective_TFLOP_s": fine_fl / (total * 1e-3) / 1e12,
+            "router_flops": router_fl, "router_TFLOP_s": router_fl / (stage[1] * 1e-3) / 1e12,
+            "launches_per_forward": 4}
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -403,6 +455,12 @@ def run_ours(args):
         except Exception:
             traffic = None
 
+    # ---- SubBlock-routed forwards on the same inputs (measured on their own)
+    subblock = None
+    if not args.no_subblock:
+        subblock = [measure_subblock(q, k, v, cfg, dev, stream, flush, steps, args.warmup, peaks, world, s)
+                    for s in SUBBLOCK_SPARSITY]
+
     # ---- fused preprocessing, measured on its own (not part of the forward step above)
     pre = None
     if not args.no_preprocess:
@@ -461,6 +519,7 @@ def run_ours(args):
                                      "kv_l2_to_smem_TB_s": kv_stream_bytes(cfg, keep) / (fine_ms * 1e-3) / 1e12},
                 "preprocess_kernel": pre,
             },
+            "subblock": subblock,
             "clocks": clocks,
             "e2e": e2e,
             "gpu_launches": LAUNCHES_PER_FORWARD * steps,
@@ -489,6 +548,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-subblock", action="store_true",
+                    help="skip the separate SubBlock-routed forward measurements")
     ap.add_argument("--no-preprocess", action="store_true",
                     help="skip the separate fused-preprocessing measurement")
     ap.add_argument("--workload", choices=["10s", "5s", "medium"], default="10s",

@@ -84,6 +84,8 @@ def load_library(path: str = LIB_PATH):
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     sig = {
         "vsa_plan_create": (i32, [ctypes.POINTER(vsa_shape_t), ctypes.c_int, ctypes.POINTER(vp)]),
+        "vsa_plan_create_subblock": (i32, [ctypes.POINTER(vsa_shape_t), ctypes.c_double, ctypes.c_int,
+                                           ctypes.POINTER(vp)]),
         "vsa_plan_info": (i32, [vp, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(sz)]),
         "vsa_forward": (i32, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "vsa_preprocess": (i32, [vp, ctypes.POINTER(vsa_preprocess_args_t), vp, sz, vp]),
@@ -144,6 +146,16 @@ def vsa_plan_create(batch, num_heads, len_text, len_audio, len_video, keep_fract
     return out.value
 
 
+def vsa_plan_create_subblock(batch, num_heads, len_text, len_audio, len_video, sparsity, head_dim=128,
+                             device=0):
+    """Plan whose selection is the SubBlock router (see vsa.h). Host only."""
+    shape = vsa_shape_t(batch, num_heads, head_dim, len_text, len_audio, len_video, 1.0)
+    out = ctypes.c_void_p()
+    _check(load_library().vsa_plan_create_subblock(ctypes.byref(shape), float(sparsity), int(device),
+                                                   ctypes.byref(out)), "vsa_plan_create_subblock")
+    return out.value
+
+
 def vsa_plan_info(plan):
     """(n_tiles T, kept tiles k, workspace bytes)."""
     t, k, ws = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_size_t()
@@ -171,7 +183,8 @@ def _check_tensor(x, name, shape, device=None):
 
 
 def vsa_forward(plan, q, k, v, gate, out, workspace, stream=None):
-    """Enqueue the forward on ``stream`` (default: torch's current stream)."""
+    """Enqueue the forward on ``stream`` (default: torch's current stream).
+    ``gate`` may be None for a SubBlock plan."""
     _check(load_library().vsa_forward(plan, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out),
                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _stream_handle(stream)), "vsa_forward")
@@ -265,6 +278,11 @@ class VSA:
 
     def __init__(self, batch, num_heads, len_text, len_audio, len_video, keep_fraction=0.2,
                  device="cuda"):
+        idx = self._setup(batch, num_heads, len_text, len_audio, len_video, device)
+        self._finish(vsa_plan_create(batch, num_heads, len_text, len_audio, len_video, keep_fraction,
+                                     device=idx))
+
+    def _setup(self, batch, num_heads, len_text, len_audio, len_video, device):
         self.device = torch.device(device)
         if self.device.type != "cuda":
             raise ValueError("the VSA forward runs on a CUDA device only")
@@ -273,8 +291,10 @@ class VSA:
         self.batch, self.num_heads = batch, num_heads
         self.len_text, self.len_audio, self.len_video = len_text, len_audio, len_video
         self.seq = len_text + len_audio + len_video
-        self.plan = vsa_plan_create(batch, num_heads, len_text, len_audio, len_video, keep_fraction,
-                                    device=idx)
+        return idx
+
+    def _finish(self, plan):
+        self.plan = plan
         self.n_tiles, self.k, self.workspace_bytes = vsa_plan_info(self.plan)
         self.workspace = torch.empty(self.workspace_bytes, dtype=torch.uint8, device=self.device)
 
@@ -362,8 +382,51 @@ class VSA:
             pass
 
 
+class SubBlock(VSA):
+    """Owner of a SubBlock-routed plan ("How SubBlock Sparse Attention Works"):
+    video query tiles keep the k video key tiles of highest estimated softmax
+    mass; no coarse branch and no gate. ``sparsity`` is the fraction of key
+    tiles that may be dropped."""
+
+    def __init__(self, batch, num_heads, len_text, len_audio, len_video, sparsity=0.75, device="cuda"):
+        idx = self._setup(batch, num_heads, len_text, len_audio, len_video, device)
+        self.sparsity = sparsity
+        self._finish(vsa_plan_create_subblock(batch, num_heads, len_text, len_audio, len_video, sparsity,
+                                              device=idx))
+
+    def forward(self, q, k, v, gate=None, out=None, stream=None):
+        for name, x in (("q", q), ("k", k), ("v", v)):
+            _check_tensor(x, name, self.shape, self.device)
+        if out is None:
+            out = torch.empty(self.shape, dtype=torch.bfloat16, device=self.device)
+        _check_tensor(out, "out", self.shape, self.device)
+        vsa_forward(self.plan, q, k, v, None, out, self.workspace, stream)
+        return out
+
+    __call__ = forward
+
+    def debug_views(self):
+        """sub_q, sub_k: fp32 [B, H, 4T, 128] sub-block means; tile_index: int32 [B, H, T, k]."""
+        ptrs = [ctypes.c_void_p() for _ in range(5)]
+        _check(load_library().vsa_debug_views(self.plan, _ptr(self.workspace), *[ctypes.byref(p) for p in ptrs]),
+               "vsa_debug_views")
+        flat = self.workspace.view(torch.uint8)
+        base = self.workspace.data_ptr()
+        b, h, t, k = self.batch, self.num_heads, self.n_tiles, self.k
+
+        def view(ptr, n_elem, dtype, shape):
+            off = ptr.value - base
+            nbytes = n_elem * torch.tensor([], dtype=dtype).element_size()
+            return flat[off:off + nbytes].view(dtype).view(*shape)
+
+        sub = b * h * 4 * t * 128
+        return dict(sub_q=view(ptrs[0], sub, torch.float32, (b, h, 4 * t, 128)),
+                    sub_k=view(ptrs[1], sub, torch.float32, (b, h, 4 * t, 128)),
+                    tile_index=view(ptrs[3], b * h * t * k, torch.int32, (b, h, t, k)))
+
+
 __all__ = [
-    "VSA", "VsaError", "load_library", "header_functions", "vsa_plan_create", "vsa_plan_info",
+    "VSA", "SubBlock", "VsaError", "vsa_plan_create_subblock", "load_library", "header_functions", "vsa_plan_create", "vsa_plan_info",
     "vsa_forward", "vsa_forward_host", "vsa_preprocess", "vsa_forward_preprocessed",
     "vsa_preprocess_args_t", "vsa_plan_host_path_bytes", "vsa_debug_views", "vsa_check",
     "vsa_plan_set_stage_events", "vsa_plan_destroy", "vsa_status_string",

@@ -20,6 +20,7 @@
 // tile ids ascending. Results are deterministic: the histograms are counts, and
 // the compaction follows tile order.
 #include "kernels.cuh"
+#include "tf32_select.cuh"
 
 namespace vsa {
 namespace {
@@ -30,15 +31,6 @@ constexpr int kChunk = 64;            // pooled tiles staged per step
 constexpr int kQPad = kHeadDim + 4;   // q rows and K chunk rows (floats): conflict-free fragment loads
 constexpr int kVPad = kHeadDim + 8;   // V chunk rows
 constexpr size_t kSmemBudget = 220 * 1024;
-constexpr int kBins = 256;            // radix-select histogram, one per warp
-
-// Order-preserving map from fp32 to uint32 (larger float -> larger key);
-// -0 and +0 map to the same key.
-__device__ __forceinline__ uint32_t order_key(float s) {
-  uint32_t u = __float_as_uint(s);
-  if (u == 0x80000000u) u = 0u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 __device__ __forceinline__ void load_rows(float* dst, const float* src, int first, int count, int rows,
                                           int pad) {
@@ -50,29 +42,6 @@ __device__ __forceinline__ void load_rows(float* dst, const float* src, int firs
       x = __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(first + r) * kHeadDim) + c4);
     *reinterpret_cast<float4*>(dst + r * pad + 4 * c4) = x;
   }
-}
-
-// x = hi + lo with hi and lo tf32 values (hi rounded to nearest)
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
-  const float r = x - __uint_as_float(hi);
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
-}
-
-__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// c += a b for a 16x8 (A) by 8x8 (B) step, from split operands (small terms first)
-__device__ __forceinline__ void mma_split(float (&c)[4], const uint32_t (&ahi)[4], const uint32_t (&alo)[4],
-                                          uint32_t bhi0, uint32_t bhi1, uint32_t blo0, uint32_t blo1) {
-  mma_tf32(c, alo, bhi0, bhi1);
-  mma_tf32(c, ahi, blo0, blo1);
-  mma_tf32(c, ahi, bhi0, bhi1);
 }
 
 // Next K or V chunk, fetched into registers (one float4 per thread and step)
@@ -99,23 +68,6 @@ __device__ __forceinline__ void stash_chunk(float* dst, const float4 (&pre)[kChu
     const int r = e / (kHeadDim / 4), c4 = e % (kHeadDim / 4);
     *reinterpret_cast<float4*>(dst + r * pad + 4 * c4) = pre[i];
   }
-}
-
-// Fragment layouts of m16n8k8 (lane = 4 g + t4): A (16 x 8, row-major) holds
-// (g, t4), (g + 8, t4), (g, t4 + 4), (g + 8, t4 + 4); B (8 x 8, k x n) holds
-// (t4, g), (t4 + 4, g); C (16 x 8) holds (g, 2 t4), (g, 2 t4 + 1), (g + 8, 2 t4),
-// (g + 8, 2 t4 + 1).
-__device__ __forceinline__ void load_a_split(const float* base, int stride, int rows_valid, int g, int t4,
-                                             uint32_t (&hi)[4], uint32_t (&lo)[4]) {
-  // base points at row 0, column t4-aligned step start; rows >= rows_valid read as zero
-  const float x0 = g < rows_valid ? base[g * stride + t4] : 0.f;
-  const float x1 = g + 8 < rows_valid ? base[(g + 8) * stride + t4] : 0.f;
-  const float x2 = g < rows_valid ? base[g * stride + t4 + 4] : 0.f;
-  const float x3 = g + 8 < rows_valid ? base[(g + 8) * stride + t4 + 4] : 0.f;
-  split_tf32(x0, hi[0], lo[0]);
-  split_tf32(x1, hi[1], lo[1]);
-  split_tf32(x2, hi[2], lo[2]);
-  split_tf32(x3, hi[3], lo[3]);
 }
 
 template <int R>
@@ -178,74 +130,11 @@ coarse_topk_kernel(const float* __restrict__ pooled_q, const float* __restrict__
 
   // ---- per row: radix select of the k-th largest key, ordered compaction, softmax
   const unsigned full = 0xffffffffu;
-  const unsigned lt_mask = (1u << lane) - 1u;
   for (int r = warp; r < R; r += kWarps) {
     float* row = S + r * sstride;
     const int t = t0 + r;
-    if (t < T) {
-      // radix select, 8 bits per pass from the top: prefix holds the digits of
-      // the k-th largest key fixed so far, rem how many keys above it are
-      // still to be taken among those that match the prefix
-      int* h = hist + warp * kBins;
-      uint32_t prefix = 0u, pmask = 0u;
-      int rem = k;
-#pragma unroll 1
-      for (int shift = 24; shift >= 0; shift -= 8) {
-#pragma unroll
-        for (int b = lane; b < kBins; b += 32) h[b] = 0;
-        __syncwarp();
-        for (int j = lane; j < T; j += 32) {
-          const uint32_t key = order_key(row[j]);
-          if ((key & pmask) == prefix) atomicAdd(&h[(key >> shift) & 0xFFu], 1);
-        }
-        __syncwarp();
-        // lane l owns bins 255 - 8l .. 248 - 8l (descending); find the bin where
-        // the count from the top first reaches rem
-        int c[8], lsum = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) { c[i] = h[255 - 8 * lane - i]; lsum += c[i]; }
-        int incl = lsum;  // inclusive prefix over lanes 0..lane
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(full, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const int excl = incl - lsum;
-        const unsigned hit = __ballot_sync(full, excl < rem && incl >= rem);
-        const int src = __ffs(hit) - 1;
-        int digit = 0, above = 0;
-        if (lane == src) {
-          int run = excl;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (run + c[i] >= rem) { digit = 255 - 8 * lane - i; above = run; break; }
-            run += c[i];
-          }
-        }
-        digit = __shfl_sync(full, digit, src);
-        above = __shfl_sync(full, above, src);
-        prefix |= static_cast<uint32_t>(digit) << shift;
-        pmask |= 0xFFu << shift;
-        rem -= above;
-        __syncwarp();
-      }
-      const uint32_t thr = prefix;  // the k-th largest key
-      const int need_eq = rem;      // how many keys equal to thr are taken (lowest tile ids first)
-      int written = 0, eq_seen = 0;
-      int32_t* dst = tile_index + (bh * T + t) * static_cast<size_t>(k);
-      for (int base = 0; base < T; base += 32) {
-        const int j = base + lane;
-        const uint32_t key = j < T ? order_key(row[j]) : 0u;
-        const bool is_gt = j < T && key > thr;
-        const bool is_eq = j < T && key == thr;
-        const unsigned eqb = __ballot_sync(full, is_eq);
-        const bool sel = is_gt || (is_eq && eq_seen + __popc(eqb & lt_mask) < need_eq);
-        const unsigned selb = __ballot_sync(full, sel);
-        if (sel) dst[written + __popc(selb & lt_mask)] = j;
-        written += __popc(selb);
-        eq_seen += __popc(eqb);
-      }
-    }
+    if (t < T)
+      warp_select_topk(row, T, k, hist + warp * kBins, tile_index + (bh * T + t) * static_cast<size_t>(k), lane);
     // softmax over the T tiles (probabilities overwrite the scores)
     float m = -INFINITY;
     for (int j = lane; j < T; j += 32) m = fmaxf(m, row[j]);

@@ -6,7 +6,9 @@
 //   * a prefix (text/audio) query tile attends to every key tile: the TP
 //     prefix tiles, then the T video tiles; its output is the attention alone;
 //   * a video query tile t attends to the TP prefix tiles and to its k selected
-//     video tiles; its output adds sigmoid(gate) * coarse[t] per channel.
+//     video tiles; its output adds sigmoid(gate) * coarse[t] per channel. With
+//     no coarse input (the SubBlock router's selection, section "How SubBlock
+//     Sparse Attention Works") the output is the attention alone.
 // Key tiles are processed two at a time (a 128-key block).
 //
 // Persistent kernel: one CTA per SM takes items from a global counter until
@@ -113,7 +115,7 @@ struct FineParams {
   float scale_log2;
   const __nv_bfloat16* gate;
   __nv_bfloat16* out;
-  const float* coarse;
+  const float* coarse;  // null: no gated coarse term on video rows (SubBlock routing)
   const int32_t* tile_index;
   unsigned int* err;
   int* work_counter;    // next work index to hand out (zeroed before the launch)
@@ -306,7 +308,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         // the epilogue, an item's duration later).
         tma_prefetch_l2_4d(&map_q, 0, it.h, it.q_row0, it.b);
         tma_prefetch_l2_4d(&map_q, 64, it.h, it.q_row0, it.b);
-        if (it.video) {
+        if (it.video && p.coarse) {
           tma_prefetch_l2_4d(&map_g, 0, it.h, it.q_row0, it.b);
           tma_prefetch_l2_4d(&map_g, 64, it.h, it.q_row0, it.b);
           bulk_prefetch_l2(p.coarse + ((static_cast<size_t>(it.b) * p.H + it.h) * p.T + it.t) * kHeadDim,
@@ -637,7 +639,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       auto prefetch_gate = [&]() {
 #pragma unroll
         for (int c = 0; c < kCols; ++c) gv[c] = 0.f;
-        if (it.video) {
+        if (it.video && p.coarse) {
           cz = __ldg(p.coarse + ((static_cast<size_t>(it.b) * p.H + it.h) * p.T + it.t) * kHeadDim + r);
 #pragma unroll
           for (int c = 0; c < kCols; ++c)
@@ -682,7 +684,8 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         const int pos = atomicAdd(p.redo_count, 1);  // at most once per item: pos < n_items
         p.redo_list[pos] = item;
       }
-      // ---- epilogue: out = O / l (+ sigmoid(gate) * coarse on video rows)
+      // ---- epilogue: out = O / l (+ sigmoid(gate) * coarse on video rows, unless
+      // there is no coarse term: SubBlock routing)
       float l[kCols];
 #pragma unroll
       for (int j = 0; j < kCols / 2; ++j) {
@@ -712,7 +715,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             const float4 x = reinterpret_cast<const float4*>(red)[wg * kCols + c];
             const float lsum = (x.x + x.y) + (x.z + x.w);
             float val = __fdividef(__uint_as_float(o[c]), lsum);
-            if (it.video) val += __fdividef(cz, 1.0f + __expf(-gv[c]));
+            if (it.video && p.coarse) val += __fdividef(cz, 1.0f + __expf(-gv[c]));
             p.out[out_base + static_cast<size_t>(qc) * row_stride] = __float2bfloat16_rn(val);
           }
         }

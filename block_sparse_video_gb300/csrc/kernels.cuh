@@ -43,7 +43,7 @@ struct PreprocessArgs {
   const float* rope_cos;       // fp32 [N, rope_dim/2]
   const float* rope_sin;
   __nv_bfloat16* out[4];       // packed q, k, v, gate, bf16 [B, N, H, 128]
-  float* pooled[3];            // fp32 [B, H, T, 128]
+  float* pooled[3];            // fp32 [B, H, T, 128]; null: no pooling
   unsigned int* err;           // error words; word 7 records the first bad map entry (token + 1)
 };
 cudaError_t launch_preprocess(const Geometry& g, const PreprocessArgs& a, cudaStream_t stream);
@@ -55,6 +55,16 @@ cudaError_t launch_coarse_topk(const Geometry& g, const float* pooled_q, const f
                                const float* pooled_v, float* coarse, int32_t* tile_index,
                                cudaStream_t stream);
 
+// SubBlock routing: 16-token sub-block means of q and k (fp32 [B, H, 4T, 128],
+// empty sub-blocks of a ragged last tile as 0), then the k video key tiles of
+// highest estimated softmax mass per video query tile (tile_index int32
+// [B, H, T, k], ascending).
+cudaError_t launch_subpool(const Geometry& g, const __nv_bfloat16* q, const __nv_bfloat16* k, float* sub_q,
+                           float* sub_k, cudaStream_t stream);
+size_t subblock_router_smem_bytes(const Geometry& g, int* rows_per_cta);
+cudaError_t launch_subblock_router(const Geometry& g, const float* sub_q, const float* sub_k,
+                                   int32_t* tile_index, cudaStream_t stream);
+
 // Fine attention: prefix query tiles over every key, video query tiles over
 // the prefix plus their selected video tiles; epilogue adds sigmoid(gate) *
 // coarse on video rows and writes bf16 out.
@@ -64,7 +74,7 @@ cudaError_t launch_coarse_topk(const Geometry& g, const float* pooled_q, const f
 struct FineArgs {
   const __nv_bfloat16* gate;
   __nv_bfloat16* out;
-  const float* coarse;
+  const float* coarse;         // null: no gated coarse term (SubBlock routing)
   const int32_t* tile_index;
   unsigned int* err;   // 3 error words in the workspace
   int* redo_count;     // zero before the launch

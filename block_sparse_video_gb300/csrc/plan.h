@@ -9,6 +9,8 @@
 struct vsa_plan {
   vsa_shape_t shape;
   int device;
+  int subblock;         // 0: VSA (coarse branch + top-k); 1: SubBlock routing, no coarse term
+  double sparsity;      // SubBlock plans: fraction of video key tiles that may be dropped
   vsa::Geometry g;
   size_t off_err, off_pq, off_pk, off_pv, off_coarse, off_idx, off_redo, ws_bytes;
   int num_sms;          // SM count of `device`, read on the first forward

@@ -337,7 +337,7 @@ preprocess_kernel(PreprocessArgs a, int H, int P, int Lv, int N, int T, int TP) 
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_bar(s));
   }
-  if (!video || !active) return;
+  if (!video || !active || a.pooled[0] == nullptr) return;
   const int t = tile - TP;
   const float fn = static_cast<float>(rows);
   const size_t po = ((static_cast<size_t>(b) * H + h) * T + t) * kHeadDim + d0;

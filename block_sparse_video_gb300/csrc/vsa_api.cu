@@ -94,15 +94,24 @@ const char* vsa_status_string(vsa_status_t s) {
   return "unknown status";
 }
 
-vsa_status_t vsa_plan_create(const vsa_shape_t* shape, int device, vsa_plan_t* out) {
+}  // extern "C"
+
+namespace {
+
+// Shared by vsa_plan_create (VSA selection) and vsa_plan_create_subblock.
+vsa_status_t create_plan(const vsa_shape_t* shape, int device, bool subblock, double sparsity,
+                         vsa_plan_t* out) {
   if (!shape || !out) return VSA_ERR_INVALID_ARG;
   *out = nullptr;
   const vsa_shape_t s = *shape;
   if (s.batch < 1 || s.num_heads < 1 || s.len_text < 0 || s.len_audio < 0 || s.len_video < 1 ||
       device < 0)
     return VSA_ERR_INVALID_ARG;
-  if (!(std::isfinite(s.keep_fraction) && s.keep_fraction > 0.0 && s.keep_fraction <= 1.0))
+  if (subblock) {
+    if (!(std::isfinite(sparsity) && sparsity >= 0.0 && sparsity < 1.0)) return VSA_ERR_INVALID_ARG;
+  } else if (!(std::isfinite(s.keep_fraction) && s.keep_fraction > 0.0 && s.keep_fraction <= 1.0)) {
     return VSA_ERR_INVALID_ARG;
+  }
   if (s.head_dim != vsa::kHeadDim) return VSA_ERR_UNSUPPORTED;
   const int64_t prefix = s.len_text + s.len_audio;
   const int64_t n = prefix + s.len_video;
@@ -116,36 +125,62 @@ vsa_status_t vsa_plan_create(const vsa_shape_t* shape, int device, vsa_plan_t* o
   g.N = static_cast<int>(n);
   g.T = static_cast<int>((s.len_video + vsa::kTile - 1) / vsa::kTile);
   g.TP = static_cast<int>((prefix + vsa::kTile - 1) / vsa::kTile);
-  // "rounded to a whole number of tiles": round half up, in IEEE double, clamped to [1, T]
-  int64_t k = static_cast<int64_t>(std::floor(s.keep_fraction * static_cast<double>(g.T) + 0.5));
+  int64_t k;
+  if (subblock) {
+    // at most floor(s T) key tiles dropped (IEEE double); the kept count rounded up to
+    // a multiple of 8 tiles and capped at T
+    const int64_t dropped = static_cast<int64_t>(std::floor(sparsity * static_cast<double>(g.T)));
+    const int64_t need = g.T - dropped;
+    k = (need + 7) / 8 * 8;
+  } else {
+    // "rounded to a whole number of tiles": round half up, in IEEE double, clamped to [1, T]
+    k = static_cast<int64_t>(std::floor(s.keep_fraction * static_cast<double>(g.T) + 0.5));
+  }
   if (k < 1) k = 1;
   if (k > g.T) k = g.T;
   g.k = static_cast<int>(k);
   if (static_cast<int64_t>(g.B) * g.H > 65535) return VSA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(g.B) * g.H * (g.TP + g.T) >= (int64_t(1) << 31)) return VSA_ERR_UNSUPPORTED;
   int rows = 0;
-  if (vsa::coarse_smem_bytes(g, &rows) == 0) return VSA_ERR_UNSUPPORTED;  // T too large
+  if (subblock ? vsa::subblock_router_smem_bytes(g, &rows) == 0 : vsa::coarse_smem_bytes(g, &rows) == 0)
+    return VSA_ERR_UNSUPPORTED;  // T too large for the selection kernel's shared memory
 
   vsa_plan* p = new (std::nothrow) vsa_plan;
   if (!p) return VSA_ERR_INTERNAL;
   std::memset(p, 0, sizeof(*p));
   p->shape = s;
   p->device = device;
+  p->subblock = subblock ? 1 : 0;
+  p->sparsity = subblock ? sparsity : 0.0;
   p->g = g;
+  // VSA: pooled q, k, v and the coarse output, fp32 [B, H, T, 128] each.
+  // SubBlock: 16-token sub-block means of q and k, fp32 [B, H, 4T, 128] each.
   const size_t pooled = static_cast<size_t>(g.B) * g.H * g.T * vsa::kHeadDim * sizeof(float);
   const size_t idx = static_cast<size_t>(g.B) * g.H * g.T * g.k * sizeof(int32_t);
   size_t off = 0;
   p->off_err = off;  off += kAlign;
-  p->off_pq = off;   off += align_up(pooled);
-  p->off_pk = off;   off += align_up(pooled);
-  p->off_pv = off;   off += align_up(pooled);
-  p->off_coarse = off; off += align_up(pooled);
+  p->off_pq = off;   off += align_up(subblock ? 4 * pooled : pooled);
+  p->off_pk = off;   off += align_up(subblock ? 4 * pooled : pooled);
+  p->off_pv = off;   off += subblock ? 0 : align_up(pooled);
+  p->off_coarse = off; off += subblock ? 0 : align_up(pooled);
   p->off_idx = off;  off += align_up(idx);
   p->off_redo = off; off += align_up(static_cast<size_t>(g.B) * g.H * (g.TP + g.T) * sizeof(int32_t));
   p->ws_bytes = off;
   p->tensor_bytes = static_cast<size_t>(g.B) * g.N * g.H * vsa::kHeadDim * 2;
   *out = p;
   return VSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+vsa_status_t vsa_plan_create(const vsa_shape_t* shape, int device, vsa_plan_t* out) {
+  return create_plan(shape, device, false, 0.0, out);
+}
+
+vsa_status_t vsa_plan_create_subblock(const vsa_shape_t* shape, double sparsity, int device, vsa_plan_t* out) {
+  return create_plan(shape, device, true, sparsity, out);
 }
 
 vsa_status_t vsa_plan_info(vsa_plan_t plan, int64_t* n_tiles, int64_t* k, size_t* workspace_bytes) {
@@ -180,11 +215,13 @@ namespace {
 vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const void* v, const void* gate,
                           void* out, void* workspace, size_t workspace_bytes, void* stream,
                           bool pool_ready) {
-  if (!plan || !q || !k || !v || !gate || !out || !workspace) return VSA_ERR_INVALID_ARG;
+  if (!plan || !q || !k || !v || !out || !workspace) return VSA_ERR_INVALID_ARG;
+  if (!gate && !plan->subblock) return VSA_ERR_INVALID_ARG;  // SubBlock routing has no gate
   if (workspace_bytes < plan->ws_bytes || !aligned(workspace, kAlign)) return VSA_ERR_INVALID_ARG;
   const void* ins[4] = {q, k, v, gate};
   const size_t tb = plan->tensor_bytes;
   for (const void* x : ins) {
+    if (!x) continue;
     if (!aligned(x, 16)) return VSA_ERR_INVALID_ARG;
     if (overlaps(x, tb, out, tb)) return VSA_ERR_INVALID_ARG;
     if (overlaps(x, tb, workspace, plan->ws_bytes)) return VSA_ERR_INVALID_ARG;
@@ -195,8 +232,9 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
   if (!guard.ok) return VSA_ERR_CUDA;
   const vsa::Geometry& g = plan->g;
   CUtensorMap mq, mk, mv, mg;
+  // without a gate (SubBlock routing) the gate map points at q; the kernel never reads it
   if (!encode_bnhd(&mq, q, g) || !encode_bnhd(&mk, k, g) || !encode_bnhd(&mv, v, g) ||
-      !encode_bnhd(&mg, gate, g))
+      !encode_bnhd(&mg, gate ? gate : q, g))
     return VSA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -215,17 +253,25 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
   if (cudaMemsetAsync(err, 0, pool_ready ? 28 : 32, st) != cudaSuccess) return VSA_ERR_CUDA;
   vsa_status_t rs = record(plan, 0, st);
   if (rs != VSA_OK) return rs;
-  if (!pool_ready &&
-      vsa::launch_pool(g, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-                       static_cast<const __nv_bfloat16*>(v), pq, pk, pv, st) != cudaSuccess)
-    return VSA_ERR_CUDA;
-  if ((rs = record(plan, 1, st)) != VSA_OK) return rs;
-  if (vsa::launch_coarse_topk(g, pq, pk, pv, coarse, idx, st) != cudaSuccess) return VSA_ERR_CUDA;
+  const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(q);
+  const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(k);
+  if (plan->subblock) {
+    // sub-block means are always taken here: the preprocessing pools 64-token tiles
+    if (vsa::launch_subpool(g, qb, kb, pq, pk, st) != cudaSuccess) return VSA_ERR_CUDA;
+    if ((rs = record(plan, 1, st)) != VSA_OK) return rs;
+    if (vsa::launch_subblock_router(g, pq, pk, idx, st) != cudaSuccess) return VSA_ERR_CUDA;
+  } else {
+    if (!pool_ready &&
+        vsa::launch_pool(g, qb, kb, static_cast<const __nv_bfloat16*>(v), pq, pk, pv, st) != cudaSuccess)
+      return VSA_ERR_CUDA;
+    if ((rs = record(plan, 1, st)) != VSA_OK) return rs;
+    if (vsa::launch_coarse_topk(g, pq, pk, pv, coarse, idx, st) != cudaSuccess) return VSA_ERR_CUDA;
+  }
   if ((rs = record(plan, 2, st)) != VSA_OK) return rs;
   vsa::FineArgs a;
   a.gate = static_cast<const __nv_bfloat16*>(gate);
   a.out = static_cast<__nv_bfloat16*>(out);
-  a.coarse = coarse;
+  a.coarse = plan->subblock ? nullptr : coarse;
   a.tile_index = idx;
   a.err = err;
   a.redo_count = reinterpret_cast<int*>(err + 4);
@@ -310,9 +356,10 @@ vsa_status_t vsa_preprocess(vsa_plan_t plan, const vsa_preprocess_args_t* args, 
   a.rope_interleaved = x.rope_interleaved;
   a.rope_cos = x.rope_cos;
   a.rope_sin = x.rope_sin;
-  a.pooled[0] = reinterpret_cast<float*>(ws + plan->off_pq);
-  a.pooled[1] = reinterpret_cast<float*>(ws + plan->off_pk);
-  a.pooled[2] = reinterpret_cast<float*>(ws + plan->off_pv);
+  // a SubBlock plan pools 16-token sub-blocks in its forward: no tile pooling here
+  a.pooled[0] = plan->subblock ? nullptr : reinterpret_cast<float*>(ws + plan->off_pq);
+  a.pooled[1] = plan->subblock ? nullptr : reinterpret_cast<float*>(ws + plan->off_pk);
+  a.pooled[2] = plan->subblock ? nullptr : reinterpret_cast<float*>(ws + plan->off_pv);
   a.err = err;
   return vsa::launch_preprocess(g, a, st) == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
@@ -326,7 +373,8 @@ vsa_status_t vsa_plan_host_path_bytes(vsa_plan_t plan, size_t* bytes) {
 vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, const void* v,
                               const void* gate, void* out, void* device_buffer,
                               size_t device_buffer_bytes, void* stream) {
-  if (!plan || !q || !k || !v || !gate || !out || !device_buffer) return VSA_ERR_INVALID_ARG;
+  if (!plan || !q || !k || !v || !out || !device_buffer) return VSA_ERR_INVALID_ARG;
+  if (!gate && !plan->subblock) return VSA_ERR_INVALID_ARG;
   size_t need = 0;
   vsa_plan_host_path_bytes(plan, &need);
   if (device_buffer_bytes < need || !aligned(device_buffer, kAlign)) return VSA_ERR_INVALID_ARG;
@@ -337,9 +385,9 @@ vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, con
   uint8_t* d = static_cast<uint8_t*>(device_buffer);
   const void* hin[4] = {q, k, v, gate};
   for (int i = 0; i < 4; ++i)
-    if (cudaMemcpyAsync(d + i * slot, hin[i], tb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    if (hin[i] && cudaMemcpyAsync(d + i * slot, hin[i], tb, cudaMemcpyHostToDevice, st) != cudaSuccess)
       return VSA_ERR_CUDA;
-  vsa_status_t s = vsa_forward(plan, d, d + slot, d + 2 * slot, d + 3 * slot, d + 4 * slot,
+  vsa_status_t s = vsa_forward(plan, d, d + slot, d + 2 * slot, gate ? d + 3 * slot : nullptr, d + 4 * slot,
                                d + 5 * slot, plan->ws_bytes, stream);
   if (s != VSA_OK) return s;
   if (cudaMemcpyAsync(out, d + 4 * slot, tb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
@@ -355,9 +403,9 @@ vsa_status_t vsa_debug_views(vsa_plan_t plan, void* workspace, const float** poo
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   if (pooled_q) *pooled_q = reinterpret_cast<const float*>(ws + plan->off_pq);
   if (pooled_k) *pooled_k = reinterpret_cast<const float*>(ws + plan->off_pk);
-  if (pooled_v) *pooled_v = reinterpret_cast<const float*>(ws + plan->off_pv);
+  if (pooled_v) *pooled_v = plan->subblock ? nullptr : reinterpret_cast<const float*>(ws + plan->off_pv);
   if (tile_index) *tile_index = reinterpret_cast<const int32_t*>(ws + plan->off_idx);
-  if (coarse) *coarse = reinterpret_cast<const float*>(ws + plan->off_coarse);
+  if (coarse) *coarse = plan->subblock ? nullptr : reinterpret_cast<const float*>(ws + plan->off_coarse);
   return VSA_OK;
 }
 

@@ -81,6 +81,32 @@ typedef struct vsa_plan* vsa_plan_t; /* opaque, host memory, owned by the librar
  * On success *out receives a plan to release with vsa_plan_destroy. */
 vsa_status_t vsa_plan_create(const vsa_shape_t* shape, int device, vsa_plan_t* out);
 
+/* A plan whose selection is the SubBlock router ("UniServe: serving FastH3 at
+ * its fastest", section "How SubBlock Sparse Attention Works") in place of the
+ * coarse branch. Each 64-token tile splits into four 16-token sub-blocks on
+ * the query and key side. The estimated softmax mass of video key tile j for
+ * video query tile i is
+ *   score(i, j) = log sum_{a,b} n_a n_b exp(q_a . k_b / sqrt(128))
+ * over the non-empty sub-blocks a of tile i and b of tile j, where q_a and k_b
+ * are the sub-block means and n_a, n_b their token counts. Each video query
+ * tile keeps the k video key tiles of highest score (ties to the lower tile,
+ * ascending).
+ *
+ * `sparsity` in [0, 1) is the fraction of key tiles that may be dropped:
+ * k = min(T, 8 * ceil((T - floor(sparsity * T)) / 8)), with the floor in IEEE
+ * double. Text and audio stay dense as in the VSA forward. There is no coarse
+ * branch: vsa_forward on this plan computes out = fine attention, and its gate
+ * argument is ignored and may be NULL. shape->keep_fraction is ignored.
+ *
+ * The forward enqueues four kernels: sub-block pooling of Q and K, the
+ * router, and the fine attention's fast and exact passes. vsa_debug_views
+ * returns the sub-block means (fp32 [batch, num_heads, 4T, 128], empty
+ * sub-blocks of a ragged last tile as 0) as pooled_q and pooled_k, NULL for
+ * pooled_v and coarse, and the selection as tile_index [batch, num_heads, T, k].
+ * vsa_preprocess on this plan packs the tensors but pools nothing. Otherwise
+ * as vsa_plan_create. */
+vsa_status_t vsa_plan_create_subblock(const vsa_shape_t* shape, double sparsity, int device, vsa_plan_t* out);
+
 /* Number of video tiles T, kept tiles per query tile k, and the device
  * workspace vsa_forward needs, in bytes. Any output pointer may be NULL. */
 vsa_status_t vsa_plan_info(vsa_plan_t plan, int64_t* n_tiles, int64_t* k, size_t* workspace_bytes);

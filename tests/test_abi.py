@@ -148,3 +148,37 @@ def test_preprocess_rejects_bad_arguments_without_launching(lib):
         assert f(plan, None, fake, fake, fake, fake, fake, ws, None) == bsv.VSA_ERR_INVALID_ARG
     finally:
         bsv.vsa_plan_destroy(plan)
+
+
+def test_subblock_plan_counts_and_validation(lib):
+    from oracle import subblock_oracle as so
+    for lv, s in [(72576, 0.75), (72576, 0.8), (36288, 0.75), (1000, 0.5), (50, 0.75), (640, 0.0),
+                  (64 * 40, 0.95), (72500, 0.8), (64 * 2600 - 30, 0.8)]:
+        plan = bsv.vsa_plan_create_subblock(1, 2, 10, 20, lv, s)
+        try:
+            t, k, ws = bsv.vsa_plan_info(plan)
+        finally:
+            bsv.vsa_plan_destroy(plan)
+        assert t == vo.video_tile_count(lv)
+        assert k == so.keep_count(t, s), (lv, s)
+        assert ws >= 256 + 2 * 2 * 4 * t * 128 * 4 + 2 * t * k * 4
+    shape = bsv.vsa_shape_t(1, 2, 128, 64, 64, 1024, float("nan"))  # keep_fraction is ignored
+    out = ctypes.c_void_p()
+    for s in (-0.1, 1.0, float("nan"), float("inf")):
+        assert lib.vsa_plan_create_subblock(ctypes.byref(shape), s, 0, ctypes.byref(out)) == bsv.VSA_ERR_INVALID_ARG
+    assert lib.vsa_plan_create_subblock(ctypes.byref(shape), 0.75, 0, ctypes.byref(out)) == bsv.VSA_OK
+    plan = out.value
+    try:
+        _, _, ws = bsv.vsa_plan_info(plan)
+        fake = ctypes.c_void_p(1 << 20)
+        # a VSA plan needs its gate; a SubBlock plan does not (rejected here only for the workspace size)
+        vplan = bsv.vsa_plan_create(1, 2, 64, 64, 1024, 0.2)
+        try:
+            assert lib.vsa_forward(vplan, fake, fake, fake, None, fake, fake, ws, None) == bsv.VSA_ERR_INVALID_ARG
+        finally:
+            bsv.vsa_plan_destroy(vplan)
+        assert lib.vsa_forward(plan, fake, fake, fake, None, fake, fake, ws - 1, None) == bsv.VSA_ERR_INVALID_ARG
+    finally:
+        bsv.vsa_plan_destroy(plan)
+    big = bsv.vsa_shape_t(1, 1, 128, 0, 0, 64 * 20000, 1.0)   # T too large for the router's tiles
+    assert lib.vsa_plan_create_subblock(ctypes.byref(big), 0.5, 0, ctypes.byref(out)) == bsv.VSA_ERR_UNSUPPORTED
