@@ -69,6 +69,15 @@ class vsa_preprocess_args_t(ctypes.Structure):
     ]
 
 
+class vsa_output_rows_t(ctypes.Structure):
+    _fields_ = [
+        ("out", ctypes.c_void_p),
+        ("out_rows", ctypes.c_int64),
+        ("out_row_stride", ctypes.c_int64),
+        ("out_row_map", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -89,6 +98,7 @@ def load_library(path: str = LIB_PATH):
         "vsa_plan_info": (i32, [vp, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(sz)]),
         "vsa_forward": (i32, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "vsa_preprocess": (i32, [vp, ctypes.POINTER(vsa_preprocess_args_t), vp, sz, vp]),
+        "vsa_forward_rows": (i32, [vp, vp, vp, vp, vp, ctypes.POINTER(vsa_output_rows_t), i32, vp, sz, vp]),
         "vsa_forward_preprocessed": (i32, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "vsa_plan_host_path_bytes": (i32, [vp, ctypes.POINTER(sz)]),
         "vsa_forward_host": (i32, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
@@ -203,6 +213,14 @@ def vsa_forward_preprocessed(plan, q, k, v, gate, out, workspace, stream=None):
                                                    _ptr(workspace),
                                                    workspace.numel() * workspace.element_size(),
                                                    _stream_handle(stream)), "vsa_forward_preprocessed")
+
+
+def vsa_forward_rows(plan, q, k, v, gate, rows, preprocessed, workspace, stream=None):
+    """Enqueue the forward writing its rows through ``rows`` (a vsa_output_rows_t)."""
+    _check(load_library().vsa_forward_rows(plan, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), ctypes.byref(rows),
+                                           1 if preprocessed else 0, _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(),
+                                           _stream_handle(stream)), "vsa_forward_rows")
 
 
 def vsa_forward_host(plan, q, k, v, gate, out, device_buffer, stream=None):
@@ -369,6 +387,26 @@ class VSA:
         vsa_forward_preprocessed(self.plan, q, k, v, gate, out, self.workspace, stream)
         return out
 
+    def forward_rows(self, q, k, v, gate, out, out_row_map=None, preprocessed=False, stream=None):
+        """The forward writing attention token n of batch b to row out_row_map[b, n]
+        (or n) of ``out``, a bf16 [B, out_rows, ...] tensor whose rows hold this
+        forward's heads as H x 128 contiguous channels at out.stride(1) elements
+        apart (e.g. a slice of a wider buffer). Rows no token maps to are left as
+        they are. ``preprocessed``: the inputs come from ``preprocess``."""
+        for name, x in (("q", q), ("k", k), ("v", v)) + ((("gate", gate),) if gate is not None else ()):
+            _check_tensor(x, name, self.shape, self.device)
+        if (out.dtype != torch.bfloat16 or out.dim() < 2 or out.shape[0] != self.batch or out.device != self.device
+                or out[0, 0].numel() < self.num_heads * 128 or not out[0, 0].is_contiguous()):
+            raise ValueError("out: expected bf16 [B, out_rows, ...] with contiguous rows of H x 128 channels")
+        if self.batch > 1 and out.stride(0) != out.shape[1] * out.stride(1):
+            raise ValueError("out: batches must be out_rows * row stride elements apart")
+        if out_row_map is not None and (out_row_map.dtype != torch.int32 or not out_row_map.is_contiguous()
+                                        or tuple(out_row_map.shape) != (self.batch, self.seq)):
+            raise ValueError(f"out_row_map: expected contiguous int32 [{self.batch}, {self.seq}]")
+        rows = vsa_output_rows_t(_ptr(out), out.shape[1], out.stride(1), _ptr(out_row_map))
+        vsa_forward_rows(self.plan, q, k, v, gate, rows, preprocessed, self.workspace, stream)
+        return out
+
     def check(self, stream=None):
         vsa_check(self.plan, self.workspace, stream)
 
@@ -427,7 +465,8 @@ class SubBlock(VSA):
 
 __all__ = [
     "VSA", "SubBlock", "VsaError", "vsa_plan_create_subblock", "load_library", "header_functions", "vsa_plan_create", "vsa_plan_info",
-    "vsa_forward", "vsa_forward_host", "vsa_preprocess", "vsa_forward_preprocessed",
+    "vsa_forward", "vsa_forward_host", "vsa_preprocess", "vsa_forward_preprocessed", "vsa_forward_rows",
+    "vsa_output_rows_t",
     "vsa_preprocess_args_t", "vsa_plan_host_path_bytes", "vsa_debug_views", "vsa_check",
     "vsa_plan_set_stage_events", "vsa_plan_destroy", "vsa_status_string",
     "vsa_forward_static_workspace", "vsa_diag_wait_timeout",

@@ -116,6 +116,9 @@ struct FineParams {
   const __nv_bfloat16* gate;
   __nv_bfloat16* out;
   const float* coarse;  // null: no gated coarse term on video rows (SubBlock routing)
+  const int32_t* out_row_map;  // null: token n of batch b -> out row b * N + n; else row b * out_rows + map[b * N + n]
+  long long out_rows;          // output rows per batch
+  long long out_row_stride;    // elements between output rows
   const int32_t* tile_index;
   unsigned int* err;
   int* work_counter;    // next work index to hand out (zeroed before the launch)
@@ -632,10 +635,11 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       // The epilogue's gate and coarse inputs were prefetched into L2 when the
       // item was fetched; all of them are requested together (loading them
       // inside the store loop serialised one round trip per column).
-      const size_t out_base = (static_cast<size_t>(it.b) * p.N + it.q_row0) * row_stride +
-                              static_cast<size_t>(it.h) * kHeadDim + r;
+      const size_t gate_base = (static_cast<size_t>(it.b) * p.N + it.q_row0) * row_stride +
+                               static_cast<size_t>(it.h) * kHeadDim + r;
       float gv[kCols];
       float cz = 0.f;
+      long long my_row = 0;  // output row of query column col0 + (lane % kCols)
       auto prefetch_gate = [&]() {
 #pragma unroll
         for (int c = 0; c < kCols; ++c) gv[c] = 0.f;
@@ -644,8 +648,12 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
 #pragma unroll
           for (int c = 0; c < kCols; ++c)
             if (col0 + c < it.q_valid)
-              gv[c] = __bfloat162float(__ldg(p.gate + out_base + static_cast<size_t>(col0 + c) * row_stride));
+              gv[c] = __bfloat162float(__ldg(p.gate + gate_base + static_cast<size_t>(col0 + c) * row_stride));
         }
+        const int qc = col0 + (lane % kCols);
+        my_row = it.q_row0 + qc;
+        if (p.out_row_map && qc < it.q_valid)
+          my_row = __ldg(p.out_row_map + static_cast<size_t>(it.b) * p.N + it.q_row0 + qc);
       };
       if (kExact) {
         // every block, even after a failure, so that all warps meet the same
@@ -711,12 +719,18 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
 #pragma unroll
         for (int c = 0; c < kCols; ++c) {
           const int qc = col0 + c;
+          const long long row = __shfl_sync(0xffffffffu, my_row, c);
           if (qc < it.q_valid) {
             const float4 x = reinterpret_cast<const float4*>(red)[wg * kCols + c];
             const float lsum = (x.x + x.y) + (x.z + x.w);
             float val = __fdividef(__uint_as_float(o[c]), lsum);
             if (it.video && p.coarse) val += __fdividef(cz, 1.0f + __expf(-gv[c]));
-            p.out[out_base + static_cast<size_t>(qc) * row_stride] = __float2bfloat16_rn(val);
+            if (row >= 0 && row < p.out_rows) {
+              p.out[(static_cast<size_t>(it.b) * p.out_rows + row) * p.out_row_stride +
+                    static_cast<size_t>(it.h) * kHeadDim + r] = __float2bfloat16_rn(val);
+            } else if (r == 0) {  // a map entry outside the output: skipped and reported (token + 1)
+              atomicCAS(err + 3, 0u, static_cast<unsigned int>(it.q_row0 + qc) + 1u);
+            }
           }
         }
       }
@@ -744,6 +758,9 @@ cudaError_t launch_fine(const Geometry& g, const CUtensorMap& map_q, const CUten
   p.scale_log2 = 1.4426950408889634f * 0.08838834764831845f;
   p.gate = a.gate;
   p.out = a.out;
+  p.out_row_map = a.out_row_map;
+  p.out_rows = a.out_row_map ? a.out_rows : g.N;
+  p.out_row_stride = a.out_row_stride > 0 ? a.out_row_stride : static_cast<long long>(g.H) * kHeadDim;
   p.coarse = a.coarse;
   p.tile_index = a.tile_index;
   p.err = a.err;

@@ -73,10 +73,13 @@ cudaError_t launch_subblock_router(const Geometry& g, const float* sub_q, const 
 // appended to the redo list.
 struct FineArgs {
   const __nv_bfloat16* gate;
-  __nv_bfloat16* out;
+  __nv_bfloat16* out;          // row r of batch b at out + (b * out_rows + r) * out_row_stride
+  const int32_t* out_row_map;  // null: token n -> row n (out_rows = N); else row map[b * N + n]
+  long long out_rows = 0;
+  long long out_row_stride = 0;  // 0: num_heads * 128
   const float* coarse;         // null: no gated coarse term (SubBlock routing)
   const int32_t* tile_index;
-  unsigned int* err;   // 3 error words in the workspace
+  unsigned int* err;   // error words in the workspace; word 3 records the first bad output map entry
   int* redo_count;     // zero before the launch
   int* redo_list;      // int32 [B * H * (TP + T)]
   int* work_counters;  // 2 counters, zero before the launch

@@ -212,21 +212,34 @@ namespace {
 // The forward behind vsa_forward (pool_ready = false: clears every counter and
 // error word, then pools Q/K/V) and vsa_forward_preprocessed (pool_ready = true:
 // the pooled statistics and word 7 come from vsa_preprocess and are kept).
+// Output layout: null `rows` means the packed [B, N, H, 128] tensor `out`.
 vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const void* v, const void* gate,
                           void* out, void* workspace, size_t workspace_bytes, void* stream,
-                          bool pool_ready) {
+                          bool pool_ready, const vsa_output_rows_t* rows = nullptr) {
   if (!plan || !q || !k || !v || !out || !workspace) return VSA_ERR_INVALID_ARG;
   if (!gate && !plan->subblock) return VSA_ERR_INVALID_ARG;  // SubBlock routing has no gate
   if (workspace_bytes < plan->ws_bytes || !aligned(workspace, kAlign)) return VSA_ERR_INVALID_ARG;
   const void* ins[4] = {q, k, v, gate};
   const size_t tb = plan->tensor_bytes;
+  // bytes the output spans: the packed tensor, or B * out_rows rows of out_row_stride elements
+  size_t out_span = tb;
+  if (rows) {
+    if (rows->out_rows < 1 || rows->out_row_stride < static_cast<int64_t>(plan->g.H) * vsa::kHeadDim ||
+        rows->out_row_stride % 8 != 0)
+      return VSA_ERR_INVALID_ARG;
+    if (!rows->out_row_map && rows->out_rows < plan->g.N) return VSA_ERR_INVALID_ARG;
+    if (rows->out_row_map && !aligned(rows->out_row_map, 4)) return VSA_ERR_INVALID_ARG;
+    if (rows->out_row_stride > (int64_t(1) << 24) || rows->out_rows > kMaxTokens * 4) return VSA_ERR_UNSUPPORTED;
+    out_span = (static_cast<size_t>(plan->g.B) * rows->out_rows - 1) * static_cast<size_t>(rows->out_row_stride) * 2 +
+               static_cast<size_t>(plan->g.H) * vsa::kHeadDim * 2;
+  }
   for (const void* x : ins) {
     if (!x) continue;
     if (!aligned(x, 16)) return VSA_ERR_INVALID_ARG;
-    if (overlaps(x, tb, out, tb)) return VSA_ERR_INVALID_ARG;
+    if (overlaps(x, tb, out, out_span)) return VSA_ERR_INVALID_ARG;
     if (overlaps(x, tb, workspace, plan->ws_bytes)) return VSA_ERR_INVALID_ARG;
   }
-  if (!aligned(out, 16) || overlaps(out, tb, workspace, plan->ws_bytes)) return VSA_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || overlaps(out, out_span, workspace, plan->ws_bytes)) return VSA_ERR_INVALID_ARG;
 
   DeviceGuard guard(plan->device);
   if (!guard.ok) return VSA_ERR_CUDA;
@@ -272,6 +285,13 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
   a.gate = static_cast<const __nv_bfloat16*>(gate);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.coarse = plan->subblock ? nullptr : coarse;
+  if (rows) {
+    a.out_row_map = rows->out_row_map;
+    a.out_rows = rows->out_rows;
+    a.out_row_stride = rows->out_row_stride;
+  } else {
+    a.out_row_map = nullptr;
+  }
   a.tile_index = idx;
   a.err = err;
   a.redo_count = reinterpret_cast<int*>(err + 4);
@@ -302,6 +322,13 @@ vsa_status_t vsa_forward_preprocessed(vsa_plan_t plan, const void* q, const void
                                       const void* gate, void* out, void* workspace,
                                       size_t workspace_bytes, void* stream) {
   return forward_impl(plan, q, k, v, gate, out, workspace, workspace_bytes, stream, true);
+}
+
+vsa_status_t vsa_forward_rows(vsa_plan_t plan, const void* q, const void* k, const void* v, const void* gate,
+                              const vsa_output_rows_t* out, int32_t preprocessed, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (!out || !out->out) return VSA_ERR_INVALID_ARG;
+  return forward_impl(plan, q, k, v, gate, out->out, workspace, workspace_bytes, stream, preprocessed != 0, out);
 }
 
 vsa_status_t vsa_preprocess(vsa_plan_t plan, const vsa_preprocess_args_t* args, void* workspace,
@@ -422,6 +449,7 @@ vsa_status_t vsa_check(vsa_plan_t plan, void* workspace, void* stream) {
   if (words[0] == static_cast<unsigned int>(VSA_ERR_DEVICE_TIMEOUT)) return VSA_ERR_DEVICE_TIMEOUT;
   if (words[0] != 0) return VSA_ERR_INTERNAL;
   if (words[7] != 0) return VSA_ERR_INVALID_ARG;  // a preprocessing map entry outside its buffer
+  if (words[3] != 0) return VSA_ERR_INVALID_ARG;  // an output map entry outside the output rows
   return VSA_OK;
 }
 

@@ -197,6 +197,34 @@ vsa_status_t vsa_forward_preprocessed(vsa_plan_t plan, const void* q, const void
                                       const void* gate, void* out, void* workspace,
                                       size_t workspace_bytes, void* stream);
 
+/* Where the forward writes its output rows. The combined rows can go straight
+ * into another layout, such as the send buffer of the output all-to-all that
+ * restores sequence sharding ("UniServe: serving FastH3 at its fastest",
+ * section "Fused output combination": the combination kernel writes each row
+ * directly into its position in the send buffer). Attention token n of batch
+ * b (segments text | audio | video) is written to row
+ *   out_row_map[b * N + n]        (or n when out_row_map is NULL)
+ * of batch b. Channel c of head h of output row r of batch b is at
+ *   out + (b * out_rows + r) * out_row_stride + h * 128 + c   (elements, bf16).
+ * When sequence shards are contiguous row ranges, the rank-major send buffer
+ * is the sequence order itself. out_row_map is then the map that packed the
+ * rows (vsa_preprocess_args_t.src_row), and out_row_stride is num_heads * 128.
+ * Rows no token maps to are left untouched. A map entry outside
+ * [0, out_rows) skips that row, and vsa_check reports VSA_ERR_INVALID_ARG. */
+typedef struct {
+  void* out;                   /* device bf16, 16-byte aligned; must not overlap the inputs or the workspace */
+  int64_t out_rows;            /* rows per batch, >= 1 (>= N without a map) */
+  int64_t out_row_stride;      /* elements between rows: >= num_heads * 128, multiple of 8 */
+  const int32_t* out_row_map;  /* device int32 [batch, N], or NULL */
+} vsa_output_rows_t;
+
+/* vsa_forward (preprocessed = 0) or vsa_forward_preprocessed (preprocessed != 0)
+ * writing its rows through `out` as described above. Same errors, same
+ * kernels, capture-safe. */
+vsa_status_t vsa_forward_rows(vsa_plan_t plan, const void* q, const void* k, const void* v, const void* gate,
+                              const vsa_output_rows_t* out, int32_t preprocessed, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
 /* Same forward on HOST buffers (q, k, v, gate read, out written, all bf16
  * [batch, N, num_heads, 128]; pinned memory makes the copies asynchronous).
  * `device_buffer` (>= host_path_bytes from vsa_plan_host_path_bytes, 256-byte
@@ -218,7 +246,8 @@ vsa_status_t vsa_debug_views(vsa_plan_t plan, void* workspace, const float** poo
 
 /* Synchronise `stream` and report the device error words of `workspace`:
  * VSA_OK; VSA_ERR_DEVICE_TIMEOUT if a bounded wait gave up; VSA_ERR_INVALID_ARG
- * if the last vsa_preprocess met a map entry outside its projection buffer. */
+ * if the last vsa_preprocess met a map entry outside its projection buffer or
+ * the last vsa_forward_rows an output map entry outside its rows. */
 vsa_status_t vsa_check(vsa_plan_t plan, void* workspace, void* stream);
 
 /* Optional per-kernel timing. When `events` is non-NULL, each vsa_forward

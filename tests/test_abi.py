@@ -182,3 +182,31 @@ def test_subblock_plan_counts_and_validation(lib):
         bsv.vsa_plan_destroy(plan)
     big = bsv.vsa_shape_t(1, 1, 128, 0, 0, 64 * 20000, 1.0)   # T too large for the router's tiles
     assert lib.vsa_plan_create_subblock(ctypes.byref(big), 0.5, 0, ctypes.byref(out)) == bsv.VSA_ERR_UNSUPPORTED
+
+
+def test_forward_rows_rejects_bad_layouts_without_launching(lib):
+    plan = bsv.vsa_plan_create(1, 2, 64, 64, 1024, 0.2)  # N = 1152, rows of 256 elements
+    try:
+        _, _, ws = bsv.vsa_plan_info(plan)
+        g = 1 << 32
+        ins = [ctypes.c_void_p(g * (i + 1)) for i in range(4)]
+        wsp = ctypes.c_void_p(10 * g)
+
+        def st(**kw):
+            a = dict(out=6 * g, out_rows=2000, out_row_stride=256, out_row_map=None)
+            a.update(kw)
+            rows = bsv.vsa_output_rows_t(**a)
+            return lib.vsa_forward_rows(plan, *ins, ctypes.byref(rows), 0, wsp, ws, None)
+
+        for kw in (dict(out_rows=1000),                    # no map: fewer rows than tokens
+                   dict(out_rows=0, out_row_map=11 * g),
+                   dict(out_row_stride=255), dict(out_row_stride=252),
+                   dict(out_row_map=11 * g + 2),           # misaligned map
+                   dict(out=g + 4096),                     # inside an input
+                   dict(out=10 * g - 1024),                # running into the workspace
+                   dict(out=6 * g + 8)):                   # misaligned output
+            assert st(**kw) == bsv.VSA_ERR_INVALID_ARG, kw
+        assert st(out_row_stride=1 << 25) == bsv.VSA_ERR_UNSUPPORTED
+        assert lib.vsa_forward_rows(plan, *ins, None, 0, wsp, ws, None) == bsv.VSA_ERR_INVALID_ARG
+    finally:
+        bsv.vsa_plan_destroy(plan)
