@@ -56,14 +56,16 @@ cudaError_t launch_coarse_topk(const Geometry& g, const float* pooled_q, const f
                                cudaStream_t stream);
 
 // SubBlock routing: 16-token sub-block means of q and k (fp32 [B, H, 4T, 128],
-// empty sub-blocks of a ragged last tile as 0), then the k video key tiles of
-// highest estimated softmax mass per video query tile (tile_index int32
-// [B, H, T, k], ascending).
+// empty sub-blocks of a ragged last tile as 0, plus the same values split into
+// bf16 hi + lo in mma fragment order, subblock_rows_padded(g) x 512 bytes per
+// (b, h)), then the k video key tiles of highest estimated softmax mass per
+// video query tile (tile_index int32 [B, H, T, k], ascending).
+int subblock_rows_padded(const Geometry& g);
 cudaError_t launch_subpool(const Geometry& g, const __nv_bfloat16* q, const __nv_bfloat16* k, float* sub_q,
-                           float* sub_k, cudaStream_t stream);
+                           float* sub_k, void* frag_q, void* frag_k, cudaStream_t stream);
 size_t subblock_router_smem_bytes(const Geometry& g, int* rows_per_cta);
-cudaError_t launch_subblock_router(const Geometry& g, const float* sub_q, const float* sub_k,
-                                   int32_t* tile_index, cudaStream_t stream);
+cudaError_t launch_subblock_router(const Geometry& g, const void* frag_q, const void* frag_k,
+                                   int32_t* tile_index, unsigned int* err, cudaStream_t stream);
 
 // Fine attention: prefix query tiles over every key, video query tiles over
 // the prefix plus their selected video tiles; epilogue adds sigmoid(gate) *

@@ -1,11 +1,11 @@
 // Tile mean-pool (HBM-bound). For every video tile j of every batch, the mean
 // of Q, K and V over the tile's valid tokens, in fp32 ("UniServe: serving
 // FastH3 at its fastest", section "Fused attention preprocessing": tile
-// pooling over valid tokens into FP32 pooled statistics). The same kernel
-// with 16-token runs gives the SubBlock router's sub-block means of Q and K
-// (section "How SubBlock Sparse Attention Works": four 16-token sub-blocks
-// per 64-token block); a run past the end of a ragged last block is empty and
-// its mean is written as 0.
+// pooling over valid tokens into FP32 pooled statistics). A second kernel
+// takes 16-token runs of Q and K for the SubBlock router (section "How
+// SubBlock Sparse Attention Works": four 16-token sub-blocks per 64-token
+// block); a run past the end of a ragged last block is empty and its mean is
+// written as 0.
 //
 // A token row holds all heads: H x 128 bf16 = H x 16 sixteen-byte vectors. A
 // CTA of 128 threads owns 128 consecutive vectors of the row (8 channels per
@@ -74,6 +74,103 @@ pool_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict
                        __fdiv_rn(acc[7], fn));
 }
 
+// bf16 hi/lo split of x (x ~ hi + lo with hi = bf16(x), lo = bf16(x - hi)),
+// packed as bf16x2 words of two consecutive channels
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// 16-token sub-block means of q and k for the SubBlock router: fp32 rows
+// [B, H, 4T, 128] (runs < 4T), and the same values split into bf16 hi + lo in
+// mma.sync m16n8k16 fragment order:
+//   frag[bh][tile8][ks][lane] = uint4 {hi a, hi b, lo a, lo b}
+// for 8 fragment rows (tile8), 16 channels (ks) and lane = 4 g + t4. The
+// words are: a = channels 16 ks + 2 t4 and + 1 of fragment row g; b = the same
+// channels + 8. A tile8 is the B operand of 8 key sub-rows, and two tile8s
+// are the A operand of 16 query sub-rows.
+//
+// Sub-rows are permuted inside each group of 16 (4 blocks, 4 sub-blocks each)
+// so that one lane's m16n8 products cover whole pairs of blocks.
+//   * Query sub-block a of block j sits in tile8 a & 1, row j + 4 (a >> 1).
+//     Rows g and g + 8 of the m16 tile are then sub-blocks 2 (g >> 2) and
+//     2 (g >> 2) + 1 of block g & 3.
+//   * Key sub-block s of block j sits in tile8 s >> 1, row 2 j + (s & 1).
+//     Columns 2 t4 and 2 t4 + 1 of the two n8 tiles are then all four
+//     sub-blocks of block t4.
+// Rows are padded to spad per (b, h). Runs past the video (n <= 0) are zeros
+// in both forms.
+__global__ void __launch_bounds__(kPoolThreads)
+subpool_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+               float* __restrict__ pq, float* __restrict__ pk, uint4* __restrict__ fq, uint4* __restrict__ fk,
+               int H, int P, int Lv, int N, int T, int spad) {
+  constexpr int kLen = kTile / 4;
+  const int vec = blockIdx.y * kPoolThreads + threadIdx.x;  // 16-byte vector within a row
+  const int row_vecs = H * (kHeadDim / 8);
+  const int b = blockIdx.x / spad, run = blockIdx.x % spad;
+  const __nv_bfloat16* src = blockIdx.z == 0 ? q : k;
+  float* dst = blockIdx.z == 0 ? pq : pk;
+  uint4* frag = blockIdx.z == 0 ? fq : fk;
+  const bool active = vec < row_vecs;  // whole lane pairs (row_vecs is even)
+  const int n = min(kLen, Lv - run * kLen);
+  const int h = vec / (kHeadDim / 8);
+  const int d0 = (vec % (kHeadDim / 8)) * 8;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  if (active && n > 0) {
+    const size_t row_stride = static_cast<size_t>(row_vecs);  // in uint4 units
+    const uint4* base = reinterpret_cast<const uint4*>(src) +
+                        (static_cast<size_t>(b) * N + P + static_cast<size_t>(run) * kLen) * row_stride + vec;
+    int r = 0;
+    for (; r + kUnroll <= n; r += kUnroll) {
+      uint4 w[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) w[u] = __ldg(base + static_cast<size_t>(r + u) * row_stride);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) accumulate(acc, w[u]);
+    }
+    for (; r < n; ++r) accumulate(acc, __ldg(base + static_cast<size_t>(r) * row_stride));
+    const float fn = static_cast<float>(n);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = __fdiv_rn(acc[i], fn);
+  }
+  if (active && run < 4 * T) {
+    float4* out = reinterpret_cast<float4*>(dst + ((static_cast<size_t>(b) * H + h) * 4 * T + run) * kHeadDim + d0);
+    out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+  // this thread's channels d0 .. d0 + 7 are word `half` (a or b) of lanes 4 g + 0..3;
+  // the neighbour thread (d0 + 8 or d0 - 8) holds the other word of the same lanes
+  uint32_t hi[4], lo[4];
+#pragma unroll
+  for (int t4 = 0; t4 < 4; ++t4) split_pair(acc[2 * t4], acc[2 * t4 + 1], hi[t4], lo[t4]);
+  const int half = (d0 / 8) & 1;
+  uint32_t ohi[4], olo[4];
+#pragma unroll
+  for (int t4 = 0; t4 < 4; ++t4) {
+    ohi[t4] = __shfl_xor_sync(0xffffffffu, hi[t4], 1);
+    olo[t4] = __shfl_xor_sync(0xffffffffu, lo[t4], 1);
+  }
+  if (!active) return;
+  const int grp = run / 16, blk = (run % 16) / 4, sb = run % 4;
+  const int tile8 = 2 * grp + (blockIdx.z == 0 ? (sb & 1) : (sb >> 1));
+  const int g = blockIdx.z == 0 ? blk + 4 * (sb >> 1) : 2 * blk + (sb & 1);
+  const int ks = d0 / 16;
+  uint4* f = frag + ((static_cast<size_t>(b) * H + h) * (spad / 8) + tile8) * 8 * 32 + ks * 32 + 4 * g;
+  // the a-word thread writes lanes 4 g + 0, 1 and the b-word thread lanes 4 g + 2, 3
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int t4 = 2 * half + j;
+    const uint32_t ha = half ? ohi[t4] : hi[t4], hb = half ? hi[t4] : ohi[t4];
+    const uint32_t la = half ? olo[t4] : lo[t4], lb = half ? lo[t4] : olo[t4];
+    f[t4] = make_uint4(ha, hb, la, lb);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_pool(const Geometry& g, const __nv_bfloat16* q, const __nv_bfloat16* k,
@@ -86,13 +183,15 @@ cudaError_t launch_pool(const Geometry& g, const __nv_bfloat16* q, const __nv_bf
   return cudaGetLastError();
 }
 
+int subblock_rows_padded(const Geometry& g) { return (4 * g.T + 127) / 128 * 128; }
+
 cudaError_t launch_subpool(const Geometry& g, const __nv_bfloat16* q, const __nv_bfloat16* k, float* sub_q,
-                           float* sub_k, cudaStream_t stream) {
+                           float* sub_k, void* frag_q, void* frag_k, cudaStream_t stream) {
   const int row_vecs = g.H * (kHeadDim / 8);
-  const int runs = 4 * g.T;  // four 16-token sub-blocks per video tile
-  dim3 grid(g.B * runs, (row_vecs + kPoolThreads - 1) / kPoolThreads, 2);
-  pool_kernel<kTile / 4><<<grid, kPoolThreads, 0, stream>>>(q, k, nullptr, sub_q, sub_k, nullptr, g.B, g.H,
-                                                            g.P, g.Lv, g.N, runs);
+  const int spad = subblock_rows_padded(g);
+  dim3 grid(g.B * spad, (row_vecs + kPoolThreads - 1) / kPoolThreads, 2);
+  subpool_kernel<<<grid, kPoolThreads, 0, stream>>>(q, k, sub_q, sub_k, static_cast<uint4*>(frag_q),
+                                                    static_cast<uint4*>(frag_k), g.H, g.P, g.Lv, g.N, g.T, spad);
   return cudaGetLastError();
 }
 

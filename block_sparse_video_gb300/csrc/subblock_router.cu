@@ -17,18 +17,31 @@
 //     stored ascending.
 //
 // A CTA owns R query blocks (4R query sub-rows) of one (batch, head) and keeps
-// their R x T block scores in shared memory. Key sub-rows stream through a
-// padded 64-row chunk (16 key blocks). The sub-block logits come from split
-// TF32 tensor-core products (fp32-level error, as in the coarse kernel).
-// Every m16n8 product tile is reduced at once in registers:
-//   * its 16 x 8 sub-block logits are 4 query blocks x 2 key blocks of 4 x 4
-//     pairs;
-//   * the 16 values of one pair of blocks sit in 8 lanes (lane bits 0, 2 and
-//     3 vary), so each log-sum-exp takes three shuffle rounds.
-// The warp-per-row radix select of the coarse kernel then picks each row's top k.
+// their R x T block scores in shared memory.
+//
+// Operands. The sub-pool kernel leaves every sub-block mean split into bf16
+// hi + lo (x ~ hi + lo, ~2^-16 relative), already in mma.sync m16n8k16
+// fragment order. So the products are bf16 tensor-core MMAs,
+//   q . k ~ hi.hi + hi.lo + lo.hi,
+// with fp32 accumulation. That is about 2^-16 relative error on each logit,
+// against the 1e-3 tie band of the selection. No operand is converted in the
+// inner loop. The CTA's query fragments (R/2 x 4 KB) come in one bulk copy,
+// and each warp keeps its own m16 tile's fragments in registers.
+// Key fragments stream through a two-slot ring of CH-sub-row chunks, filled by
+// bulk copies that complete on mbarriers.
+//
+// The sub-pool kernel permutes sub-rows inside each group of 4 blocks (see
+// pool.cu). A warp's tile is one m16 tile (4 query blocks) by two n8 tiles
+// (4 key blocks), and each lane then holds 8 of the 16 logits of one (query
+// block, key block) pair; lane ^ 16 holds the other 8. The log-sum-exp is
+// lane-local plus one shuffle for the maximum and one for the sum. It runs in
+// log2 units (ex2 and lg2 on the MUFU pipe), which ranks in the same order.
+// The warp-per-row radix select of the coarse kernel then picks each row's
+// top k.
 #include <cmath>
 
 #include "kernels.cuh"
+#include "ptx.cuh"
 #include "tf32_select.cuh"
 
 namespace vsa {
@@ -36,128 +49,172 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 64;            // key sub-rows staged per step (16 key blocks)
-constexpr int kQPad = kHeadDim + 4;   // padded rows: conflict-free fragment loads
+constexpr int kTile8Bytes = 8 * 32 * 16;          // fragments of 8 sub-rows x 128 channels: 4 KB
 constexpr size_t kSmemBudget = 220 * 1024;
-constexpr int kSub = 16;              // tokens per sub-block
+constexpr int kSub = 16;                          // tokens per sub-block
+constexpr unsigned int kDetailRouterQ = 0x700, kDetailRouterK = 0x710;
 
-__device__ __forceinline__ void load_rows(float* dst, const float* src, int first, int count, int rows) {
-  for (int e = threadIdx.x; e < rows * (kHeadDim / 4); e += kThreads) {
-    const int r = e / (kHeadDim / 4), c4 = e % (kHeadDim / 4);
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (first + r < count)
-      x = __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(first + r) * kHeadDim) + c4);
-    *reinterpret_cast<float4*>(dst + r * kQPad + 4 * c4) = x;
-  }
-}
-
-constexpr int kChunkF4PerThread = kChunk * (kHeadDim / 4) / kThreads;
-
-__device__ __forceinline__ void fetch_chunk(float4 (&pre)[kChunkF4PerThread], const float* src, int first,
-                                            int count) {
-#pragma unroll
-  for (int i = 0; i < kChunkF4PerThread; ++i) {
-    const int e = threadIdx.x + i * kThreads;
-    const int r = e / (kHeadDim / 4), c4 = e % (kHeadDim / 4);
-    pre[i] = first + r < count
-                 ? __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(first + r) * kHeadDim) + c4)
-                 : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-}
-
-__device__ __forceinline__ void stash_chunk(float* dst, const float4 (&pre)[kChunkF4PerThread]) {
-#pragma unroll
-  for (int i = 0; i < kChunkF4PerThread; ++i) {
-    const int e = threadIdx.x + i * kThreads;
-    const int r = e / (kHeadDim / 4), c4 = e % (kHeadDim / 4);
-    *reinterpret_cast<float4*>(dst + r * kQPad + 4 * c4) = pre[i];
-  }
-}
-
-// ln(number of valid tokens of sub-block s), -inf for an empty one
-__device__ __forceinline__ float ln_count(int s, int Lv) {
+// log2(number of valid tokens of sub-block s), -inf for an empty one
+__device__ __forceinline__ float lg_count(int s, int Lv) {
   const int n = min(kSub, Lv - kSub * s);
-  return n >= kSub ? 2.772588722239781f : (n > 0 ? logf(static_cast<float>(n)) : -INFINITY);
+  return n >= kSub ? 4.f : (n > 0 ? __log2f(static_cast<float>(n)) : -INFINITY);
 }
 
-template <int R>
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
+  return r;
+}
+
+// R query blocks per CTA (R/4 m16 tiles), CH key sub-rows per chunk (CH/16
+// n-pairs). Warp w takes m16 tile w / (CH/16) and n-pair w % (CH/16) of each
+// chunk; warps past R/4 m16 tiles idle.
+template <int R, int CH>
 __global__ void __launch_bounds__(kThreads, 1)
-subblock_router_kernel(const float* __restrict__ sub_q, const float* __restrict__ sub_k,
-                       int32_t* __restrict__ tile_index, int T, int Lv, int k, int spad) {
-  constexpr int MT = R / 4;                 // m16 tiles of query sub-rows
-  const int bstride = spad / 4 + 4;         // block-score row stride (floats)
-  extern __shared__ __align__(16) float smem[];
-  float* S = smem;                          // [R][bstride] block scores
-  float* sq = S + R * bstride;              // [16 MT][kQPad] query sub-block means
-  float* sx = sq + 16 * MT * kQPad;         // [kChunk][kQPad] key sub-block means
-  int* hist = reinterpret_cast<int*>(sx + kChunk * kQPad);  // [kWarps][kBins]
+subblock_router_kernel(const uint4* __restrict__ frag_q, const uint4* __restrict__ frag_k,
+                       int32_t* __restrict__ tile_index, unsigned int* err, int T, int Lv, int k, int spad) {
+  constexpr int MT = R / 4;
+  constexpr int NP = CH / 16;
+  constexpr int kChunkBytes = CH / 8 * kTile8Bytes;
+  const int bstride = spad / 4 + 4;                 // block-score row stride (floats)
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* s_kbuf = smem;                           // [2][kChunkBytes] key fragments
+  uint8_t* s_q = smem + 2 * kChunkBytes;            // [R/2 tile8][kTile8Bytes] query fragments
+  float* S = reinterpret_cast<float*>(s_q + (R / 2) * kTile8Bytes);  // [R][bstride] block scores
+  uint64_t* bars = reinterpret_cast<uint64_t*>(S + R * bstride);     // q, k slot 0, k slot 1
+  int* hist = reinterpret_cast<int*>(smem);         // [kWarps][kBins], over the key ring after the products
 
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const int g = lane >> 2, t4 = lane & 3;
-  const int q0 = blockIdx.x * R;            // first query block of this CTA
+  const int q0 = blockIdx.x * R;                    // first query block of this CTA
   const size_t bh = blockIdx.y;
-  const int n_sub = 4 * T;
-  const float* gq = sub_q + bh * n_sub * kHeadDim;
-  const float* gk = sub_k + bh * n_sub * kHeadDim;
-  const float scale = 0.08838834764831845f;  // 1/sqrt(128)
+  const size_t tiles_per_bh = static_cast<size_t>(spad) / 8;
+  const uint8_t* gq = reinterpret_cast<const uint8_t*>(frag_q + bh * tiles_per_bh * 256);
+  const uint8_t* gk = reinterpret_cast<const uint8_t*>(frag_k + bh * tiles_per_bh * 256);
+  const float scale_log2 = 0.08838834764831845f * 1.4426950408889634f;  // log2(e) / sqrt(128)
+  const int n_chunks = spad / CH;
+  const uint32_t bar_q = smem_u32(bars), bar_k0 = smem_u32(bars + 1);
 
-  load_rows(sq, gq, 4 * q0, n_sub, 16 * MT);
-
-  // warp w: key columns 8 (w % 8) .. + 7 of each chunk, m16 tiles w / 8, w / 8 + 2, ...
-  const int nt = warp % 8, mg = warp / 8;
-  // ln n of this lane's query sub-rows (16 m + g and 16 m + g + 8 of the CTA's 4R)
-  float lnq[MT][2];
-#pragma unroll
-  for (int m = 0; m < MT; ++m)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) lnq[m][h] = ln_count(4 * q0 + 16 * m + g + 8 * h, Lv);
-
-  float4 pre[kChunkF4PerThread];
-  fetch_chunk(pre, gk, 0, n_sub);
-  for (int c0 = 0; c0 < spad; c0 += kChunk) {
-    __syncthreads();
-    stash_chunk(sx, pre);
-    __syncthreads();
-    if (c0 + kChunk < spad) fetch_chunk(pre, gk, c0 + kChunk, n_sub);  // in flight during the products
-    const int col = c0 + 8 * nt + 2 * t4;  // this lane's two key sub-rows: col, col + 1
-    const float lnk0 = ln_count(col, Lv), lnk1 = ln_count(col + 1, Lv);
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      if ((m & 1) != mg) continue;  // warp-uniform: this warp's m16 tiles are mg, mg + 2, ...
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      const float* kb = sx + (8 * nt + g) * kQPad;
-#pragma unroll 4
-      for (int kk = 0; kk < kHeadDim; kk += 8) {
-        uint32_t bh0, bl0, bh1, bl1;
-        split_tf32(kb[kk + t4], bh0, bl0);
-        split_tf32(kb[kk + t4 + 4], bh1, bl1);
-        uint32_t ah[4], al[4];
-        load_a_split(sq + 16 * m * kQPad + kk, kQPad, 16, g, t4, ah, al);
-        mma_split(acc, ah, al, bh0, bh1, bl0, bl1);
-      }
-      // acc: (row g, cols 2t4, 2t4+1), (row g+8, same cols). Row g belongs to
-      // query block 4m + g/4, row g+8 to 4m + 2 + g/4; columns 2t4, 2t4+1 to
-      // key block c0/4 + 2nt + t4/2.
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float x0 = acc[2 * h] * scale + lnq[m][h] + lnk0;
-        const float x1 = acc[2 * h + 1] * scale + lnq[m][h] + lnk1;
-        float mx = fmaxf(x0, x1);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        float sum = 0.f;
-        if (mx > -INFINITY) sum = expf(x0 - mx) + expf(x1 - mx);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-        const int lb = 4 * m + 2 * h + g / 4;  // query block within the CTA
-        if ((g & 3) == 0 && (t4 & 1) == 0 && lb < R)
-          S[lb * bstride + c0 / 4 + 2 * nt + t4 / 2] = mx > -INFINITY ? mx + logf(sum) : -INFINITY;
-      }
-    }
+  if (tid == 0) {
+    mbar_init(bar_q, 1);
+    mbar_init(bar_k0, 1);
+    mbar_init(bar_k0 + 8, 1);
+    fence_barrier_init();
   }
   __syncthreads();
+  int issued = 0;  // key chunks whose copy thread 0 has issued
+  if (tid == 0) {
+    // query sub-rows 4 q0 .. 4 q0 + 4R: R/2 tile8s, contiguous (within spad for every CTA)
+    mbar_arrive_expect_tx(bar_q, (R / 2) * kTile8Bytes);
+    bulk_load(smem_u32(s_q), gq + static_cast<size_t>(q0 / 2) * kTile8Bytes, (R / 2) * kTile8Bytes, bar_q);
+    for (; issued < 2 && issued < n_chunks; ++issued) {
+      mbar_arrive_expect_tx(bar_k0 + 8 * issued, kChunkBytes);
+      bulk_load(smem_u32(s_kbuf + issued * kChunkBytes), gk + static_cast<size_t>(issued) * kChunkBytes,
+                kChunkBytes, bar_k0 + 8 * issued);
+    }
+  }
+
+  const int m = warp / NP, np = warp % NP;
+  const bool has_work = m < MT;
+  // this lane's pair: query block 4 m + (g & 3) of the CTA, key block 4 np + t4 of each chunk;
+  // its query sub-blocks are a0 = 2 (g >> 2) (row g) and a0 + 1 (row g + 8)
+  const int qsub = 4 * (q0 + 4 * m + (g & 3)) + 2 * (g >> 2);
+  const float lq0 = lg_count(qsub, Lv), lq1 = lg_count(qsub + 1, Lv);
+  const uint32_t qa = smem_u32(s_q + (2 * m) * kTile8Bytes) + lane * 16;
+
+  bool ok = mbar_wait(bar_q, 0, err, kDetailRouterQ);
+  // this warp's m16 tile is the same for every chunk: its A fragments stay in registers
+  uint4 aq[kHeadDim / 16][2];
+#pragma unroll
+  for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+    aq[ks][0] = (ok && has_work) ? lds128(qa + ks * 512) : make_uint4(0, 0, 0, 0);                // rows g
+    aq[ks][1] = (ok && has_work) ? lds128(qa + kTile8Bytes + ks * 512) : make_uint4(0, 0, 0, 0);  // rows g + 8
+  }
+  for (int c = 0; c < n_chunks; ++c) {
+    const int slot = c & 1;
+    ok = ok && mbar_wait(bar_k0 + 8 * slot, (c >> 1) & 1, err, kDetailRouterK);
+    if (ok && has_work) {
+      const int kblk = c * (CH / 4) + 4 * np + t4;  // key block of this lane
+      float lk[4];
+#pragma unroll
+      for (int sb = 0; sb < 4; ++sb) lk[sb] = lg_count(4 * kblk + sb, Lv);
+      const uint32_t kb = smem_u32(s_kbuf + slot * kChunkBytes + (2 * np) * kTile8Bytes) + lane * 16;
+      float acc[2][4];
+#pragma unroll
+      for (int ni = 0; ni < 2; ++ni) acc[ni][0] = acc[ni][1] = acc[ni][2] = acc[ni][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+        const uint4 t0 = aq[ks][0], t1 = aq[ks][1];
+#pragma unroll
+        for (int ni = 0; ni < 2; ++ni) {
+          const uint4 bf = lds128(kb + ni * kTile8Bytes + ks * 512);  // {hi b0, hi b1, lo b0, lo b1}
+          // A = {rows g, g+8} x {cols 2t4.., 2t4+8..}: a0 = t0.a, a1 = t1.a, a2 = t0.b, a3 = t1.b
+          mma_bf16(acc[ni], t0.z, t1.z, t0.w, t1.w, bf.x, bf.y);   // lo . hi
+          mma_bf16(acc[ni], t0.x, t1.x, t0.y, t1.y, bf.z, bf.w);   // hi . lo
+          mma_bf16(acc[ni], t0.x, t1.x, t0.y, t1.y, bf.x, bf.y);   // hi . hi
+        }
+      }
+      // acc[ni][e] (e < 2): row g, key sub-block 2 ni + e; acc[ni][2 + e]: row g + 8
+      float x[8];
+#pragma unroll
+      for (int ni = 0; ni < 2; ++ni)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          x[4 * ni + e] = fmaf(acc[ni][e], scale_log2, lq0 + lk[2 * ni + e]);
+          x[4 * ni + 2 + e] = fmaf(acc[ni][2 + e], scale_log2, lq1 + lk[2 * ni + e]);
+        }
+      float mx = x[0];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) mx = fmaxf(mx, x[i]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      float sum = 0.f;
+      if (mx > -INFINITY) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sum += ex2(x[i] - mx);
+      }
+      sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+      if (g < 4)
+        S[(4 * m + g) * bstride + kblk] = mx > -INFINITY ? mx + lg2(sum) : -INFINITY;
+    }
+    __syncthreads();  // every warp is done with this slot
+    if (tid == 0 && ok && c + 2 < n_chunks) {
+      mbar_arrive_expect_tx(bar_k0 + 8 * slot, kChunkBytes);
+      bulk_load(smem_u32(s_kbuf + slot * kChunkBytes), gk + static_cast<size_t>(c + 2) * kChunkBytes,
+                kChunkBytes, bar_k0 + 8 * slot);
+      ++issued;
+    }
+  }
+  if (!__syncthreads_and(ok)) {
+    // gave up: let the copies already issued land before the CTA ends. Thread 0
+    // issued them all; the last two chunks are the latest phase of each slot.
+    if (tid == 0) {
+      mbar_wait_drain(bar_q, 0, kWaitLimitNs);
+      for (int c = max(0, issued - 2); c < issued; ++c)
+        mbar_wait_drain(bar_k0 + 8 * (c & 1), (c >> 1) & 1, kWaitLimitNs);
+    }
+    return;
+  }
 
   for (int r = warp; r < R; r += kWarps)
     if (q0 + r < T)
@@ -165,9 +222,14 @@ subblock_router_kernel(const float* __restrict__ sub_q, const float* __restrict_
                        tile_index + (bh * T + q0 + r) * static_cast<size_t>(k), lane);
 }
 
+int sub_pad(int T) { return (4 * T + 127) / 128 * 128; }  // as subblock_rows_padded
+
+// chunk length for R query blocks per CTA: enough n-pairs to give each of the 16 warps a tile
+int chunk_for(int r) { return r == 16 ? 64 : 128; }
+
 size_t smem_for(int r, int spad) {
-  return (static_cast<size_t>(r) * (spad / 4 + 4) + static_cast<size_t>(4 * r) * kQPad +
-          static_cast<size_t>(kChunk) * kQPad + kWarps * kBins) * sizeof(float);
+  return 2 * static_cast<size_t>(chunk_for(r) / 8) * kTile8Bytes + static_cast<size_t>(r / 2) * kTile8Bytes +
+         static_cast<size_t>(r) * (spad / 4 + 4) * sizeof(float) + 4 * sizeof(uint64_t);
 }
 
 int pick_rows(int spad) {
@@ -176,17 +238,16 @@ int pick_rows(int spad) {
   return 0;
 }
 
-int sub_pad(int T) { return (4 * T + kChunk - 1) / kChunk * kChunk; }
-
-template <int R>
-cudaError_t launch_rows(const Geometry& g, const float* sub_q, const float* sub_k, int32_t* tile_index,
-                        size_t smem, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(subblock_router_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+template <int R, int CH>
+cudaError_t launch_rows(const Geometry& g, const void* frag_q, const void* frag_k, int32_t* tile_index,
+                        unsigned int* err, size_t smem, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(subblock_router_kernel<R, CH>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid((g.T + R - 1) / R, g.B * g.H);
-  subblock_router_kernel<R><<<grid, kThreads, smem, stream>>>(sub_q, sub_k, tile_index, g.T, g.Lv, g.k,
-                                                              sub_pad(g.T));
+  subblock_router_kernel<R, CH><<<grid, kThreads, smem, stream>>>(static_cast<const uint4*>(frag_q),
+                                                                  static_cast<const uint4*>(frag_k), tile_index,
+                                                                  err, g.T, g.Lv, g.k, sub_pad(g.T));
   return cudaGetLastError();
 }
 
@@ -198,14 +259,14 @@ size_t subblock_router_smem_bytes(const Geometry& g, int* rows_per_cta) {
   return r ? smem_for(r, sub_pad(g.T)) : 0;
 }
 
-cudaError_t launch_subblock_router(const Geometry& g, const float* sub_q, const float* sub_k,
-                                   int32_t* tile_index, cudaStream_t stream) {
+cudaError_t launch_subblock_router(const Geometry& g, const void* frag_q, const void* frag_k,
+                                   int32_t* tile_index, unsigned int* err, cudaStream_t stream) {
   int r = 0;
   const size_t smem = subblock_router_smem_bytes(g, &r);
   switch (r) {
-    case 16: return launch_rows<16>(g, sub_q, sub_k, tile_index, smem, stream);
-    case 8: return launch_rows<8>(g, sub_q, sub_k, tile_index, smem, stream);
-    case 4: return launch_rows<4>(g, sub_q, sub_k, tile_index, smem, stream);
+    case 16: return launch_rows<16, 64>(g, frag_q, frag_k, tile_index, err, smem, stream);
+    case 8: return launch_rows<8, 128>(g, frag_q, frag_k, tile_index, err, smem, stream);
+    case 4: return launch_rows<4, 128>(g, frag_q, frag_k, tile_index, err, smem, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -165,6 +165,10 @@ vsa_status_t create_plan(const vsa_shape_t* shape, int device, bool subblock, do
   p->off_coarse = off; off += subblock ? 0 : align_up(pooled);
   p->off_idx = off;  off += align_up(idx);
   p->off_redo = off; off += align_up(static_cast<size_t>(g.B) * g.H * (g.TP + g.T) * sizeof(int32_t));
+  // SubBlock: the sub-block means again, as bf16 hi/lo mma fragments (512 bytes per padded sub-row)
+  const size_t frag = subblock ? static_cast<size_t>(g.B) * g.H * vsa::subblock_rows_padded(g) * 512 : 0;
+  p->off_fq = off;   off += align_up(frag);
+  p->off_fk = off;   off += align_up(frag);
   p->ws_bytes = off;
   p->tensor_bytes = static_cast<size_t>(g.B) * g.N * g.H * vsa::kHeadDim * 2;
   *out = p;
@@ -270,9 +274,11 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
   const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(k);
   if (plan->subblock) {
     // sub-block means are always taken here: the preprocessing pools 64-token tiles
-    if (vsa::launch_subpool(g, qb, kb, pq, pk, st) != cudaSuccess) return VSA_ERR_CUDA;
+    if (vsa::launch_subpool(g, qb, kb, pq, pk, ws + plan->off_fq, ws + plan->off_fk, st) != cudaSuccess)
+      return VSA_ERR_CUDA;
     if ((rs = record(plan, 1, st)) != VSA_OK) return rs;
-    if (vsa::launch_subblock_router(g, pq, pk, idx, st) != cudaSuccess) return VSA_ERR_CUDA;
+    if (vsa::launch_subblock_router(g, ws + plan->off_fq, ws + plan->off_fk, idx, err, st) != cudaSuccess)
+      return VSA_ERR_CUDA;
   } else {
     if (!pool_ready &&
         vsa::launch_pool(g, qb, kb, static_cast<const __nv_bfloat16*>(v), pq, pk, pv, st) != cudaSuccess)
