@@ -486,7 +486,8 @@ def run_ours(args):
         tb = hq.numel() * hq.element_size()
         e2e = {"value": total_flops / e2e_s / 1e12, "unit": UNIT, "ms_per_step": e2e_s * 1e3,
                "h2d_bytes_per_step": 4 * tb, "d2h_bytes_per_step": tb,
-               "api": "vsa_forward_host (C ABI), pinned host buffers, synchronous"}
+               "api": "vsa_forward_host (C ABI), pinned host buffers, synchronous; "
+                      "head groups pipelined: copy-in, forward and copy-out overlap"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -6,6 +6,16 @@
 #include "kernels.cuh"
 #include "vsa.h"
 
+// Head-group pipeline of the host-buffer path: group g's inputs are copied in
+// while group g - 1 computes and group g - 2's output is copied out.
+struct HostPipe {
+  int groups = 0;           // head groups; 1: no pipeline
+  int heads_per_group = 0;  // all groups but the last
+  vsa_plan* sub[2] = {nullptr, nullptr};  // plans for a full group and for the last group
+  cudaStream_t s_in = nullptr, s_out = nullptr;  // created on first use
+  cudaEvent_t entry = nullptr, in_ready[2] = {}, fwd_done[2] = {}, out_done[2] = {};
+};
+
 struct vsa_plan {
   vsa_shape_t shape;
   int device;
@@ -17,4 +27,5 @@ struct vsa_plan {
   size_t tensor_bytes;  // one bf16 [B, N, H, 128] tensor
   cudaEvent_t events[4];
   bool have_events;
+  HostPipe* pipe;       // host-buffer path (null for the plans of head groups)
 };

@@ -175,16 +175,83 @@ vsa_status_t create_plan(const vsa_shape_t* shape, int device, bool subblock, do
   return VSA_OK;
 }
 
+void destroy_plan(vsa_plan* p);
+
+// The host-buffer path pipelines up to 8 head groups (host only: the streams
+// and events are created on the first call).
+vsa_status_t make_pipe(vsa_plan* p, bool subblock) {
+  const int H = p->g.H;
+  const int want = H < 8 ? H : 8;
+  const int hg = (H + want - 1) / want;
+  const int groups = (H + hg - 1) / hg;
+  HostPipe* pipe = new (std::nothrow) HostPipe;
+  if (!pipe) return VSA_ERR_INTERNAL;
+  pipe->groups = groups;
+  pipe->heads_per_group = hg;
+  p->pipe = pipe;
+  if (groups == 1) return VSA_OK;
+  const int last = H - (groups - 1) * hg;
+  vsa_shape_t s = p->shape;
+  for (int i = 0; i < 2; ++i) {
+    if (i == 1 && last == hg) break;
+    s.num_heads = i == 0 ? hg : last;
+    vsa_plan_t sub = nullptr;
+    const vsa_status_t st = create_plan(&s, p->device, subblock, p->sparsity, &sub);
+    if (st != VSA_OK) return st;
+    pipe->sub[i] = sub;
+  }
+  return VSA_OK;
+}
+
+void destroy_plan(vsa_plan* p) {
+  if (!p) return;
+  if (HostPipe* pipe = p->pipe) {
+    for (vsa_plan* sub : pipe->sub) destroy_plan(sub);
+    if (pipe->s_in) {
+      int prev = -1;
+      cudaGetDevice(&prev);
+      cudaSetDevice(p->device);
+      cudaStreamDestroy(pipe->s_in);
+      cudaStreamDestroy(pipe->s_out);
+      cudaEventDestroy(pipe->entry);
+      for (int i = 0; i < 2; ++i) {
+        cudaEventDestroy(pipe->in_ready[i]);
+        cudaEventDestroy(pipe->fwd_done[i]);
+        cudaEventDestroy(pipe->out_done[i]);
+      }
+      if (prev >= 0) cudaSetDevice(prev);
+    }
+    delete pipe;
+  }
+  delete p;
+}
+
 }  // namespace
 
 extern "C" {
 
+namespace {
+
+vsa_status_t create_with_pipe(const vsa_shape_t* shape, int device, bool subblock, double sparsity,
+                              vsa_plan_t* out) {
+  vsa_status_t st = create_plan(shape, device, subblock, sparsity, out);
+  if (st != VSA_OK) return st;
+  st = make_pipe(*out, subblock);
+  if (st != VSA_OK) {
+    destroy_plan(*out);
+    *out = nullptr;
+  }
+  return st;
+}
+
+}  // namespace
+
 vsa_status_t vsa_plan_create(const vsa_shape_t* shape, int device, vsa_plan_t* out) {
-  return create_plan(shape, device, false, 0.0, out);
+  return create_with_pipe(shape, device, false, 0.0, out);
 }
 
 vsa_status_t vsa_plan_create_subblock(const vsa_shape_t* shape, double sparsity, int device, vsa_plan_t* out) {
-  return create_plan(shape, device, true, sparsity, out);
+  return create_with_pipe(shape, device, true, sparsity, out);
 }
 
 vsa_status_t vsa_plan_info(vsa_plan_t plan, int64_t* n_tiles, int64_t* k, size_t* workspace_bytes) {
@@ -397,9 +464,36 @@ vsa_status_t vsa_preprocess(vsa_plan_t plan, const vsa_preprocess_args_t* args, 
   return vsa::launch_preprocess(g, a, st) == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
+namespace {
+
+// Device bytes of one head group's five tensors (q, k, v, gate, out), each 256-byte aligned.
+size_t group_slot_bytes(const vsa_plan* sub) { return 5 * align_up(sub->tensor_bytes); }
+
+size_t pipe_bytes(const vsa_plan* p) {
+  const HostPipe* pipe = p->pipe;
+  if (!pipe || pipe->groups == 1) return 5 * align_up(p->tensor_bytes) + p->ws_bytes;
+  size_t ws = pipe->sub[0]->ws_bytes;
+  if (pipe->sub[1] && pipe->sub[1]->ws_bytes > ws) ws = pipe->sub[1]->ws_bytes;
+  return 2 * group_slot_bytes(pipe->sub[0]) + ws;
+}
+
+vsa_status_t ensure_streams(HostPipe* pipe) {
+  if (pipe->s_in) return VSA_OK;
+  bool ok = cudaStreamCreateWithFlags(&pipe->s_in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&pipe->s_out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&pipe->entry, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; i < 2 && ok; ++i)
+    ok = cudaEventCreateWithFlags(&pipe->in_ready[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&pipe->fwd_done[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&pipe->out_done[i], cudaEventDisableTiming) == cudaSuccess;
+  return ok ? VSA_OK : VSA_ERR_CUDA;
+}
+
+}  // namespace
+
 vsa_status_t vsa_plan_host_path_bytes(vsa_plan_t plan, size_t* bytes) {
   if (!plan || !bytes) return VSA_ERR_INVALID_ARG;
-  *bytes = 5 * align_up(plan->tensor_bytes) + plan->ws_bytes;
+  *bytes = pipe_bytes(plan);
   return VSA_OK;
 }
 
@@ -408,25 +502,71 @@ vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, con
                               size_t device_buffer_bytes, void* stream) {
   if (!plan || !q || !k || !v || !out || !device_buffer) return VSA_ERR_INVALID_ARG;
   if (!gate && !plan->subblock) return VSA_ERR_INVALID_ARG;
-  size_t need = 0;
-  vsa_plan_host_path_bytes(plan, &need);
-  if (device_buffer_bytes < need || !aligned(device_buffer, kAlign)) return VSA_ERR_INVALID_ARG;
+  if (device_buffer_bytes < pipe_bytes(plan) || !aligned(device_buffer, kAlign)) return VSA_ERR_INVALID_ARG;
   DeviceGuard guard(plan->device);
   if (!guard.ok) return VSA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t tb = plan->tensor_bytes, slot = align_up(tb);
   uint8_t* d = static_cast<uint8_t*>(device_buffer);
   const void* hin[4] = {q, k, v, gate};
-  for (int i = 0; i < 4; ++i)
-    if (hin[i] && cudaMemcpyAsync(d + i * slot, hin[i], tb, cudaMemcpyHostToDevice, st) != cudaSuccess)
-      return VSA_ERR_CUDA;
-  vsa_status_t s = vsa_forward(plan, d, d + slot, d + 2 * slot, gate ? d + 3 * slot : nullptr, d + 4 * slot,
-                               d + 5 * slot, plan->ws_bytes, stream);
-  if (s != VSA_OK) return s;
-  if (cudaMemcpyAsync(out, d + 4 * slot, tb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+  HostPipe* pipe = plan->pipe;
+  if (!pipe || pipe->groups == 1) {
+    const size_t tb = plan->tensor_bytes, slot = align_up(tb);
+    for (int i = 0; i < 4; ++i)
+      if (hin[i] && cudaMemcpyAsync(d + i * slot, hin[i], tb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return VSA_ERR_CUDA;
+    vsa_status_t s = vsa_forward(plan, d, d + slot, d + 2 * slot, gate ? d + 3 * slot : nullptr, d + 4 * slot,
+                                 d + 5 * slot, plan->ws_bytes, stream);
+    if (s != VSA_OK) return s;
+    if (cudaMemcpyAsync(out, d + 4 * slot, tb, cudaMemcpyDeviceToHost, st) != cudaSuccess) return VSA_ERR_CUDA;
+    return cudaStreamSynchronize(st) == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
+  }
+
+  // Head groups: group g's q/k/v/gate rows (its heads' 256-byte slices of every
+  // host row) are copied in on s_in, its forward runs on the caller's stream,
+  // and its output is copied out on s_out, two groups' buffers alternating.
+  vsa_status_t rs = ensure_streams(pipe);
+  if (rs != VSA_OK) return rs;
+  const vsa::Geometry& g = plan->g;
+  const size_t rows = static_cast<size_t>(g.B) * g.N;
+  const size_t host_pitch = static_cast<size_t>(g.H) * vsa::kHeadDim * 2;
+  const size_t slot_bytes = group_slot_bytes(pipe->sub[0]);
+  uint8_t* ws = d + 2 * slot_bytes;
+  size_t ws_bytes = pipe->sub[0]->ws_bytes;
+  if (pipe->sub[1] && pipe->sub[1]->ws_bytes > ws_bytes) ws_bytes = pipe->sub[1]->ws_bytes;
+  auto cuda = [](cudaError_t e) { return e == cudaSuccess; };
+  if (!cuda(cudaEventRecord(pipe->entry, st)) || !cuda(cudaStreamWaitEvent(pipe->s_in, pipe->entry, 0)))
     return VSA_ERR_CUDA;
-  if (cudaStreamSynchronize(st) != cudaSuccess) return VSA_ERR_CUDA;
-  return VSA_OK;
+  for (int gi = 0; gi < pipe->groups; ++gi) {
+    const int s = gi & 1;
+    const int h0 = gi * pipe->heads_per_group;
+    vsa_plan* sub = (gi == pipe->groups - 1 && pipe->sub[1]) ? pipe->sub[1] : pipe->sub[0];
+    const size_t width = static_cast<size_t>(sub->g.H) * vsa::kHeadDim * 2;
+    const size_t tslot = align_up(sub->tensor_bytes);
+    uint8_t* base = d + s * slot_bytes;
+    // inputs: slot s is free once the forward of group gi - 2 has read it
+    if (gi >= 2 && !cuda(cudaStreamWaitEvent(pipe->s_in, pipe->fwd_done[s], 0))) return VSA_ERR_CUDA;
+    for (int i = 0; i < 4; ++i)
+      if (hin[i] && !cuda(cudaMemcpy2DAsync(base + i * tslot, width, static_cast<const uint8_t*>(hin[i]) + h0 * 256,
+                                            host_pitch, width, rows, cudaMemcpyHostToDevice, pipe->s_in)))
+        return VSA_ERR_CUDA;
+    if (!cuda(cudaEventRecord(pipe->in_ready[s], pipe->s_in))) return VSA_ERR_CUDA;
+    // forward: after its inputs, and after group gi - 2's output left slot s
+    if (!cuda(cudaStreamWaitEvent(st, pipe->in_ready[s], 0))) return VSA_ERR_CUDA;
+    if (gi >= 2 && !cuda(cudaStreamWaitEvent(st, pipe->out_done[s], 0))) return VSA_ERR_CUDA;
+    rs = vsa_forward(sub, base, base + tslot, base + 2 * tslot, gate ? base + 3 * tslot : nullptr,
+                     base + 4 * tslot, ws, ws_bytes, stream);
+    if (rs != VSA_OK) return rs;
+    if (!cuda(cudaEventRecord(pipe->fwd_done[s], st))) return VSA_ERR_CUDA;
+    // output
+    if (!cuda(cudaStreamWaitEvent(pipe->s_out, pipe->fwd_done[s], 0)) ||
+        !cuda(cudaMemcpy2DAsync(static_cast<uint8_t*>(out) + h0 * 256, host_pitch, base + 4 * tslot, width, width,
+                                rows, cudaMemcpyDeviceToHost, pipe->s_out)) ||
+        !cuda(cudaEventRecord(pipe->out_done[s], pipe->s_out)))
+      return VSA_ERR_CUDA;
+  }
+  for (int s = 0; s < 2 && s < pipe->groups; ++s)
+    if (!cuda(cudaStreamWaitEvent(st, pipe->out_done[s], 0))) return VSA_ERR_CUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
 vsa_status_t vsa_debug_views(vsa_plan_t plan, void* workspace, const float** pooled_q,
@@ -459,6 +599,6 @@ vsa_status_t vsa_check(vsa_plan_t plan, void* workspace, void* stream) {
   return VSA_OK;
 }
 
-void vsa_plan_destroy(vsa_plan_t plan) { delete plan; }
+void vsa_plan_destroy(vsa_plan_t plan) { destroy_plan(plan); }
 
 }  // extern "C"

@@ -226,10 +226,21 @@ vsa_status_t vsa_forward_rows(vsa_plan_t plan, const void* q, const void* k, con
                               size_t workspace_bytes, void* stream);
 
 /* Same forward on HOST buffers (q, k, v, gate read, out written, all bf16
- * [batch, N, num_heads, 128]; pinned memory makes the copies asynchronous).
- * `device_buffer` (>= host_path_bytes from vsa_plan_host_path_bytes, 256-byte
- * aligned) receives the inputs, the output and the workspace. Copies in,
- * runs the forward, copies out, and synchronises `stream` before returning. */
+ * [batch, N, num_heads, 128]; pinned memory makes the copies asynchronous; the
+ * gate may be NULL for a SubBlock plan). `device_buffer` (>= host_path_bytes
+ * from vsa_plan_host_path_bytes, 256-byte aligned) receives the inputs, the
+ * output and the workspace.
+ *
+ * With two or more heads the work is pipelined over up to 8 head groups:
+ *   * each group's heads are copied in on a library-owned stream (strided
+ *     copies of each host row's slice);
+ *   * the group's forward runs on `stream`;
+ *   * its output is copied out on a second library-owned stream;
+ *   * two groups' device buffers alternate.
+ * The results equal vsa_forward's bit for bit. The two streams and their
+ * events are created on the first call and released by vsa_plan_destroy.
+ * Synchronises `stream` before returning; device-side errors are not reported
+ * here. */
 vsa_status_t vsa_plan_host_path_bytes(vsa_plan_t plan, size_t* bytes);
 vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, const void* v,
                               const void* gate, void* out, void* device_buffer,
