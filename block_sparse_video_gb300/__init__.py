@@ -99,6 +99,7 @@ def load_library(path: str = LIB_PATH):
         "vsa_forward": (i32, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "vsa_preprocess": (i32, [vp, ctypes.POINTER(vsa_preprocess_args_t), vp, sz, vp]),
         "vsa_forward_rows": (i32, [vp, vp, vp, vp, vp, ctypes.POINTER(vsa_output_rows_t), i32, vp, sz, vp]),
+        "vsa_forward_lengths": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "vsa_forward_preprocessed": (i32, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "vsa_plan_host_path_bytes": (i32, [vp, ctypes.POINTER(sz)]),
         "vsa_forward_host": (i32, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
@@ -221,6 +222,16 @@ def vsa_forward_rows(plan, q, k, v, gate, rows, preprocessed, workspace, stream=
                                            1 if preprocessed else 0, _ptr(workspace),
                                            workspace.numel() * workspace.element_size(),
                                            _stream_handle(stream)), "vsa_forward_rows")
+
+
+def vsa_forward_lengths(plan, lengths, q, k, v, gate, out, workspace, stream=None):
+    """Enqueue the forward of a request whose lengths (int64 [3] on the device:
+    text, audio, video) the kernels read at run time; the plan's shape is the
+    capacity of the [B, N_cap, H, 128] buffers."""
+    _check(load_library().vsa_forward_lengths(plan, _ptr(lengths), _ptr(q), _ptr(k), _ptr(v), _ptr(gate),
+                                              _ptr(out), _ptr(workspace),
+                                              workspace.numel() * workspace.element_size(),
+                                              _stream_handle(stream)), "vsa_forward_lengths")
 
 
 def vsa_forward_host(plan, q, k, v, gate, out, device_buffer, stream=None):
@@ -387,6 +398,22 @@ class VSA:
         vsa_forward_preprocessed(self.plan, q, k, v, gate, out, self.workspace, stream)
         return out
 
+    def forward_lengths(self, lengths, q, k, v, gate, out=None, stream=None):
+        """Forward of a request whose lengths (device int64 [3]: text, audio,
+        video) are read by the kernels: this object's lengths are the capacity,
+        and the tensors are [B, N_cap, H, 128] with the request in rows 0 .. N - 1.
+        Capture it once in a CUDA graph and replay it for any request that fits."""
+        for name, x in (("q", q), ("k", k), ("v", v), ("gate", gate)):
+            _check_tensor(x, name, self.shape, self.device)
+        if (lengths.dtype != torch.int64 or lengths.numel() != 3 or not lengths.is_contiguous()
+                or lengths.device != self.device):
+            raise ValueError(f"lengths: expected a contiguous int64 [3] tensor on {self.device}")
+        if out is None:
+            out = torch.empty(self.shape, dtype=torch.bfloat16, device=self.device)
+        _check_tensor(out, "out", self.shape, self.device)
+        vsa_forward_lengths(self.plan, lengths, q, k, v, gate, out, self.workspace, stream)
+        return out
+
     def forward_rows(self, q, k, v, gate, out, out_row_map=None, preprocessed=False, stream=None):
         """The forward writing attention token n of batch b to row out_row_map[b, n]
         (or n) of ``out``, a bf16 [B, out_rows, ...] tensor whose rows hold this
@@ -466,7 +493,7 @@ class SubBlock(VSA):
 __all__ = [
     "VSA", "SubBlock", "VsaError", "vsa_plan_create_subblock", "load_library", "header_functions", "vsa_plan_create", "vsa_plan_info",
     "vsa_forward", "vsa_forward_host", "vsa_preprocess", "vsa_forward_preprocessed", "vsa_forward_rows",
-    "vsa_output_rows_t",
+    "vsa_output_rows_t", "vsa_forward_lengths",
     "vsa_preprocess_args_t", "vsa_plan_host_path_bytes", "vsa_debug_views", "vsa_check",
     "vsa_plan_set_stage_events", "vsa_plan_destroy", "vsa_status_string",
     "vsa_forward_static_workspace", "vsa_diag_wait_timeout",

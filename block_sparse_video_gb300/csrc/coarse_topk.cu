@@ -70,13 +70,20 @@ __device__ __forceinline__ void stash_chunk(float* dst, const float4 (&pre)[kChu
   }
 }
 
+// With device lengths the grid and the layout strides are the plan's capacity
+// (T_cap tiles per (b, h), k_cap kept tiles per row, score rows of tpad_cap);
+// the actual T and k come from the lengths, and CTAs past the actual T return.
 template <int R>
 __global__ void __launch_bounds__(kThreads, 1)
 coarse_topk_kernel(const float* __restrict__ pooled_q, const float* __restrict__ pooled_k,
                    const float* __restrict__ pooled_v, float* __restrict__ coarse,
-                   int32_t* __restrict__ tile_index, int T, int k, int tpad) {
+                   int32_t* __restrict__ tile_index, Geometry cap, DeviceLengths dl, int tpad_cap) {
   constexpr int MT = R >= 16 ? R / 16 : 1;  // m16 row tiles (R = 8 leaves rows 8-15 empty)
-  const int sstride = tpad + 4;             // score row stride: conflict-free A-fragment reads
+  const DynGeom dg = dyn_geom(cap, dl);
+  const int T = dg.T, k = dg.k, T_cap = cap.T, k_cap = cap.k;
+  if (!dg.valid || static_cast<int>(blockIdx.x) * R >= T) return;  // uniform per CTA
+  const int tpad = (T + kChunk - 1) / kChunk * kChunk;
+  const int sstride = tpad_cap + 4;         // score row stride: conflict-free A-fragment reads
   extern __shared__ __align__(16) float smem[];
   float* S = smem;                          // [R][sstride] scores, then probabilities
   float* sq = S + R * sstride;              // [16 MT][kQPad] pooled queries
@@ -88,9 +95,9 @@ coarse_topk_kernel(const float* __restrict__ pooled_q, const float* __restrict__
   const int g = lane >> 2, t4 = lane & 3;
   const int t0 = blockIdx.x * R;
   const size_t bh = blockIdx.y;
-  const float* gq = pooled_q + bh * T * kHeadDim;
-  const float* gk = pooled_k + bh * T * kHeadDim;
-  const float* gv = pooled_v + bh * T * kHeadDim;
+  const float* gq = pooled_q + bh * T_cap * kHeadDim;
+  const float* gk = pooled_k + bh * T_cap * kHeadDim;
+  const float* gv = pooled_v + bh * T_cap * kHeadDim;
   const float scale = 0.08838834764831845f;  // 1/sqrt(128)
   const int rows = min(R, T - t0);           // query tiles of this CTA
 
@@ -134,7 +141,8 @@ coarse_topk_kernel(const float* __restrict__ pooled_q, const float* __restrict__
     float* row = S + r * sstride;
     const int t = t0 + r;
     if (t < T)
-      warp_select_topk(row, T, k, hist + warp * kBins, tile_index + (bh * T + t) * static_cast<size_t>(k), lane);
+      warp_select_topk(row, T, k, hist + warp * kBins, tile_index + (bh * T_cap + t) * static_cast<size_t>(k_cap),
+                       lane);
     // softmax over the T tiles (probabilities overwrite the scores)
     float m = -INFINITY;
     for (int j = lane; j < T; j += 32) m = fmaxf(m, row[j]);
@@ -180,7 +188,7 @@ coarse_topk_kernel(const float* __restrict__ pooled_q, const float* __restrict__
       const int r = 16 * m + g + 8 * half;
       if (r < rows) {
         const float inv = 1.0f / sl[r];
-        float* dst = coarse + (bh * T + t0 + r) * kHeadDim;
+        float* dst = coarse + (bh * T_cap + t0 + r) * kHeadDim;
         *reinterpret_cast<float2*>(dst + 8 * warp + 2 * t4) = make_float2(o[m][2 * half] * inv, o[m][2 * half + 1] * inv);
       }
     }
@@ -210,7 +218,7 @@ size_t coarse_smem_bytes(const Geometry& g, int* rows_per_cta) {
 
 cudaError_t launch_coarse_topk(const Geometry& g, const float* pooled_q, const float* pooled_k,
                                const float* pooled_v, float* coarse, int32_t* tile_index,
-                               cudaStream_t stream) {
+                               const DeviceLengths& dl, cudaStream_t stream) {
   int r = 0;
   const size_t smem = coarse_smem_bytes(g, &r);
   if (r == 0) return cudaErrorInvalidValue;
@@ -221,17 +229,17 @@ cudaError_t launch_coarse_topk(const Geometry& g, const float* pooled_q, const f
     case 32:
       e = cudaFuncSetAttribute(coarse_topk_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e == cudaSuccess)
-        coarse_topk_kernel<32><<<grid, kThreads, smem, stream>>>(pooled_q, pooled_k, pooled_v, coarse, tile_index, g.T, g.k, tpad);
+        coarse_topk_kernel<32><<<grid, kThreads, smem, stream>>>(pooled_q, pooled_k, pooled_v, coarse, tile_index, g, dl, tpad);
       break;
     case 16:
       e = cudaFuncSetAttribute(coarse_topk_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e == cudaSuccess)
-        coarse_topk_kernel<16><<<grid, kThreads, smem, stream>>>(pooled_q, pooled_k, pooled_v, coarse, tile_index, g.T, g.k, tpad);
+        coarse_topk_kernel<16><<<grid, kThreads, smem, stream>>>(pooled_q, pooled_k, pooled_v, coarse, tile_index, g, dl, tpad);
       break;
     default:
       e = cudaFuncSetAttribute(coarse_topk_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e == cudaSuccess)
-        coarse_topk_kernel<8><<<grid, kThreads, smem, stream>>>(pooled_q, pooled_k, pooled_v, coarse, tile_index, g.T, g.k, tpad);
+        coarse_topk_kernel<8><<<grid, kThreads, smem, stream>>>(pooled_q, pooled_k, pooled_v, coarse, tile_index, g, dl, tpad);
       break;
   }
   if (e != cudaSuccess) return e;

@@ -85,7 +85,8 @@ constexpr uint32_t kOffBar = kOffP + kNumP * kPBytes;
 constexpr uint32_t kOffRed = kOffBar + 512;
 constexpr uint32_t kOffItems = kOffRed + 64 * 4 * 4;  // red: [64 query columns][4 lane quarters] fp32
 constexpr uint32_t kOffSlot = kOffItems + kItemSlots * 4;
-constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;  // + 1024-byte alignment slack
+constexpr uint32_t kOffGeo = kOffSlot + 16;            // this forward's geometry (FineGeo)
+constexpr uint32_t kSmemBytes = kOffGeo + 32 + 1024;   // + 1024-byte alignment slack
 
 // barrier indices
 constexpr int kBarQFull = 0;
@@ -109,9 +110,14 @@ static_assert(kNumK == kNumS, "K slot g % kNumK is released through S-full barri
 static_assert(kColO + kNumO * 64 <= kTmemCols, "TMEM columns");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
+// Geometry of the plan: the capacity when lengths come from the device. N is
+// the buffer rows per batch, T and k the layout strides of the coarse rows and
+// tile selections; P, Lv, TP, T, k and n_items are this forward's own unless
+// dl.len is set (then FineGeo holds the actual ones).
 struct FineParams {
   int B, H, P, Lv, N, T, TP, k;
   int n_items;          // B * H * (TP + T)
+  DeviceLengths dl;
   float scale_log2;
   const __nv_bfloat16* gate;
   __nv_bfloat16* out;
@@ -126,6 +132,18 @@ struct FineParams {
   int* redo_list;
 };
 
+// This forward's geometry, computed once per CTA into shared memory.
+struct FineGeo {
+  int P, Lv, T, TP, k, n_items;
+};
+
+__device__ __forceinline__ FineGeo fine_geo(const FineParams& p) {
+  Geometry cap;
+  cap.B = p.B; cap.H = p.H; cap.P = p.P; cap.Lv = p.Lv; cap.N = p.N; cap.T = p.T; cap.TP = p.TP; cap.k = p.k;
+  const DynGeom d = dyn_geom(cap, p.dl);
+  return FineGeo{d.P, d.Lv, d.T, d.TP, d.k, d.valid ? p.B * p.H * (d.TP + d.T) : 0};
+}
+
 struct Item {
   int b, h, t;
   bool video;
@@ -138,26 +156,27 @@ struct Item {
 // tiles (the long, dense items) and then its T video query tiles. The CTAs in
 // flight at any time then read the K/V of one or two heads, which stay resident
 // in L2; taking all prefix items first would stream every head's K/V at once.
-__device__ __forceinline__ Item decode_item(const FineParams& p, int item) {
+__device__ __forceinline__ Item decode_item(const FineParams& p, const FineGeo& G, int item) {
   Item it;
-  const int per_head = p.TP + p.T;
+  const int per_head = G.TP + G.T;
   const int bh = item / per_head;
   const int local = item - bh * per_head;
   it.b = bh / p.H;
   it.h = bh - it.b * p.H;
-  if (local < p.TP) {
+  if (local < G.TP) {
     it.video = false;
     it.t = local;
     it.q_row0 = it.t * kTile;
-    it.q_valid = min(kTile, p.P - it.q_row0);
-    it.n_kv = p.TP + p.T;
+    it.q_valid = min(kTile, G.P - it.q_row0);
+    it.n_kv = G.TP + G.T;
     it.list = nullptr;
   } else {
     it.video = true;
-    it.t = local - p.TP;
-    it.q_row0 = p.P + it.t * kTile;
-    it.q_valid = min(kTile, p.Lv - it.t * kTile);
-    it.n_kv = p.TP + p.k;
+    it.t = local - G.TP;
+    it.q_row0 = G.P + it.t * kTile;
+    it.q_valid = min(kTile, G.Lv - it.t * kTile);
+    it.n_kv = G.TP + G.k;
+    // selections are stored at the plan's strides (T and k of the capacity)
     it.list = p.tile_index + ((static_cast<size_t>(it.b) * p.H + it.h) * p.T + it.t) * p.k;
   }
   return it;
@@ -199,7 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_g,
                  const FineParams p) {
-  const int n_work = kExact ? *reinterpret_cast<const volatile int*>(p.redo_count) : p.n_items;
+  const FineGeo geo = fine_geo(p);
+  const int n_work = kExact ? *reinterpret_cast<const volatile int*>(p.redo_count) : geo.n_items;
   if (n_work <= 0) return;  // uniform: nothing to do (the exact kernel's usual case)
 
   extern __shared__ uint8_t smem_raw[];
@@ -214,11 +234,13 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
   float* red = reinterpret_cast<float*>(smem + kOffRed);
   volatile int* items = reinterpret_cast<volatile int*>(smem + kOffItems);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
+  FineGeo* s_geo = reinterpret_cast<FineGeo*>(smem + kOffGeo);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   unsigned int* err = p.err;
 
   if (tid == 0) {
+    *s_geo = geo;
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 1);
     for (int s = 0; s < kNumK; ++s) mbar_init(bar(kBarKFull + s), 1);
@@ -243,6 +265,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
+  const FineGeo& G = *s_geo;
 
   // Item n of this CTA (n = 0, 1, ...) sits in ring slot n % kItemSlots; -1
   // ends the sequence. Read by lane 0 of each reading warp, then broadcast.
@@ -303,7 +326,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         item = read_item(n, ok);
       }
       if (!ok || item < 0) break;
-      const Item it = decode_item(p, item);
+      const Item it = decode_item(p, G, item);
       const int nblk = (it.n_kv + 1) / 2;
       if (!v_warp && lane == 0) {
         // Into L2 ahead of use: the item's Q tile (loaded once its S^T products
@@ -318,12 +341,12 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                            kHeadDim * sizeof(float));
         }
       }
-      // Token row of key tile ti of this item (p.N for an absent tile: the TMA
+      // Token row of key tile ti of this item (p.N, the buffer rows, for an absent tile: the TMA
       // box is then fully out of bounds and reads as zeros).
       auto tile_row = [&](int ti) -> int {
         if (ti >= it.n_kv) return p.N;
-        if (ti < p.TP) return ti * kTile;
-        return p.P + (it.list ? __ldg(it.list + (ti - p.TP)) : ti - p.TP) * kTile;
+        if (ti < G.TP) return ti * kTile;
+        return G.P + (it.list ? __ldg(it.list + (ti - G.TP)) : ti - G.TP) * kTile;
       };
       // Rows are worked out 32 blocks at a time, lane l taking block base + l,
       // so that each block only needs two shuffles here (this warp's loop is on
@@ -377,7 +400,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
     auto load_q = [&](int itm) {
       if (lane == 0) {
-        const Item qi = decode_item(p, itm);
+        const Item qi = decode_item(p, G, itm);
         mbar_arrive_expect_tx(bar(kBarQFull), kQBytes);
         for (int c = 0; c < 2; ++c)
           tma_load_4d(sQ + c * 8192, &map_q, 64 * c, qi.h, qi.q_row0, qi.b, bar(kBarQFull));
@@ -387,7 +410,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     if (ok && item >= 0) load_q(item);
     uint32_t g = 0;  // blocks issued so far, over all items
     for (int n = 0; ok && item >= 0; ++n) {
-      const Item it = decode_item(p, item);
+      const Item it = decode_item(p, G, item);
       const int nblk = (it.n_kv + 1) / 2;
       ok = mbar_wait_warp(bar(kBarQFull), n & 1, err, 0x500u, 64);
       for (int i = 0; i < nblk && ok; ++i, ++g) {
@@ -425,7 +448,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     for (int n = 0; ok; ++n) {
       const int item = read_item(n, ok);
       if (!ok || item < 0) break;
-      const Item it = decode_item(p, item);
+      const Item it = decode_item(p, G, item);
       const int nblk = (it.n_kv + 1) / 2;
       const uint32_t ob = n % kNumO;
       // accumulator ob was last read by the epilogue of item n - kNumO
@@ -458,11 +481,11 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     const float2 sl2v = make_float2(sl2, sl2);
     // Only two key tiles can be ragged: the last prefix tile, and video tile T-1,
     // which (selections being ascending) can only be the item's last key tile.
-    const int prefix_tail = p.TP > 0 ? p.P - (p.TP - 1) * kTile : kTile;
-    const int video_tail = p.Lv - (p.T - 1) * kTile;
+    const int prefix_tail = G.TP > 0 ? G.P - (G.TP - 1) * kTile : kTile;
+    const int video_tail = G.Lv - (G.T - 1) * kTile;
     // Blocks that may hold masked key lanes: the one with the ragged last prefix
     // tile, and the last block (an absent second tile, or ragged video tile T-1).
-    const int ragged_prefix_blk = (p.TP > 0 && prefix_tail < kTile) ? (p.TP - 1) / 2 : -1;
+    const int ragged_prefix_blk = (G.TP > 0 && prefix_tail < kTile) ? (G.TP - 1) / 2 : -1;
     const size_t row_stride = static_cast<size_t>(p.H) * kHeadDim;
     bool failed = false;
     uint32_t gs = 0;  // blocks consumed so far, over all items
@@ -472,11 +495,11 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       failed = failed || !ok;
       // all softmax warps read the same item sequence; agree on stopping
       if (named_bar_or(kBarSoftmaxAll, 32 * kSoftmaxWarps, failed || item < 0)) break;
-      const Item it = decode_item(p, item);
+      const Item it = decode_item(p, G, item);
       const int nblk = (it.n_kv + 1) / 2;
       const uint32_t ob = n % kNumO;
       const bool last_is_ragged =
-          video_tail < kTile && (it.list == nullptr || __ldg(it.list + p.k - 1) == p.T - 1);
+          video_tail < kTile && (it.list == nullptr || __ldg(it.list + G.k - 1) == G.T - 1);
       // Per column pair: -reference (log2 units) and this lane's partial row sums.
       float2 nm2[kCols / 2], l2[kCols / 2];
 #pragma unroll
@@ -491,7 +514,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         const uint32_t ph = (g / kNumS) & 1, pph = (g / kNumP) & 1;
         const int ti = 2 * i + key_slot;
         bool valid = ti < it.n_kv;
-        if (ti == p.TP - 1) valid = key_row < prefix_tail;
+        if (ti == G.TP - 1) valid = key_row < prefix_tail;
         if (ti == it.n_kv - 1 && last_is_ragged) valid = valid && key_row < video_tail;
 
         failed = warp_any(failed || !mbar_wait(bar(kBarSFull + st), ph, err, 0x800u));
@@ -754,7 +777,8 @@ cudaError_t launch_fine(const Geometry& g, const CUtensorMap& map_q, const CUten
                         cudaStream_t stream) {
   FineParams p;
   p.B = g.B; p.H = g.H; p.P = g.P; p.Lv = g.Lv; p.N = g.N; p.T = g.T; p.TP = g.TP; p.k = g.k;
-  p.n_items = g.B * g.H * (g.TP + g.T);
+  p.n_items = g.B * g.H * (g.TP + g.T);  // the capacity's, for the grid; the kernels use FineGeo
+  p.dl = a.dl;
   p.scale_log2 = 1.4426950408889634f * 0.08838834764831845f;
   p.gate = a.gate;
   p.out = a.out;

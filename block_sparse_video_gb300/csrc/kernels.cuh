@@ -22,11 +22,45 @@ struct Geometry {
   int k = 0;   // kept video tiles per video query tile
 };
 
+// Lengths read on the device (a capacity plan's forward): the plan's geometry
+// is the capacity (buffer rows per batch N, tiles T, kept tiles k: the layout
+// strides); the actual text/audio/video lengths come from `len` (3 x int64)
+// and must satisfy text, audio >= 0, 1 <= video <= Lv, text + audio <= P.
+struct DeviceLengths {
+  const long long* len = nullptr;  // null: the plan's own lengths
+  double keep = 0.0;               // keep fraction (the actual k is derived from the actual T)
+  unsigned int* invalid = nullptr; // set to 1 when the lengths are outside the capacity
+};
+
+// Actual geometry of one forward: the plan's, or the one the device lengths give.
+struct DynGeom {
+  int P, Lv, T, TP, k;
+  bool valid;
+};
+
+__device__ __forceinline__ DynGeom dyn_geom(const Geometry& cap, const DeviceLengths& dl) {
+  DynGeom d{cap.P, cap.Lv, cap.T, cap.TP, cap.k, true};
+  if (!dl.len) return d;
+  const long long text = dl.len[0], audio = dl.len[1], video = dl.len[2];
+  if (text < 0 || audio < 0 || video < 1 || video > cap.Lv || text + audio > cap.P) {
+    d.valid = false;
+    return d;
+  }
+  d.P = static_cast<int>(text + audio);
+  d.Lv = static_cast<int>(video);
+  d.T = (d.Lv + kTile - 1) / kTile;
+  d.TP = (d.P + kTile - 1) / kTile;
+  // "rounded to a whole number of tiles": round half up in IEEE double, clamped to [1, T]
+  int k = static_cast<int>(floor(dl.keep * static_cast<double>(d.T) + 0.5));
+  d.k = k < 1 ? 1 : (k > d.T ? d.T : k);
+  return d;
+}
+
 // Tile pool: mean over the valid tokens of each video tile of q, k and v.
-// pooled_* are fp32 [B, H, T, 128].
+// pooled_* are fp32 [B, H, T, 128] (T of the plan: the layout stride).
 cudaError_t launch_pool(const Geometry& g, const __nv_bfloat16* q, const __nv_bfloat16* k,
                         const __nv_bfloat16* v, float* pooled_q, float* pooled_k,
-                        float* pooled_v, cudaStream_t stream);
+                        float* pooled_v, const DeviceLengths& dl, cudaStream_t stream);
 
 // Fused attention preprocessing: Q/K RMSNorm, partial RoPE, packing of the
 // projection rows into [B, N, H, 128], gate copy and the Q/K/V tile pooling.
@@ -53,7 +87,7 @@ cudaError_t launch_preprocess(const Geometry& g, const PreprocessArgs& a, cudaSt
 size_t coarse_smem_bytes(const Geometry& g, int* rows_per_cta);
 cudaError_t launch_coarse_topk(const Geometry& g, const float* pooled_q, const float* pooled_k,
                                const float* pooled_v, float* coarse, int32_t* tile_index,
-                               cudaStream_t stream);
+                               const DeviceLengths& dl, cudaStream_t stream);
 
 // SubBlock routing: 16-token sub-block means of q and k (fp32 [B, H, 4T, 128],
 // empty sub-blocks of a ragged last tile as 0, plus the same values split into
@@ -85,6 +119,7 @@ struct FineArgs {
   int* redo_count;     // zero before the launch
   int* redo_list;      // int32 [B * H * (TP + T)]
   int* work_counters;  // 2 counters, zero before the launch
+  DeviceLengths dl;
 };
 size_t fine_smem_bytes();
 cudaError_t launch_fine(const Geometry& g, const CUtensorMap& map_q, const CUtensorMap& map_k,

@@ -31,18 +31,27 @@ __device__ __forceinline__ void accumulate(float (&acc)[8], const uint4& w) {
 
 // kLen-token runs: run t of batch b covers video tokens kLen t .. kLen t + n - 1
 // (n = min(kLen, Lv - kLen t), possibly <= 0); blockIdx.z picks q, k or v.
+// With device lengths, the grid covers the plan's capacity and runs past the
+// actual video return at once.
 template <int kLen>
 __global__ void __launch_bounds__(kPoolThreads)
 pool_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
             const __nv_bfloat16* __restrict__ v, float* __restrict__ pq, float* __restrict__ pk,
-            float* __restrict__ pv, int B, int H, int P, int Lv, int N, int T) {
+            float* __restrict__ pv, Geometry cap, DeviceLengths dl) {
+  const int H = cap.H, N = cap.N, T = cap.T;
+  const DynGeom dg = dyn_geom(cap, dl);
+  if (!dg.valid) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) *dl.invalid = 1u;
+    return;
+  }
+  const int P = dg.P, Lv = dg.Lv;
   const int vec = blockIdx.y * kPoolThreads + threadIdx.x;  // 16-byte vector within a row
   const int row_vecs = H * (kHeadDim / 8);
   const int bt = blockIdx.x;  // b * T + t (T runs per batch)
   const int b = bt / T, t = bt % T;
   const __nv_bfloat16* src = blockIdx.z == 0 ? q : (blockIdx.z == 1 ? k : v);
   float* dst = blockIdx.z == 0 ? pq : (blockIdx.z == 1 ? pk : pv);
-  if (vec >= row_vecs) return;
+  if (vec >= row_vecs || t >= dg.T) return;
   const int n = min(kLen, Lv - t * kLen);
   const int h = vec / (kHeadDim / 8);
   const int d0 = (vec % (kHeadDim / 8)) * 8;
@@ -175,11 +184,10 @@ subpool_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
 
 cudaError_t launch_pool(const Geometry& g, const __nv_bfloat16* q, const __nv_bfloat16* k,
                         const __nv_bfloat16* v, float* pooled_q, float* pooled_k,
-                        float* pooled_v, cudaStream_t stream) {
+                        float* pooled_v, const DeviceLengths& dl, cudaStream_t stream) {
   const int row_vecs = g.H * (kHeadDim / 8);
   dim3 grid(g.B * g.T, (row_vecs + kPoolThreads - 1) / kPoolThreads, 3);
-  pool_kernel<kTile><<<grid, kPoolThreads, 0, stream>>>(q, k, v, pooled_q, pooled_k, pooled_v, g.B, g.H,
-                                                        g.P, g.Lv, g.N, g.T);
+  pool_kernel<kTile><<<grid, kPoolThreads, 0, stream>>>(q, k, v, pooled_q, pooled_k, pooled_v, g, dl);
   return cudaGetLastError();
 }
 

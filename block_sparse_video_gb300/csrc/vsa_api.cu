@@ -284,10 +284,14 @@ namespace {
 // error word, then pools Q/K/V) and vsa_forward_preprocessed (pool_ready = true:
 // the pooled statistics and word 7 come from vsa_preprocess and are kept).
 // Output layout: null `rows` means the packed [B, N, H, 128] tensor `out`.
+// Lengths: null means the plan's own; otherwise device memory read by the kernels.
 vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const void* v, const void* gate,
                           void* out, void* workspace, size_t workspace_bytes, void* stream,
-                          bool pool_ready, const vsa_output_rows_t* rows = nullptr) {
+                          bool pool_ready, const vsa_output_rows_t* rows = nullptr,
+                          const vsa_lengths_t* lengths = nullptr) {
   if (!plan || !q || !k || !v || !out || !workspace) return VSA_ERR_INVALID_ARG;
+  if (lengths && (plan->subblock || pool_ready)) return VSA_ERR_UNSUPPORTED;
+  if (lengths && !aligned(lengths, 8)) return VSA_ERR_INVALID_ARG;
   if (!gate && !plan->subblock) return VSA_ERR_INVALID_ARG;  // SubBlock routing has no gate
   if (workspace_bytes < plan->ws_bytes || !aligned(workspace, kAlign)) return VSA_ERR_INVALID_ARG;
   const void* ins[4] = {q, k, v, gate};
@@ -332,9 +336,17 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
   if (plan->num_sms == 0 &&
       cudaDeviceGetAttribute(&plan->num_sms, cudaDevAttrMultiProcessorCount, plan->device) != cudaSuccess)
     return VSA_ERR_CUDA;
-  // error words 0-2, redo count (word 4), the fine kernels' work counters (words 5, 6) and,
-  // unless the preprocessing just wrote it, its bad-map-entry word (7)
-  if (cudaMemsetAsync(err, 0, pool_ready ? 28 : 32, st) != cudaSuccess) return VSA_ERR_CUDA;
+  // Error words: 0-2 (first error, detail, abort flag), 3 (bad output row map entry), 4 (redo
+  // count), 5-6 (the fine kernels' work counters), 7 (bad preprocessing map entry, kept when the
+  // preprocessing just wrote it) and 9 (device lengths outside the capacity).
+  if (cudaMemsetAsync(err, 0, pool_ready ? 28 : 40, st) != cudaSuccess) return VSA_ERR_CUDA;
+  if (pool_ready && cudaMemsetAsync(err + 8, 0, 8, st) != cudaSuccess) return VSA_ERR_CUDA;
+  vsa::DeviceLengths dl;
+  if (lengths) {
+    dl.len = reinterpret_cast<const long long*>(lengths);
+    dl.keep = plan->shape.keep_fraction;
+    dl.invalid = err + 9;
+  }
   vsa_status_t rs = record(plan, 0, st);
   if (rs != VSA_OK) return rs;
   const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(q);
@@ -348,16 +360,17 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
       return VSA_ERR_CUDA;
   } else {
     if (!pool_ready &&
-        vsa::launch_pool(g, qb, kb, static_cast<const __nv_bfloat16*>(v), pq, pk, pv, st) != cudaSuccess)
+        vsa::launch_pool(g, qb, kb, static_cast<const __nv_bfloat16*>(v), pq, pk, pv, dl, st) != cudaSuccess)
       return VSA_ERR_CUDA;
     if ((rs = record(plan, 1, st)) != VSA_OK) return rs;
-    if (vsa::launch_coarse_topk(g, pq, pk, pv, coarse, idx, st) != cudaSuccess) return VSA_ERR_CUDA;
+    if (vsa::launch_coarse_topk(g, pq, pk, pv, coarse, idx, dl, st) != cudaSuccess) return VSA_ERR_CUDA;
   }
   if ((rs = record(plan, 2, st)) != VSA_OK) return rs;
   vsa::FineArgs a;
   a.gate = static_cast<const __nv_bfloat16*>(gate);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.coarse = plan->subblock ? nullptr : coarse;
+  a.dl = dl;
   if (rows) {
     a.out_row_map = rows->out_row_map;
     a.out_rows = rows->out_rows;
@@ -395,6 +408,13 @@ vsa_status_t vsa_forward_preprocessed(vsa_plan_t plan, const void* q, const void
                                       const void* gate, void* out, void* workspace,
                                       size_t workspace_bytes, void* stream) {
   return forward_impl(plan, q, k, v, gate, out, workspace, workspace_bytes, stream, true);
+}
+
+vsa_status_t vsa_forward_lengths(vsa_plan_t plan, const vsa_lengths_t* lengths, const void* q, const void* k,
+                                 const void* v, const void* gate, void* out, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (!lengths) return VSA_ERR_INVALID_ARG;
+  return forward_impl(plan, q, k, v, gate, out, workspace, workspace_bytes, stream, false, nullptr, lengths);
 }
 
 vsa_status_t vsa_forward_rows(vsa_plan_t plan, const void* q, const void* k, const void* v, const void* gate,
@@ -439,8 +459,8 @@ vsa_status_t vsa_preprocess(vsa_plan_t plan, const vsa_preprocess_args_t* args, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   unsigned int* err = reinterpret_cast<unsigned int*>(ws + plan->off_err);
-  // a preprocessing starts a new call sequence: every error word and counter starts at zero
-  if (cudaMemsetAsync(err, 0, 32, st) != cudaSuccess) return VSA_ERR_CUDA;
+  // a preprocessing starts a new call sequence: every error word and counter (0-9) starts at zero
+  if (cudaMemsetAsync(err, 0, 40, st) != cudaSuccess) return VSA_ERR_CUDA;
   vsa::PreprocessArgs a;
   for (int i = 0; i < 4; ++i) {
     a.in[i] = static_cast<const __nv_bfloat16*>(ins[i]);
@@ -588,7 +608,7 @@ vsa_status_t vsa_check(vsa_plan_t plan, void* workspace, void* stream) {
   if (!guard.ok) return VSA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return VSA_ERR_CUDA;
-  unsigned int words[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  unsigned int words[10] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
   if (cudaMemcpy(words, static_cast<uint8_t*>(workspace) + plan->off_err, sizeof(words),
                  cudaMemcpyDeviceToHost) != cudaSuccess)
     return VSA_ERR_CUDA;
@@ -596,6 +616,7 @@ vsa_status_t vsa_check(vsa_plan_t plan, void* workspace, void* stream) {
   if (words[0] != 0) return VSA_ERR_INTERNAL;
   if (words[7] != 0) return VSA_ERR_INVALID_ARG;  // a preprocessing map entry outside its buffer
   if (words[3] != 0) return VSA_ERR_INVALID_ARG;  // an output map entry outside the output rows
+  if (words[9] != 0) return VSA_ERR_INVALID_ARG;  // device lengths outside the plan's capacity
   return VSA_OK;
 }
 

@@ -197,6 +197,49 @@ vsa_status_t vsa_forward_preprocessed(vsa_plan_t plan, const void* q, const void
                                       const void* gate, void* out, void* workspace,
                                       size_t workspace_bytes, void* stream);
 
+/* Lengths of one request, read by the kernels at run time (device memory,
+ * 8-byte aligned): the token counts of the text, audio and video segments. */
+typedef struct {
+  int64_t len_text;
+  int64_t len_audio;
+  int64_t len_video;
+} vsa_lengths_t;
+
+/* The forward of a request whose lengths live in DEVICE memory, inside a
+ * capacity-padded buffer ("UniServe: serving FastH3 at its fastest", section
+ * "Architecture": workspaces are allocated once for the largest shape and
+ * smaller shapes run on views of it; CUDA graphs are captured once per shape
+ * bucket and address each request through device-side tensors).
+ *
+ * The plan's shape is the capacity. q, k, v, gate and out are bf16
+ * [batch, N_cap, num_heads, 128] with N_cap = the plan's text + audio + video.
+ * The request's tokens occupy rows 0 .. N - 1 of each batch (text, then audio,
+ * then video, N = len_text + len_audio + len_video). The kernels read
+ * *lengths when they run, so one captured graph of this call serves every
+ * request that fits the capacity: write the next request's lengths into the
+ * same device buffer and replay.
+ *
+ * Requirements and effects:
+ *   - 0 <= len_text, 0 <= len_audio, len_text + len_audio <= the plan's
+ *     len_text + len_audio, and 1 <= len_video <= the plan's len_video.
+ *     Otherwise nothing is computed, out is untouched and vsa_check reports
+ *     VSA_ERR_INVALID_ARG;
+ *   - k = max(1, min(T, floor(keep_fraction * T + 0.5))) for the request's T;
+ *   - rows N .. N + 63 of q, k and v (capacity padding, when it exists) must
+ *     hold finite values. A ragged last tile's loads read them, and they are
+ *     masked by exact zeros, so NaN or Inf there would propagate. The
+ *     preprocessing writes real rows only; clearing the padding once at
+ *     allocation is enough;
+ *   - rows N .. N_cap - 1 of out are not written;
+ *   - the workspace and its views (vsa_debug_views) keep the plan's layout:
+ *     the request's tiles are the first T rows of each [T_cap] block, and
+ *     its selections the first k entries of each row of k_cap.
+ * SubBlock plans return VSA_ERR_UNSUPPORTED. Otherwise as vsa_forward
+ * (capture-safe, four kernels). */
+vsa_status_t vsa_forward_lengths(vsa_plan_t plan, const vsa_lengths_t* lengths, const void* q, const void* k,
+                                 const void* v, const void* gate, void* out, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 /* Where the forward writes its output rows. The combined rows can go straight
  * into another layout, such as the send buffer of the output all-to-all that
  * restores sequence sharding ("UniServe: serving FastH3 at its fastest",
@@ -257,8 +300,9 @@ vsa_status_t vsa_debug_views(vsa_plan_t plan, void* workspace, const float** poo
 
 /* Synchronise `stream` and report the device error words of `workspace`:
  * VSA_OK; VSA_ERR_DEVICE_TIMEOUT if a bounded wait gave up; VSA_ERR_INVALID_ARG
- * if the last vsa_preprocess met a map entry outside its projection buffer or
- * the last vsa_forward_rows an output map entry outside its rows. */
+ * if the last vsa_preprocess met a map entry outside its projection buffer,
+ * the last vsa_forward_rows an output map entry outside its rows, or the last
+ * vsa_forward_lengths lengths outside the plan's capacity. */
 vsa_status_t vsa_check(vsa_plan_t plan, void* workspace, void* stream);
 
 /* Optional per-kernel timing. When `events` is non-NULL, each vsa_forward
