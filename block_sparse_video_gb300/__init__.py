@@ -66,6 +66,7 @@ class vsa_preprocess_args_t(ctypes.Structure):
         ("k_out", ctypes.c_void_p),
         ("v_out", ctypes.c_void_p),
         ("gate_out", ctypes.c_void_p),
+        ("lengths", ctypes.c_void_p),
     ]
 
 
@@ -75,6 +76,19 @@ class vsa_output_rows_t(ctypes.Structure):
         ("out_rows", ctypes.c_int64),
         ("out_row_stride", ctypes.c_int64),
         ("out_row_map", ctypes.c_void_p),
+    ]
+
+
+class vsa_forward_args_t(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p),
+        ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
+        ("gate", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+        ("rows", ctypes.POINTER(vsa_output_rows_t)),
+        ("lengths", ctypes.c_void_p),
+        ("preprocessed", ctypes.c_int32),
     ]
 
 
@@ -100,6 +114,7 @@ def load_library(path: str = LIB_PATH):
         "vsa_preprocess": (i32, [vp, ctypes.POINTER(vsa_preprocess_args_t), vp, sz, vp]),
         "vsa_forward_rows": (i32, [vp, vp, vp, vp, vp, ctypes.POINTER(vsa_output_rows_t), i32, vp, sz, vp]),
         "vsa_forward_lengths": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "vsa_forward_ex": (i32, [vp, ctypes.POINTER(vsa_forward_args_t), vp, sz, vp]),
         "vsa_forward_preprocessed": (i32, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "vsa_plan_host_path_bytes": (i32, [vp, ctypes.POINTER(sz)]),
         "vsa_forward_host": (i32, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
@@ -186,6 +201,13 @@ def vsa_plan_destroy(plan):
         load_library().vsa_plan_destroy(plan)
 
 
+def _check_lengths(lengths, device):
+    if (lengths.dtype != torch.int64 or lengths.numel() != 3 or not lengths.is_contiguous()
+            or lengths.device != device):
+        raise ValueError(f"lengths: expected a contiguous int64 [3] tensor on {device}")
+    return lengths
+
+
 def _check_tensor(x, name, shape, device=None):
     if x.dtype != torch.bfloat16 or tuple(x.shape) != tuple(shape) or not x.is_contiguous():
         raise ValueError(f"{name}: expected contiguous bf16 {tuple(shape)}, got {x.dtype} {tuple(x.shape)}")
@@ -232,6 +254,13 @@ def vsa_forward_lengths(plan, lengths, q, k, v, gate, out, workspace, stream=Non
                                               _ptr(out), _ptr(workspace),
                                               workspace.numel() * workspace.element_size(),
                                               _stream_handle(stream)), "vsa_forward_lengths")
+
+
+def vsa_forward_ex(plan, args, workspace, stream=None):
+    """Enqueue the general forward; ``args`` is a filled vsa_forward_args_t."""
+    _check(load_library().vsa_forward_ex(plan, ctypes.byref(args), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(),
+                                         _stream_handle(stream)), "vsa_forward_ex")
 
 
 def vsa_forward_host(plan, q, k, v, gate, out, device_buffer, stream=None):
@@ -344,7 +373,7 @@ class VSA:
 
     def preprocess(self, q_in, k_in, v_in, gate_in, q_norm_weight, k_norm_weight, rope_cos=None,
                    rope_sin=None, rope_dim=0, rope_interleaved=True, eps=1e-6, src_row=None, out=None,
-                   stream=None):
+                   lengths=None, stream=None):
         """Fused preprocessing of projection rows into packed (q, k, v, gate).
 
         q_in .. gate_in: bf16 [B, rows_in, H, 128] views sharing one row stride
@@ -352,7 +381,8 @@ class VSA:
         contiguous. q/k_norm_weight: fp32 [H, 128]. rope_cos/sin: fp32
         [N, rope_dim / 2]. src_row: int32 [B, N] or None. out: optional tuple
         of four bf16 [B, N, H, 128] tensors. The pooled statistics stay in this
-        object's workspace for forward_preprocessed.
+        object's workspace for forward_preprocessed. lengths: optional device
+        int64 [3] (text, audio, video) of a request inside this plan's capacity.
         """
         ins = (q_in, k_in, v_in, gate_in)
         b, h = self.batch, self.num_heads
@@ -384,7 +414,7 @@ class VSA:
             _ptr(q_in), _ptr(k_in), _ptr(v_in), _ptr(gate_in), rows_in, row_stride, _ptr(src_row),
             _ptr(q_norm_weight), _ptr(k_norm_weight), float(eps), int(rope_dim), 1 if rope_interleaved else 0,
             _ptr(rope_cos) if rope_dim else None, _ptr(rope_sin) if rope_dim else None,
-            *[_ptr(x) for x in out])
+            *[_ptr(x) for x in out], _ptr(_check_lengths(lengths, self.device)) if lengths is not None else None)
         vsa_preprocess(self.plan, args, self.workspace, stream)
         return out
 
@@ -396,6 +426,31 @@ class VSA:
             out = torch.empty(self.shape, dtype=torch.bfloat16, device=self.device)
         _check_tensor(out, "out", self.shape, self.device)
         vsa_forward_preprocessed(self.plan, q, k, v, gate, out, self.workspace, stream)
+        return out
+
+    def forward_ex(self, q, k, v, gate=None, out=None, out_row_map=None, lengths=None, preprocessed=False,
+                   stream=None):
+        """The general forward (vsa_forward_ex). ``out``: the packed [B, N, H, 128]
+        output, or with ``out_row_map`` (or a non-packed ``out``) output rows as in
+        forward_rows; ``lengths``: device int64 [3] of a request inside this
+        plan's capacity; ``preprocessed``: the inputs come from ``preprocess``."""
+        for name, x in (("q", q), ("k", k), ("v", v)) + ((("gate", gate),) if gate is not None else ()):
+            _check_tensor(x, name, self.shape, self.device)
+        if out is None:
+            out = torch.empty(self.shape, dtype=torch.bfloat16, device=self.device)
+        rows = None
+        if out_row_map is not None or tuple(out.shape) != self.shape or not out.is_contiguous():
+            if out.dtype != torch.bfloat16 or out.dim() < 2 or out.shape[0] != self.batch or not out[0, 0].is_contiguous():
+                raise ValueError("out: expected bf16 [B, out_rows, ...] with contiguous rows of H x 128 channels")
+            if out_row_map is not None and (out_row_map.dtype != torch.int32 or not out_row_map.is_contiguous()
+                                            or tuple(out_row_map.shape) != (self.batch, self.seq)):
+                raise ValueError(f"out_row_map: expected contiguous int32 [{self.batch}, {self.seq}]")
+            rows = vsa_output_rows_t(_ptr(out), out.shape[1], out.stride(1), _ptr(out_row_map))
+        args = vsa_forward_args_t(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out),
+                                  ctypes.pointer(rows) if rows is not None else None,
+                                  _ptr(_check_lengths(lengths, self.device)) if lengths is not None else None,
+                                  1 if preprocessed else 0)
+        vsa_forward_ex(self.plan, args, self.workspace, stream)
         return out
 
     def forward_lengths(self, lengths, q, k, v, gate, out=None, stream=None):
@@ -493,7 +548,7 @@ class SubBlock(VSA):
 __all__ = [
     "VSA", "SubBlock", "VsaError", "vsa_plan_create_subblock", "load_library", "header_functions", "vsa_plan_create", "vsa_plan_info",
     "vsa_forward", "vsa_forward_host", "vsa_preprocess", "vsa_forward_preprocessed", "vsa_forward_rows",
-    "vsa_output_rows_t", "vsa_forward_lengths",
+    "vsa_output_rows_t", "vsa_forward_lengths", "vsa_forward_ex", "vsa_forward_args_t",
     "vsa_preprocess_args_t", "vsa_plan_host_path_bytes", "vsa_debug_views", "vsa_check",
     "vsa_plan_set_stage_events", "vsa_plan_destroy", "vsa_status_string",
     "vsa_forward_static_workspace", "vsa_diag_wait_timeout",

@@ -81,7 +81,11 @@ coarse_topk_kernel(const float* __restrict__ pooled_q, const float* __restrict__
   constexpr int MT = R >= 16 ? R / 16 : 1;  // m16 row tiles (R = 8 leaves rows 8-15 empty)
   const DynGeom dg = dyn_geom(cap, dl);
   const int T = dg.T, k = dg.k, T_cap = cap.T, k_cap = cap.k;
-  if (!dg.valid || static_cast<int>(blockIdx.x) * R >= T) return;  // uniform per CTA
+  if (!dg.valid) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *dl.invalid = 1u;  // also without a pool launch
+    return;
+  }
+  if (static_cast<int>(blockIdx.x) * R >= T) return;  // uniform per CTA
   const int tpad = (T + kChunk - 1) / kChunk * kChunk;
   const int sstride = tpad_cap + 4;         // score row stride: conflict-free A-fragment reads
   extern __shared__ __align__(16) float smem[];

@@ -79,6 +79,7 @@ struct PreprocessArgs {
   __nv_bfloat16* out[4];       // packed q, k, v, gate, bf16 [B, N, H, 128]
   float* pooled[3];            // fp32 [B, H, T, 128]; null: no pooling
   unsigned int* err;           // error words; word 7 records the first bad map entry (token + 1)
+  DeviceLengths dl;            // request lengths read on the device (null: the plan's)
 };
 cudaError_t launch_preprocess(const Geometry& g, const PreprocessArgs& a, cudaStream_t stream);
 

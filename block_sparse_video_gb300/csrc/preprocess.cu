@@ -104,7 +104,16 @@ constexpr unsigned int kDetailPreFull = 0x500;
 constexpr unsigned int kDetailPreEmpty = 0x600;
 
 __global__ void __launch_bounds__(kPreThreads, 3)
-preprocess_kernel(PreprocessArgs a, int H, int P, int Lv, int N, int T, int TP) {
+preprocess_kernel(PreprocessArgs a, Geometry cap) {
+  // the plan's geometry is the layout (buffer rows N, pooled tiles T per (b, h)); with device
+  // lengths the request's own P, Lv, T, TP place the tiles, and the tiles past them return
+  const int H = cap.H, N = cap.N, T = cap.T;
+  const DynGeom dg = dyn_geom(cap, a.dl);
+  if (!dg.valid) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.dl.invalid = 1u;
+    return;
+  }
+  const int P = dg.P, Lv = dg.Lv, TP = dg.TP;
   extern __shared__ __align__(128) uint8_t smem[];
   float* s_w = reinterpret_cast<float*>(smem + kRingBytes);          // [2][8][128]
   int* s_src = reinterpret_cast<int*>(smem + kRingBytes + kWeightBytes);
@@ -113,9 +122,10 @@ preprocess_kernel(PreprocessArgs a, int H, int P, int Lv, int N, int T, int TP) 
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
 
-  const int tiles = TP + T;
+  const int tiles = cap.TP + cap.T;  // grid tiles per batch (the capacity)
   const int b = blockIdx.x / tiles;
   const int tile = blockIdx.x % tiles;
+  if (tile >= TP + dg.T) return;      // uniform per CTA
   const bool video = tile >= TP;
   const int n0 = video ? P + (tile - TP) * kTile : tile * kTile;
   const int rows = video ? min(kTile, Lv - (tile - TP) * kTile) : min(kTile, P - n0);
@@ -360,7 +370,7 @@ cudaError_t launch_preprocess(const Geometry& g, const PreprocessArgs& a, cudaSt
                                        static_cast<int>(kPreSmem));
   if (e != cudaSuccess) return e;
   dim3 grid(g.B * (g.TP + g.T), (g.H + kHeadsPerCta - 1) / kHeadsPerCta);
-  preprocess_kernel<<<grid, kPreThreads, kPreSmem, stream>>>(a, g.H, g.P, g.Lv, g.N, g.T, g.TP);
+  preprocess_kernel<<<grid, kPreThreads, kPreSmem, stream>>>(a, g);
   return cudaGetLastError();
 }
 

@@ -290,7 +290,7 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
                           bool pool_ready, const vsa_output_rows_t* rows = nullptr,
                           const vsa_lengths_t* lengths = nullptr) {
   if (!plan || !q || !k || !v || !out || !workspace) return VSA_ERR_INVALID_ARG;
-  if (lengths && (plan->subblock || pool_ready)) return VSA_ERR_UNSUPPORTED;
+  if (lengths && plan->subblock) return VSA_ERR_UNSUPPORTED;
   if (lengths && !aligned(lengths, 8)) return VSA_ERR_INVALID_ARG;
   if (!gate && !plan->subblock) return VSA_ERR_INVALID_ARG;  // SubBlock routing has no gate
   if (workspace_bytes < plan->ws_bytes || !aligned(workspace, kAlign)) return VSA_ERR_INVALID_ARG;
@@ -417,6 +417,14 @@ vsa_status_t vsa_forward_lengths(vsa_plan_t plan, const vsa_lengths_t* lengths, 
   return forward_impl(plan, q, k, v, gate, out, workspace, workspace_bytes, stream, false, nullptr, lengths);
 }
 
+vsa_status_t vsa_forward_ex(vsa_plan_t plan, const vsa_forward_args_t* a, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (!a) return VSA_ERR_INVALID_ARG;
+  void* out = a->rows ? a->rows->out : a->out;
+  return forward_impl(plan, a->q, a->k, a->v, a->gate, out, workspace, workspace_bytes, stream, a->preprocessed != 0,
+                      a->rows, a->lengths);
+}
+
 vsa_status_t vsa_forward_rows(vsa_plan_t plan, const void* q, const void* k, const void* v, const void* gate,
                               const vsa_output_rows_t* out, int32_t preprocessed, void* workspace,
                               size_t workspace_bytes, void* stream) {
@@ -476,6 +484,13 @@ vsa_status_t vsa_preprocess(vsa_plan_t plan, const vsa_preprocess_args_t* args, 
   a.rope_interleaved = x.rope_interleaved;
   a.rope_cos = x.rope_cos;
   a.rope_sin = x.rope_sin;
+  if (x.lengths) {
+    if (plan->subblock) return VSA_ERR_UNSUPPORTED;
+    if (!aligned(x.lengths, 8)) return VSA_ERR_INVALID_ARG;
+    a.dl.len = reinterpret_cast<const long long*>(x.lengths);
+    a.dl.keep = plan->shape.keep_fraction;
+    a.dl.invalid = err + 9;
+  }
   // a SubBlock plan pools 16-token sub-blocks in its forward: no tile pooling here
   a.pooled[0] = plan->subblock ? nullptr : reinterpret_cast<float*>(ws + plan->off_pq);
   a.pooled[1] = plan->subblock ? nullptr : reinterpret_cast<float*>(ws + plan->off_pk);

@@ -130,6 +130,14 @@ vsa_status_t vsa_forward(vsa_plan_t plan, const void* q, const void* k, const vo
                          const void* gate, void* out, void* workspace, size_t workspace_bytes,
                          void* stream);
 
+/* Lengths of one request, read by the kernels at run time (device memory,
+ * 8-byte aligned): the token counts of the text, audio and video segments. */
+typedef struct {
+  int64_t len_text;
+  int64_t len_audio;
+  int64_t len_video;
+} vsa_lengths_t;
+
 /* Fused attention preprocessing ("UniServe: serving FastH3 at its fastest",
  * section "Fused attention preprocessing"; section "The Kernel Layer" gives the
  * rotary width of 96 channels and the rounding of the normalised value before
@@ -178,6 +186,11 @@ typedef struct {
   void* k_out;
   void* v_out;
   void* gate_out;
+  /* Device lengths of the request (see vsa_forward_lengths), or NULL for the
+   * plan's own. With lengths the plan's shape is the capacity: N above is the
+   * plan's row count (the src_row stride, the RoPE table rows and the output
+   * rows per batch), and only the request's tokens are written. */
+  const vsa_lengths_t* lengths;
 } vsa_preprocess_args_t;
 
 /* Enqueue the fused preprocessing on `stream`. `workspace` is this plan's
@@ -197,13 +210,6 @@ vsa_status_t vsa_forward_preprocessed(vsa_plan_t plan, const void* q, const void
                                       const void* gate, void* out, void* workspace,
                                       size_t workspace_bytes, void* stream);
 
-/* Lengths of one request, read by the kernels at run time (device memory,
- * 8-byte aligned): the token counts of the text, audio and video segments. */
-typedef struct {
-  int64_t len_text;
-  int64_t len_audio;
-  int64_t len_video;
-} vsa_lengths_t;
 
 /* The forward of a request whose lengths live in DEVICE memory, inside a
  * capacity-padded buffer ("UniServe: serving FastH3 at its fastest", section
@@ -267,6 +273,33 @@ typedef struct {
 vsa_status_t vsa_forward_rows(vsa_plan_t plan, const void* q, const void* k, const void* v, const void* gate,
                               const vsa_output_rows_t* out, int32_t preprocessed, void* workspace,
                               size_t workspace_bytes, void* stream);
+
+/* The general forward: every option of the entry points above in one call.
+ *   q, k, v, gate : as vsa_forward (gate may be NULL for a SubBlock plan)
+ *   out           : packed bf16 [batch, N, num_heads, 128] output, used when
+ *                   rows is NULL
+ *   rows          : output rows (vsa_forward_rows), or NULL
+ *   lengths       : device lengths of the request (vsa_forward_lengths), or
+ *                   NULL for the plan's own (SubBlock plans: NULL only)
+ *   preprocessed  : nonzero when q, k, v, gate and the pooled statistics come
+ *                   from vsa_preprocess on this workspace and stream
+ * With lengths, preprocessed and rows together, one captured graph runs the
+ * whole serving step: pack and normalise a request from its capacity-padded
+ * projection buffer, attend, and write the combined rows into the all-to-all
+ * send layout, for any request the capacity holds. */
+typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* gate;
+  void* out;
+  const vsa_output_rows_t* rows;
+  const vsa_lengths_t* lengths;
+  int32_t preprocessed;
+} vsa_forward_args_t;
+
+vsa_status_t vsa_forward_ex(vsa_plan_t plan, const vsa_forward_args_t* args, void* workspace,
+                            size_t workspace_bytes, void* stream);
 
 /* Same forward on HOST buffers (q, k, v, gate read, out written, all bf16
  * [batch, N, num_heads, 128]; pinned memory makes the copies asynchronous; the

@@ -142,3 +142,60 @@ def test_page_requests_in_the_10s_capacity_buffer(cuda_ok):
         assert torch.equal(_bits(out[:, :n]), _bits(ref)), (lt, la, lv)
         del q, k, v, g, ref, op
         torch.cuda.empty_cache()
+
+
+def test_serving_step_in_one_graph(cuda_ok):
+    """The serving step of one layer replayed from a single captured graph for
+    requests of different lengths (device-side lengths throughout):
+      1. vsa_preprocess packs and normalises the request from a capacity-padded
+         projection buffer through its row map;
+      2. vsa_forward_ex attends over the packed tensors;
+      3. it writes each combined row back to its sequence position, the output
+         all-to-all's send layout.
+    Each replay equals the same chain on an exact-shape plan, bit for bit."""
+    from block_sparse_video_gb300.synthetic import make_norm_weights, make_projections, make_rope_tables, make_row_map
+    b, h = 1, 4
+    cap_lt, cap_la, cap_lv = 100, 60, 64 * 12 + 5
+    cap = bsv.VSA(b, h, cap_lt, cap_la, cap_lv, KEEP)
+    n_cap = cap.seq
+    rows_in = n_cap + 64
+    proj = torch.zeros((b, rows_in, 4, h, 128), dtype=torch.bfloat16, device="cuda")
+    ins = [proj[:, :, i] for i in range(4)]
+    wq, wk = (w.cuda() for w in make_norm_weights(h, 90))
+    cos = torch.zeros((n_cap, 48), dtype=torch.float32, device="cuda")
+    sin = torch.zeros((n_cap, 48), dtype=torch.float32, device="cuda")
+    src = torch.zeros((b, n_cap), dtype=torch.int32, device="cuda")
+    packed = tuple(torch.zeros(cap.shape, dtype=torch.bfloat16, device="cuda") for _ in range(4))
+    send = torch.full((b, rows_in, h, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lengths = torch.tensor([cap_lt, cap_la, cap_lv], dtype=torch.int64, device="cuda")
+
+    def step():
+        cap.preprocess(*ins, wq, wk, cos, sin, 96, True, 1e-6, src, out=packed, lengths=lengths)
+        cap.forward_ex(*packed, out=send, out_row_map=src, lengths=lengths, preprocessed=True)
+
+    step()
+    cap.check()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for i, (lt, la, lv) in enumerate([(100, 60, 64 * 12 + 5), (37, 0, 64 * 7 + 1), (64, 50, 300)]):
+        n = lt + la + lv
+        proj.copy_(make_projections(b, rows_in, h, 91 + i, device="cuda"))
+        c, s_ = make_rope_tables(lt, la, lv, 96)
+        cos[:n].copy_(c)
+        sin[:n].copy_(s_)
+        src[:, :n].copy_(make_row_map(b, n, rows_in, 95 + i))
+        lengths.copy_(torch.tensor([lt, la, lv]))
+        send.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        cap.check()
+        # the exact-shape chain on the same data
+        ex = bsv.VSA(b, h, lt, la, lv, KEEP)
+        ex_send = torch.full_like(send, float("nan"))
+        ex_src = src[:, :n].contiguous()
+        pk = ex.preprocess(*ins, wq, wk, cos[:n].contiguous(), sin[:n].contiguous(), 96, True, 1e-6, ex_src)
+        ex.forward_rows(*pk, ex_send, ex_src, preprocessed=True)
+        ex.check()
+        assert torch.equal(_bits(send), _bits(ex_send)), (lt, la, lv)
+        assert torch.isnan(send.float()).sum() == (rows_in - n) * h * 128 * b
