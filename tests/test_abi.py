@@ -210,3 +210,26 @@ def test_forward_rows_rejects_bad_layouts_without_launching(lib):
         assert lib.vsa_forward_rows(plan, *ins, None, 0, wsp, ws, None) == bsv.VSA_ERR_INVALID_ARG
     finally:
         bsv.vsa_plan_destroy(plan)
+
+
+def test_forward_ex_and_lengths_validation(lib):
+    plan = bsv.vsa_plan_create(1, 2, 64, 64, 1024, 0.2)
+    sub = bsv.vsa_plan_create_subblock(1, 2, 64, 64, 1024, 0.75)
+    try:
+        _, _, ws = bsv.vsa_plan_info(plan)
+        g = 1 << 32
+        wsp = ctypes.c_void_p(10 * g)
+        assert lib.vsa_forward_ex(plan, None, wsp, ws, None) == bsv.VSA_ERR_INVALID_ARG
+        args = bsv.vsa_forward_args_t(g, 2 * g, 3 * g, 4 * g, 6 * g, None, 12 * g + 4, 0)  # misaligned lengths
+        assert lib.vsa_forward_ex(plan, ctypes.byref(args), wsp, ws, None) == bsv.VSA_ERR_INVALID_ARG
+        args = bsv.vsa_forward_args_t(g, 2 * g, 3 * g, 4 * g, None, None, None, 0)          # no output
+        assert lib.vsa_forward_ex(plan, ctypes.byref(args), wsp, ws, None) == bsv.VSA_ERR_INVALID_ARG
+        _, _, ws_sub = bsv.vsa_plan_info(sub)
+        args = bsv.vsa_forward_args_t(g, 2 * g, 3 * g, None, 6 * g, None, 12 * g, 0)       # SubBlock + lengths
+        assert lib.vsa_forward_ex(sub, ctypes.byref(args), wsp, ws_sub, None) == bsv.VSA_ERR_UNSUPPORTED
+        assert lib.vsa_forward_lengths(plan, None, ctypes.c_void_p(g), ctypes.c_void_p(2 * g), ctypes.c_void_p(3 * g),
+                                       ctypes.c_void_p(4 * g), ctypes.c_void_p(6 * g), wsp, ws,
+                                       None) == bsv.VSA_ERR_INVALID_ARG
+    finally:
+        bsv.vsa_plan_destroy(plan)
+        bsv.vsa_plan_destroy(sub)
