@@ -101,9 +101,9 @@ def kv_stream_bytes(cfg=None, keep=None):
     return float(blocks * 2 * 128 * 128 * 2)
 
 
-# kernels launched by one forward: tile pool, coarse attention + top-k, the
-# fine-attention fast kernel and its exact redo pass
-LAUNCHES_PER_FORWARD = 4
+# kernels launched by one forward: tile pool, the pooled V in fragment form,
+# coarse attention + top-k, the fine-attention fast kernel and its exact redo pass
+LAUNCHES_PER_FORWARD = 5
 
 
 def pool_bytes(cfg=None):

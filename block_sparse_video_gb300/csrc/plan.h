@@ -22,7 +22,7 @@ struct vsa_plan {
   int subblock;         // 0: VSA (coarse branch + top-k); 1: SubBlock routing, no coarse term
   double sparsity;      // SubBlock plans: fraction of video key tiles that may be dropped
   vsa::Geometry g;
-  size_t off_err, off_pq, off_pk, off_pv, off_coarse, off_idx, off_redo, off_fq, off_fk, ws_bytes;
+  size_t off_err, off_pq, off_pk, off_pv, off_coarse, off_idx, off_redo, off_fq, off_fk, off_vf, ws_bytes;
   int num_sms;          // SM count of `device`, read on the first forward
   size_t tensor_bytes;  // one bf16 [B, N, H, 128] tensor
   cudaEvent_t events[4];

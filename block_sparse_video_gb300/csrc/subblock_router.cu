@@ -72,21 +72,6 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 r;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
-  return r;
-}
-
 // R query blocks per CTA (R/4 m16 tiles), CH key sub-rows per chunk (CH/16
 // n-pairs). Warp w takes m16 tile w / (CH/16) and n-pair w % (CH/16) of each
 // chunk; warps past R/4 m16 tiles idle.
@@ -169,10 +154,7 @@ subblock_router_kernel(const uint4* __restrict__ frag_q, const uint4* __restrict
 #pragma unroll
         for (int ni = 0; ni < 2; ++ni) {
           const uint4 bf = lds128(kb + ni * kTile8Bytes + ks * 512);  // {hi b0, hi b1, lo b0, lo b1}
-          // A = {rows g, g+8} x {cols 2t4.., 2t4+8..}: a0 = t0.a, a1 = t1.a, a2 = t0.b, a3 = t1.b
-          mma_bf16(acc[ni], t0.z, t1.z, t0.w, t1.w, bf.x, bf.y);   // lo . hi
-          mma_bf16(acc[ni], t0.x, t1.x, t0.y, t1.y, bf.z, bf.w);   // hi . lo
-          mma_bf16(acc[ni], t0.x, t1.x, t0.y, t1.y, bf.x, bf.y);   // hi . hi
+          mma_bf16x3(acc[ni], t0, t1, bf);
         }
       }
       // acc[ni][e] (e < 2): row g, key sub-block 2 ni + e; acc[ni][2 + e]: row g + 8

@@ -1,8 +1,9 @@
 // Device helpers shared by the kernels that rank pooled tiles (the coarse
 // attention + top-k, and the SubBlock router):
-//   * fp32 products on the tensor cores with mma.sync m16n8k8 tf32, each
-//     operand split into a tf32 head and a tf32 remainder so that a*b is
-//     hi*hi + hi*lo + lo*hi, which drops only the lo*lo term (~2^-22 relative);
+//   * fp32 products on the tensor cores with mma.sync, each operand split into
+//     a head and a remainder so that a*b is hi*hi + hi*lo + lo*hi, dropping
+//     only the lo*lo term. The split is either tf32 + tf32 (m16n8k8,
+//     ~2^-22 relative) or bf16 + bf16 (m16n8k16, ~2^-16 relative);
 //   * a warp-per-row exact top-k: a radix select over the order-preserving
 //     integer image of the fp32 scores, four passes of 8-bit digits each
 //     counted in a 256-bin shared-memory histogram, then an in-order
@@ -10,6 +11,7 @@
 //     lower index; deterministic).
 #pragma once
 #include <cstdint>
+#include <cuda_bf16.h>
 
 namespace vsa {
 
@@ -61,6 +63,40 @@ __device__ __forceinline__ void load_a_split(const float* base, int stride, int 
   split_tf32(x1, hi[1], lo[1]);
   split_tf32(x2, hi[2], lo[2]);
   split_tf32(x3, hi[3], lo[3]);
+}
+
+// bf16 hi/lo split of two consecutive values (x ~ hi + lo, hi = bf16(x),
+// lo = bf16(x - hi)), packed as bf16x2 words
+__device__ __forceinline__ void split_bf16_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// c += a b from bf16 hi/lo fragments in the m16n8k16 "tile8" form: t0, t1 =
+// {hi a, hi b, lo a, lo b} of A rows g and g + 8 (a = k 2 t4, 2 t4 + 1; b = the
+// same + 8), bf = the same form of B column g. Small terms first.
+__device__ __forceinline__ void mma_bf16x3(float (&c)[4], const uint4& t0, const uint4& t1, const uint4& bf) {
+  mma_bf16(c, t0.z, t1.z, t0.w, t1.w, bf.x, bf.y);   // lo . hi
+  mma_bf16(c, t0.x, t1.x, t0.y, t1.y, bf.z, bf.w);   // hi . lo
+  mma_bf16(c, t0.x, t1.x, t0.y, t1.y, bf.x, bf.y);   // hi . hi
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
+  return r;
 }
 
 // The k largest of row[0 .. T) by one warp: their indices, ascending, into

@@ -169,6 +169,8 @@ vsa_status_t create_plan(const vsa_shape_t* shape, int device, bool subblock, do
   const size_t frag = subblock ? static_cast<size_t>(g.B) * g.H * vsa::subblock_rows_padded(g) * 512 : 0;
   p->off_fq = off;   off += align_up(frag);
   p->off_fk = off;   off += align_up(frag);
+  // VSA: the pooled V again, as bf16 hi/lo mma fragments for the coarse product
+  p->off_vf = off;   off += subblock ? 0 : align_up(vsa::coarse_vfrag_bytes(g));
   p->ws_bytes = off;
   p->tensor_bytes = static_cast<size_t>(g.B) * g.N * g.H * vsa::kHeadDim * 2;
   *out = p;
@@ -363,7 +365,8 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
         vsa::launch_pool(g, qb, kb, static_cast<const __nv_bfloat16*>(v), pq, pk, pv, dl, st) != cudaSuccess)
       return VSA_ERR_CUDA;
     if ((rs = record(plan, 1, st)) != VSA_OK) return rs;
-    if (vsa::launch_coarse_topk(g, pq, pk, pv, coarse, idx, dl, st) != cudaSuccess) return VSA_ERR_CUDA;
+    if (vsa::launch_coarse_topk(g, pq, pk, pv, coarse, idx, ws + plan->off_vf, dl, st) != cudaSuccess)
+      return VSA_ERR_CUDA;
   }
   if ((rs = record(plan, 2, st)) != VSA_OK) return rs;
   vsa::FineArgs a;

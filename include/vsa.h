@@ -120,10 +120,11 @@ vsa_status_t vsa_plan_info(vsa_plan_t plan, int64_t* n_tiles, int64_t* k, size_t
  *                   coarse output and the error words; contents on entry are
  *                   ignored (the forward clears what must start at zero)
  *   stream        : cudaStream_t to launch on (NULL = legacy default stream)
- * Enqueues four kernels (tile pool; coarse attention + top-k; fine attention
- * with the gated combination fused into its epilogue; the fine attention's exact
- * pass over the query tiles whose fast pass left its numeric range, which
- * returns at once when there are none) and returns without synchronising. It
+ * Enqueues five kernels (tile pool; the pooled V in tensor-core fragment form;
+ * coarse attention + top-k; fine attention with the gated combination fused
+ * into its epilogue; the fine attention's exact pass over the query tiles whose
+ * fast pass left its numeric range, which returns at once when there are none)
+ * and returns without synchronising. It
  * allocates nothing and reads no device data on the host. The first call on a
  * plan reads the device's SM count (cudaDeviceGetAttribute). */
 vsa_status_t vsa_forward(vsa_plan_t plan, const void* q, const void* k, const void* v,
@@ -241,7 +242,7 @@ vsa_status_t vsa_forward_preprocessed(vsa_plan_t plan, const void* q, const void
  *     the request's tiles are the first T rows of each [T_cap] block, and
  *     its selections the first k entries of each row of k_cap.
  * SubBlock plans return VSA_ERR_UNSUPPORTED. Otherwise as vsa_forward
- * (capture-safe, four kernels). */
+ * (capture-safe, five kernels). */
 vsa_status_t vsa_forward_lengths(vsa_plan_t plan, const vsa_lengths_t* lengths, const void* q, const void* k,
                                  const void* v, const void* gate, void* out, void* workspace,
                                  size_t workspace_bytes, void* stream);
