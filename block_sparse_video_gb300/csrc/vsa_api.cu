@@ -6,6 +6,8 @@
 #include <cstring>
 #include <new>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kernels.cuh"
 #include "vsa.h"
 
@@ -71,6 +73,16 @@ struct DeviceGuard {
   ~DeviceGuard() {
     if (ok && prev >= 0) cudaSetDevice(prev);
   }
+};
+
+// NVTX range around the enqueueing of one call (or one kernel launch): a
+// profiler attributes the kernels launched inside it to the range. Without a
+// profiler attached the calls do nothing.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
 vsa_status_t record(const vsa_plan* p, int i, cudaStream_t s) {
@@ -320,6 +332,7 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
 
   DeviceGuard guard(plan->device);
   if (!guard.ok) return VSA_ERR_CUDA;
+  NvtxRange range(plan->subblock ? "vsa_forward (SubBlock)" : "vsa_forward");
   const vsa::Geometry& g = plan->g;
   CUtensorMap mq, mk, mv, mg;
   // without a gate (SubBlock routing) the gate map points at q; the kernel never reads it
@@ -354,6 +367,7 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
   const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(q);
   const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(k);
   if (plan->subblock) {
+    NvtxRange r_sel("vsa_subpool + vsa_subblock_router");
     // sub-block means are always taken here: the preprocessing pools 64-token tiles
     if (vsa::launch_subpool(g, qb, kb, pq, pk, ws + plan->off_fq, ws + plan->off_fk, st) != cudaSuccess)
       return VSA_ERR_CUDA;
@@ -361,6 +375,7 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
     if (vsa::launch_subblock_router(g, ws + plan->off_fq, ws + plan->off_fk, idx, err, st) != cudaSuccess)
       return VSA_ERR_CUDA;
   } else {
+    NvtxRange r_sel("vsa_pool + vsa_coarse_topk");
     if (!pool_ready &&
         vsa::launch_pool(g, qb, kb, static_cast<const __nv_bfloat16*>(v), pq, pk, pv, dl, st) != cudaSuccess)
       return VSA_ERR_CUDA;
@@ -386,7 +401,10 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
   a.redo_count = reinterpret_cast<int*>(err + 4);
   a.redo_list = reinterpret_cast<int32_t*>(ws + plan->off_redo);
   a.work_counters = reinterpret_cast<int*>(err + 5);
-  if (vsa::launch_fine(g, mq, mk, mv, mg, a, plan->num_sms, st) != cudaSuccess) return VSA_ERR_CUDA;
+  {
+    NvtxRange r_fine("vsa_fine_attn");
+    if (vsa::launch_fine(g, mq, mk, mv, mg, a, plan->num_sms, st) != cudaSuccess) return VSA_ERR_CUDA;
+  }
   return record(plan, 3, st);
 }
 
@@ -467,6 +485,7 @@ vsa_status_t vsa_preprocess(vsa_plan_t plan, const vsa_preprocess_args_t* args, 
 
   DeviceGuard guard(plan->device);
   if (!guard.ok) return VSA_ERR_CUDA;
+  NvtxRange range("vsa_preprocess");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   unsigned int* err = reinterpret_cast<unsigned int*>(ws + plan->off_err);
@@ -543,6 +562,7 @@ vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, con
   if (device_buffer_bytes < pipe_bytes(plan) || !aligned(device_buffer, kAlign)) return VSA_ERR_INVALID_ARG;
   DeviceGuard guard(plan->device);
   if (!guard.ok) return VSA_ERR_CUDA;
+  NvtxRange range("vsa_forward_host");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* d = static_cast<uint8_t*>(device_buffer);
   const void* hin[4] = {q, k, v, gate};
