@@ -26,7 +26,7 @@
 // tile ids ascending. Results are deterministic: the histograms are counts, and
 // the compaction follows tile order.
 #include "kernels.cuh"
-#include "tf32_select.cuh"
+#include "rank_helpers.cuh"
 
 namespace vsa {
 namespace {

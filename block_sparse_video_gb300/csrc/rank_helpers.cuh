@@ -1,9 +1,8 @@
 // Device helpers shared by the kernels that rank pooled tiles (the coarse
 // attention + top-k, and the SubBlock router):
-//   * fp32 products on the tensor cores with mma.sync, each operand split into
-//     a head and a remainder so that a*b is hi*hi + hi*lo + lo*hi, dropping
-//     only the lo*lo term. The split is either tf32 + tf32 (m16n8k8,
-//     ~2^-22 relative) or bf16 + bf16 (m16n8k16, ~2^-16 relative);
+//   * fp32 products on the tensor cores with mma.sync bf16 m16n8k16, each
+//     operand split into a bf16 head and a bf16 remainder so that a*b is
+//     hi*hi + hi*lo + lo*hi, dropping only the lo*lo term (~2^-16 relative);
 //   * a warp-per-row exact top-k: a radix select over the order-preserving
 //     integer image of the fp32 scores, four passes of 8-bit digits each
 //     counted in a 256-bin shared-memory histogram, then an in-order
@@ -23,46 +22,6 @@ __device__ __forceinline__ uint32_t order_key(float s) {
   uint32_t u = __float_as_uint(s);
   if (u == 0x80000000u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// x = hi + lo with hi and lo tf32 values (hi rounded to nearest)
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
-  const float r = x - __uint_as_float(hi);
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
-}
-
-__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// c += a b for a 16x8 (A) by 8x8 (B) step, from split operands (small terms first)
-__device__ __forceinline__ void mma_split(float (&c)[4], const uint32_t (&ahi)[4], const uint32_t (&alo)[4],
-                                          uint32_t bhi0, uint32_t bhi1, uint32_t blo0, uint32_t blo1) {
-  mma_tf32(c, alo, bhi0, bhi1);
-  mma_tf32(c, ahi, blo0, blo1);
-  mma_tf32(c, ahi, bhi0, bhi1);
-}
-
-// Fragment layouts of m16n8k8 (lane = 4 g + t4): A (16 x 8, row-major) holds
-// (g, t4), (g + 8, t4), (g, t4 + 4), (g + 8, t4 + 4); B (8 x 8, k x n) holds
-// (t4, g), (t4 + 4, g); C (16 x 8) holds (g, 2 t4), (g, 2 t4 + 1), (g + 8, 2 t4),
-// (g + 8, 2 t4 + 1).
-__device__ __forceinline__ void load_a_split(const float* base, int stride, int rows_valid, int g, int t4,
-                                             uint32_t (&hi)[4], uint32_t (&lo)[4]) {
-  // base points at row 0, column t4-aligned step start; rows >= rows_valid read as zero
-  const float x0 = g < rows_valid ? base[g * stride + t4] : 0.f;
-  const float x1 = g + 8 < rows_valid ? base[(g + 8) * stride + t4] : 0.f;
-  const float x2 = g < rows_valid ? base[g * stride + t4 + 4] : 0.f;
-  const float x3 = g + 8 < rows_valid ? base[(g + 8) * stride + t4 + 4] : 0.f;
-  split_tf32(x0, hi[0], lo[0]);
-  split_tf32(x1, hi[1], lo[1]);
-  split_tf32(x2, hi[2], lo[2]);
-  split_tf32(x3, hi[3], lo[3]);
 }
 
 // bf16 hi/lo split of two consecutive values (x ~ hi + lo, hi = bf16(x),

@@ -42,7 +42,7 @@
 
 #include "kernels.cuh"
 #include "ptx.cuh"
-#include "tf32_select.cuh"
+#include "rank_helpers.cuh"
 
 namespace vsa {
 namespace {
