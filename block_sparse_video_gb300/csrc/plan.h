@@ -1,17 +1,21 @@
 // The host-side plan behind the opaque vsa_plan_t handle of include/vsa.h.
 #pragma once
 #include <cstddef>
+#include <vector>
 #include <cuda_runtime.h>
 
 #include "kernels.cuh"
 #include "vsa.h"
 
 // Head-group pipeline of the host-buffer path: group g's inputs are copied in
-// while group g - 1 computes and group g - 2's output is copied out.
+// while group g - 1 computes and group g - 2's output is copied out. Groups
+// ramp up in width (4, 6, then 8 heads) so that the first group, whose copy
+// nothing hides, is small, while the later ones keep copy rows wide.
 struct HostPipe {
-  int groups = 0;           // head groups; 1: no pipeline
-  int heads_per_group = 0;  // all groups but the last
-  vsa_plan* sub[2] = {nullptr, nullptr};  // plans for a full group and for the last group
+  static constexpr int kMaxWidth = 8;  // heads in the widest group
+  std::vector<int> widths;             // heads per group, in order; one entry: no pipeline
+  vsa_plan* sub[kMaxWidth + 1] = {};   // sub[w]: the plan of a w-head group (where used)
+  int max_width = 0;
   cudaStream_t s_in = nullptr, s_out = nullptr;  // created on first use
   cudaEvent_t entry = nullptr, in_ready[2] = {}, fwd_done[2] = {}, out_done[2] = {};
 };

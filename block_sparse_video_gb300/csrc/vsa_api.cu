@@ -193,26 +193,41 @@ void destroy_plan(vsa_plan* p);
 
 // The host-buffer path pipelines up to 8 head groups (host only: the streams
 // and events are created on the first call).
+// Head widths of the pipeline's groups. Up to 8 heads: two halves. Beyond:
+// 4, 6, then 8 heads per group, the last taking what remains. The ramp keeps
+// the first group's copy (which nothing hides) short, and the next groups'
+// copies no longer than the forward of the group before them; 8-head groups
+// copy 2 KB host rows, wide enough for the copy engines to run near the link
+// rate.
+std::vector<int> head_group_widths(int H) {
+  std::vector<int> w;
+  if (H <= 1) return {H};
+  if (H <= HostPipe::kMaxWidth) return {(H + 1) / 2, H / 2};
+  int left = H;
+  for (int step = 0; left > 0; ++step) {
+    const int want = step == 0 ? 4 : step == 1 ? 6 : HostPipe::kMaxWidth;
+    const int take = want < left ? want : left;
+    w.push_back(take);
+    left -= take;
+  }
+  return w;
+}
+
 vsa_status_t make_pipe(vsa_plan* p, bool subblock) {
-  const int H = p->g.H;
-  const int want = H < 8 ? H : 8;
-  const int hg = (H + want - 1) / want;
-  const int groups = (H + hg - 1) / hg;
   HostPipe* pipe = new (std::nothrow) HostPipe;
   if (!pipe) return VSA_ERR_INTERNAL;
-  pipe->groups = groups;
-  pipe->heads_per_group = hg;
   p->pipe = pipe;
-  if (groups == 1) return VSA_OK;
-  const int last = H - (groups - 1) * hg;
+  pipe->widths = head_group_widths(p->g.H);
+  if (pipe->widths.size() == 1) return VSA_OK;
   vsa_shape_t s = p->shape;
-  for (int i = 0; i < 2; ++i) {
-    if (i == 1 && last == hg) break;
-    s.num_heads = i == 0 ? hg : last;
+  for (int w : pipe->widths) {
+    if (w > pipe->max_width) pipe->max_width = w;
+    if (pipe->sub[w]) continue;
+    s.num_heads = w;
     vsa_plan_t sub = nullptr;
     const vsa_status_t st = create_plan(&s, p->device, subblock, p->sparsity, &sub);
     if (st != VSA_OK) return st;
-    pipe->sub[i] = sub;
+    pipe->sub[w] = sub;
   }
   return VSA_OK;
 }
@@ -220,7 +235,7 @@ vsa_status_t make_pipe(vsa_plan* p, bool subblock) {
 void destroy_plan(vsa_plan* p) {
   if (!p) return;
   if (HostPipe* pipe = p->pipe) {
-    for (vsa_plan* sub : pipe->sub) destroy_plan(sub);
+    for (vsa_plan* sub : pipe->sub) destroy_plan(sub);  // null entries are skipped
     if (pipe->s_in) {
       int prev = -1;
       cudaGetDevice(&prev);
@@ -526,12 +541,29 @@ namespace {
 // Device bytes of one head group's five tensors (q, k, v, gate, out), each 256-byte aligned.
 size_t group_slot_bytes(const vsa_plan* sub) { return 5 * align_up(sub->tensor_bytes); }
 
+size_t pipe_ws_bytes(const HostPipe* pipe) {
+  size_t ws = 0;
+  for (const vsa_plan* sub : pipe->sub)
+    if (sub && sub->ws_bytes > ws) ws = sub->ws_bytes;
+  return ws;
+}
+
 size_t pipe_bytes(const vsa_plan* p) {
   const HostPipe* pipe = p->pipe;
-  if (!pipe || pipe->groups == 1) return 5 * align_up(p->tensor_bytes) + p->ws_bytes;
-  size_t ws = pipe->sub[0]->ws_bytes;
-  if (pipe->sub[1] && pipe->sub[1]->ws_bytes > ws) ws = pipe->sub[1]->ws_bytes;
-  return 2 * group_slot_bytes(pipe->sub[0]) + ws;
+  if (!pipe || pipe->widths.size() == 1) return 5 * align_up(p->tensor_bytes) + p->ws_bytes;
+  return 2 * group_slot_bytes(pipe->sub[pipe->max_width]) + pipe_ws_bytes(pipe);
+}
+
+// Device-side address of host memory the device can read (pinned or
+// registered), else null.
+const uint8_t* device_view_of_host(const void* h) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, h) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (attr.type != cudaMemoryTypeHost || !attr.devicePointer) return nullptr;
+  return static_cast<const uint8_t*>(attr.devicePointer);
 }
 
 vsa_status_t ensure_streams(HostPipe* pipe) {
@@ -567,7 +599,7 @@ vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, con
   uint8_t* d = static_cast<uint8_t*>(device_buffer);
   const void* hin[4] = {q, k, v, gate};
   HostPipe* pipe = plan->pipe;
-  if (!pipe || pipe->groups == 1) {
+  if (!pipe || pipe->widths.size() == 1) {
     const size_t tb = plan->tensor_bytes, slot = align_up(tb);
     for (int i = 0; i < 4; ++i)
       if (hin[i] && cudaMemcpyAsync(d + i * slot, hin[i], tb, cudaMemcpyHostToDevice, st) != cudaSuccess)
@@ -582,31 +614,57 @@ vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, con
   // Head groups: group g's q/k/v/gate rows (its heads' 256-byte slices of every
   // host row) are copied in on s_in, its forward runs on the caller's stream,
   // and its output is copied out on s_out, two groups' buffers alternating.
+  // The first group's rows are gathered by a kernel reading the host memory
+  // when every input is pinned; the rest go through strided copies that hide
+  // under the previous group's forward.
   vsa_status_t rs = ensure_streams(pipe);
   if (rs != VSA_OK) return rs;
+  if (plan->num_sms == 0 &&
+      cudaDeviceGetAttribute(&plan->num_sms, cudaDevAttrMultiProcessorCount, plan->device) != cudaSuccess)
+    return VSA_ERR_CUDA;
   const vsa::Geometry& g = plan->g;
   const size_t rows = static_cast<size_t>(g.B) * g.N;
   const size_t host_pitch = static_cast<size_t>(g.H) * vsa::kHeadDim * 2;
-  const size_t slot_bytes = group_slot_bytes(pipe->sub[0]);
+  const size_t slot_bytes = group_slot_bytes(pipe->sub[pipe->max_width]);
   uint8_t* ws = d + 2 * slot_bytes;
-  size_t ws_bytes = pipe->sub[0]->ws_bytes;
-  if (pipe->sub[1] && pipe->sub[1]->ws_bytes > ws_bytes) ws_bytes = pipe->sub[1]->ws_bytes;
+  const size_t ws_bytes = pipe_ws_bytes(pipe);
+  const int n_in = gate ? 4 : 3;
+  const uint8_t* dev_in[4] = {nullptr, nullptr, nullptr, nullptr};
+  bool gather_first = true;
+  for (int i = 0; i < n_in && gather_first; ++i) {
+    dev_in[i] = device_view_of_host(hin[i]);
+    gather_first = dev_in[i] && reinterpret_cast<uintptr_t>(dev_in[i]) % 16 == 0;
+  }
   auto cuda = [](cudaError_t e) { return e == cudaSuccess; };
   if (!cuda(cudaEventRecord(pipe->entry, st)) || !cuda(cudaStreamWaitEvent(pipe->s_in, pipe->entry, 0)))
     return VSA_ERR_CUDA;
-  for (int gi = 0; gi < pipe->groups; ++gi) {
+  const int groups = static_cast<int>(pipe->widths.size());
+  int h0 = 0;
+  for (int gi = 0; gi < groups; h0 += pipe->widths[gi], ++gi) {
     const int s = gi & 1;
-    const int h0 = gi * pipe->heads_per_group;
-    vsa_plan* sub = (gi == pipe->groups - 1 && pipe->sub[1]) ? pipe->sub[1] : pipe->sub[0];
+    vsa_plan* sub = pipe->sub[pipe->widths[gi]];
     const size_t width = static_cast<size_t>(sub->g.H) * vsa::kHeadDim * 2;
     const size_t tslot = align_up(sub->tensor_bytes);
     uint8_t* base = d + s * slot_bytes;
     // inputs: slot s is free once the forward of group gi - 2 has read it
     if (gi >= 2 && !cuda(cudaStreamWaitEvent(pipe->s_in, pipe->fwd_done[s], 0))) return VSA_ERR_CUDA;
-    for (int i = 0; i < 4; ++i)
-      if (hin[i] && !cuda(cudaMemcpy2DAsync(base + i * tslot, width, static_cast<const uint8_t*>(hin[i]) + h0 * 256,
-                                            host_pitch, width, rows, cudaMemcpyHostToDevice, pipe->s_in)))
-        return VSA_ERR_CUDA;
+    if (gi == 0 && gather_first) {
+      vsa::HostGather a{};
+      for (int i = 0; i < n_in; ++i) {
+        a.src[i] = dev_in[i] + h0 * 256;
+        a.dst[i] = base + i * tslot;
+      }
+      a.src_pitch = host_pitch;
+      a.width = width;
+      a.rows = rows;
+      a.tensors = n_in;
+      if (!cuda(vsa::launch_gather_host_rows(a, plan->num_sms, pipe->s_in))) return VSA_ERR_CUDA;
+    } else {
+      for (int i = 0; i < n_in; ++i)
+        if (!cuda(cudaMemcpy2DAsync(base + i * tslot, width, static_cast<const uint8_t*>(hin[i]) + h0 * 256,
+                                    host_pitch, width, rows, cudaMemcpyHostToDevice, pipe->s_in)))
+          return VSA_ERR_CUDA;
+    }
     if (!cuda(cudaEventRecord(pipe->in_ready[s], pipe->s_in))) return VSA_ERR_CUDA;
     // forward: after its inputs, and after group gi - 2's output left slot s
     if (!cuda(cudaStreamWaitEvent(st, pipe->in_ready[s], 0))) return VSA_ERR_CUDA;
@@ -622,7 +680,7 @@ vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, con
         !cuda(cudaEventRecord(pipe->out_done[s], pipe->s_out)))
       return VSA_ERR_CUDA;
   }
-  for (int s = 0; s < 2 && s < pipe->groups; ++s)
+  for (int s = 0; s < 2 && s < groups; ++s)
     if (!cuda(cudaStreamWaitEvent(st, pipe->out_done[s], 0))) return VSA_ERR_CUDA;
   return cudaStreamSynchronize(st) == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }

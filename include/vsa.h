@@ -308,9 +308,13 @@ vsa_status_t vsa_forward_ex(vsa_plan_t plan, const vsa_forward_args_t* args, voi
  * from vsa_plan_host_path_bytes, 256-byte aligned) receives the inputs, the
  * output and the workspace.
  *
- * With two or more heads the work is pipelined over up to 8 head groups:
+ * With two or more heads the work is pipelined over head groups (up to 8
+ * heads: two halves; beyond, groups of 4, 6, then 8 heads, the last taking
+ * the rest):
  *   * each group's heads are copied in on a library-owned stream (strided
- *     copies of each host row's slice);
+ *     copies of each host row's slice). When q, k, v (and gate) are pinned or
+ *     registered host memory, the first group's slices are instead gathered by
+ *     a kernel that reads the host memory directly;
  *   * the group's forward runs on `stream`;
  *   * its output is copied out on a second library-owned stream;
  *   * two groups' device buffers alternate.

@@ -125,22 +125,32 @@ def test_deterministic(cuda_ok):
     assert torch.equal(ia, op.debug_views()["tile_index"])
 
 
-@pytest.mark.parametrize("heads,subblock", [(2, False), (11, False), (11, True), (1, False)])
-def test_host_buffer_path_matches_device_path(cuda_ok, heads, subblock):
+@pytest.mark.parametrize("heads,subblock,pinned", [(2, False, True), (11, False, True), (11, True, True),
+                                                    (1, False, True), (24, False, True), (24, False, False),
+                                                    (11, True, False)])
+def test_host_buffer_path_matches_device_path(cuda_ok, heads, subblock, pinned):
     """The host-buffer path copies head groups in, runs each group's forward and
-    copies it out, pipelined (11 heads: five groups of 2 and one of 1). Every
-    head's result must equal the device path bit for bit."""
+    copies it out, pipelined. Group widths ramp up: 11 heads run as groups of
+    4, 6 and 1; 24 heads as 4, 6, 8 and 6; 2 heads as two of one. With pinned
+    inputs the first group is gathered by a kernel reading host memory, with
+    pageable ones by strided copies. Every head's result must equal the device
+    path bit for bit."""
     lt, la, lv = 64, 37, 1000
     q, k, v, g = make_inputs(1, heads, lt, la, lv, 0, device="cuda")
     op = bsv.SubBlock(1, heads, lt, la, lv, 0.6) if subblock else bsv.VSA(1, heads, lt, la, lv, 0.2)
     dev = op(q, k, v, None if subblock else g)
     op.check()
-    hq, hk, hv, hg = [x.cpu().pin_memory() for x in (q, k, v, g)]
-    hout = torch.full_like(hq, float("nan")).pin_memory()
+    host = [x.cpu() for x in (q, k, v, g)]
+    hout = torch.full_like(host[0], float("nan"))
+    if pinned:
+        host = [x.pin_memory() for x in host]
+        hout = hout.pin_memory()
+    hq, hk, hv, hg = host
     buf = torch.empty(bsv.vsa_plan_host_path_bytes(op.plan), dtype=torch.uint8, device="cuda")
     for _ in range(2):  # the second call reuses the pipeline's streams and events
         bsv.vsa_forward_host(op.plan, hq, hk, hv, None if subblock else hg, hout, buf)
         assert torch.equal(hout.view(torch.int16), dev.cpu().view(torch.int16))
+        hout.fill_(float("nan"))
 
 
 def test_stage_events_time_each_kernel(cuda_ok):
