@@ -86,8 +86,8 @@ cudaError_t launch_preprocess(const Geometry& g, const PreprocessArgs& a, cudaSt
 // Coarse attention over pooled tiles fused with the top-k tile selection.
 // coarse fp32 [B, H, T, 128]; tile_index int32 [B, H, T, k] ascending.
 size_t coarse_smem_bytes(const Geometry& g, int* rows_per_cta);
-// vfrag: workspace of coarse_vfrag_bytes(g) for the pooled V in mma fragment
-// form (written by a first, small kernel of the launch).
+// vfrag: workspace of coarse_vfrag_bytes(g) for the pooled K and V in mma
+// fragment form (written by a first, small kernel of the launch).
 size_t coarse_vfrag_bytes(const Geometry& g);
 cudaError_t launch_coarse_topk(const Geometry& g, const float* pooled_q, const float* pooled_k,
                                const float* pooled_v, float* coarse, int32_t* tile_index, void* vfrag,

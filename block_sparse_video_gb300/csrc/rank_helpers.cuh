@@ -7,7 +7,12 @@
 //     integer image of the fp32 scores, four passes of 8-bit digits each
 //     counted in a 256-bin shared-memory histogram, then an in-order
 //     compaction that writes the selected indices ascending (ties to the
-//     lower index; deterministic).
+//     lower index; deterministic);
+//   * a faster warp top-k for rows without ties at the cut: a search for a
+//     threshold with exactly k scores at or above it, counting with compares
+//     and warp reductions only (no shared-memory atomics); rows where no such
+//     threshold exists (equal scores at the cut) or that hold a non-finite
+//     score fall back to the radix select, so the result is the same set.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -124,6 +129,88 @@ __device__ __forceinline__ void warp_select_topk(const float* row, int T, int k,
     if (sel) dst[written + __popc(selb & lt_mask)] = j;
     written += __popc(selb);
     eq_seen += __popc(eqb);
+  }
+}
+
+// The k largest of row[0 .. T), as warp_select_topk, for rows whose entries
+// T .. tpad - 1 hold -inf (tpad a multiple of 64, row 16-byte aligned). The
+// count c(x) = #{j : row[j] >= x} falls as x rises; the search keeps lo with
+// c(lo) > k and hi with c(hi) < k and tries the point where the straight line
+// between (lo, c(lo)) and (hi, c(hi)) reaches k (every third try: the
+// midpoint, so the bracket shrinks geometrically in any case). A try with
+// c(x) == k separates the k-th largest score from the (k+1)-th: the k scores
+// >= x are the selection, the same set the radix select returns. Brackets that
+// can no longer be split (equal scores at the cut), non-finite scores and the
+// iteration limit hand the row to warp_select_topk.
+__device__ __forceinline__ void warp_select_topk_count(const float* row, int T, int tpad, int k, int* h,
+                                                       int32_t* dst, int lane) {
+  const unsigned full = 0xffffffffu;
+  if (k >= T) {
+    for (int j = lane; j < T; j += 32) dst[j] = j;
+    return;
+  }
+  float vmin = INFINITY, vmax = -INFINITY;
+  bool bad = false;
+  for (int j = lane; j < T; j += 32) {
+    const float x = row[j];
+    vmin = fminf(vmin, x);
+    vmax = fmaxf(vmax, x);
+    bad |= !(fabsf(x) <= 3.0e38f);  // NaN or +-inf (or close to overflow)
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    vmin = fminf(vmin, __shfl_xor_sync(full, vmin, o));
+    vmax = fmaxf(vmax, __shfl_xor_sync(full, vmax, o));
+  }
+  float theta = 0.f;
+  bool found = false;
+  if (!__any_sync(full, bad) && k >= 1) {
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    const int n4 = tpad / 4;
+    auto count_ge = [&](float x) {
+      int c = 0;
+      for (int i = lane; i < n4; i += 32) {
+        const float4 v = r4[i];
+        c += (v.x >= x) + (v.y >= x) + (v.z >= x) + (v.w >= x);
+      }
+      return static_cast<int>(__reduce_add_sync(full, static_cast<unsigned>(c)));
+    };
+    float lo = vmin, hi = nextafterf(vmax, INFINITY);
+    int clo = T, chi = 0;
+#pragma unroll 1
+    for (int it = 0; it < 48; ++it) {
+      const float mid = 0.5f * (lo + hi);
+      float x = mid;
+      if (it % 3 != 2) x = lo + (hi - lo) * (static_cast<float>(clo - k) / static_cast<float>(clo - chi));
+      if (!(x > lo && x < hi)) x = mid;
+      if (!(x > lo && x < hi)) break;  // lo and hi adjacent: equal scores at the cut
+      const int c = count_ge(x);
+      if (c == k) {
+        theta = x;
+        found = true;
+        break;
+      }
+      if (c > k) {
+        lo = x;
+        clo = c;
+      } else {
+        hi = x;
+        chi = c;
+      }
+    }
+  }
+  if (!found) {
+    warp_select_topk(row, T, k, h, dst, lane);
+    return;
+  }
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int written = 0;
+  for (int base = 0; base < T; base += 32) {
+    const int j = base + lane;
+    const bool sel = j < T && row[j] >= theta;
+    const unsigned selb = __ballot_sync(full, sel);
+    if (sel) dst[written + __popc(selb & lt_mask)] = j;
+    written += __popc(selb);
   }
 }
 
