@@ -133,7 +133,7 @@ __device__ __forceinline__ void warp_select_topk(const float* row, int T, int k,
 }
 
 // The k largest of row[0 .. T), as warp_select_topk, for rows whose entries
-// T .. tpad - 1 hold -inf (tpad a multiple of 64, row 16-byte aligned). The
+// T .. tpad - 1 hold -inf (tpad >= T a multiple of 4, row 16-byte aligned). The
 // count c(x) = #{j : row[j] >= x} falls as x rises; the search keeps lo with
 // c(lo) > k and hi with c(hi) < k and tries the point where the straight line
 // between (lo, c(lo)) and (hi, c(hi)) reaches k (every third try: the

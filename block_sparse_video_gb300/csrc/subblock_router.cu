@@ -198,10 +198,12 @@ subblock_router_kernel(const uint4* __restrict__ frag_q, const uint4* __restrict
     return;
   }
 
+  // Key blocks T .. spad / 4 - 1 hold only empty sub-blocks and scored -inf
+  // above, as the counting select requires of a row's padding.
   for (int r = warp; r < R; r += kWarps)
     if (q0 + r < T)
-      warp_select_topk(S + r * bstride, T, k, hist + warp * kBins,
-                       tile_index + (bh * T + q0 + r) * static_cast<size_t>(k), lane);
+      warp_select_topk_count(S + r * bstride, T, spad / 4, k, hist + warp * kBins,
+                             tile_index + (bh * T + q0 + r) * static_cast<size_t>(k), lane);
 }
 
 int sub_pad(int T) { return (4 * T + 127) / 128 * 128; }  // as subblock_rows_padded
