@@ -106,7 +106,6 @@ constexpr int kBarItemFull = kBarOEmpty + kNumO;
 constexpr int kBarItemEmpty = kBarItemFull + kItemSlots;
 constexpr int kNumBars = kBarItemEmpty + kItemSlots;
 static_assert(kNumBars * 8 <= 512, "barrier area");
-static_assert(kNumK == kNumS, "K slot g % kNumK is released through S-full barrier g % kNumS");
 static_assert(kColO + kNumO * 64 <= kTmemCols, "TMEM columns");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
@@ -303,7 +302,6 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     const int box_tile = (lane >> 1) & 1, box_half = lane & 1;  // this lane's box within a block
     const uint32_t box_off = box_half * 16384 + box_tile * 8192;
     int slot = 0;        // ring slot of the next block (counting over all items)
-    uint32_t phase = 0;  // parity of that slot's use
     uint32_t g = 0;      // blocks loaded so far, over all items
     for (int n = 0; ok; ++n) {
       int item;
@@ -363,20 +361,18 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         // lane 0 arms the full barrier. A box may land before the arming: the
         // transaction count may run negative until the arrive, and the phase
         // cannot complete before it.
-        // The slot's previous block must have been read: K slot (block g - 3) via
-        // S-full of that block (same slot index, parity phase ^ 1: a fresh
-        // barrier passes the first kNumK blocks), V slot (block g - 2) via
-        // P-empty of that block.
-        int rel_bar = kBarSFull + slot;
-        uint32_t rel_par = phase ^ 1u;
-        if (v_warp) {
-          const uint32_t gp = g - kNumV;  // wraps for the first kNumV blocks, which wait for nothing
-          rel_bar = kBarPEmpty + gp % kNumP;
-          rel_par = (gp / kNumP) & 1u;
-        }
+        // The slot's previous block, gp = g - nstage, must have been read: a K
+        // slot via S-full of that block, a V slot via its P-empty (the first
+        // nstage blocks wait for nothing). The parity wait cannot alias: the
+        // next completion of that barrier needs a block this warp has not
+        // loaded yet, and the one before it was waited for when block gp was
+        // loaded.
+        const uint32_t gp = g - static_cast<uint32_t>(nstage);  // wraps for the first nstage blocks
+        const int rel_bar = v_warp ? kBarPEmpty + gp % kNumP : kBarSFull + gp % kNumS;
+        const uint32_t rel_par = v_warp ? (gp / kNumP) & 1u : (gp / kNumS) & 1u;
         bool lane_ok = true;
         if (lane < 4) {
-          if (!v_warp || g >= static_cast<uint32_t>(kNumV))
+          if (g >= static_cast<uint32_t>(nstage))
             lane_ok = mbar_wait(bar(rel_bar), rel_par, err, v_warp ? 0x200u : 0x100u);
           if (lane_ok) {
             if (lane == 0) mbar_arrive_expect_tx(bar(bar_full + slot), kKVBytes);
@@ -385,7 +381,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
           }
         }
         if (!__all_sync(0xffffffffu, lane_ok)) { ok = false; break; }
-        if (++slot == nstage) { slot = 0; phase ^= 1u; }
+        if (++slot == nstage) slot = 0;
         ++g;
       }
     }
