@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -101,14 +102,26 @@ def kv_stream_bytes(cfg=None, keep=None):
     return float(blocks * 2 * 128 * 128 * 2)
 
 
-# kernels launched by one forward: tile pool, the pooled V in fragment form,
-# coarse attention + top-k, the fine-attention fast kernel and its exact redo pass
+# kernels launched by one forward: tile pool, the pooled K and V in fragment
+# form, coarse attention + top-k, the fine-attention fast kernel and its exact
+# redo pass
 LAUNCHES_PER_FORWARD = 5
 
 
 def pool_bytes(cfg=None):
     cfg = CFG if cfg is None else cfg
     return 3 * cfg.batch * cfg.len_video * cfg.heads * 128 * 2 + 3 * cfg.batch * cfg.heads * cfg.n_video_tiles * 128 * 4
+
+
+def coarse_bytes(cfg=None, keep=None):
+    """Algorithmic HBM bytes of the coarse + top-k step: the pooled Q, K, V read
+    once (fp32), the selected tile ids (int32) and the coarse output (fp32)
+    written once."""
+    cfg = CFG if cfg is None else cfg
+    keep = cfg.keep[0] if keep is None else keep
+    bh, t = cfg.batch * cfg.heads, cfg.n_video_tiles
+    k = max(1, min(t, int(math.floor(keep * t + 0.5))))
+    return 3 * bh * t * 128 * 4 + bh * t * k * 4 + bh * t * 128 * 4
 
 
 # fused preprocessing workload: the projections of a 10 s request arrive in a
@@ -580,7 +593,14 @@ def run_ours(args):
                 "pool_kernel": {"ms": pool_ms, "bytes": pool_bytes(cfg), "GB_s": pool_gbs,
                                 "frac_of_hbm": pool_gbs / peaks["hbm_gbs"]},
                 "coarse_topk_kernel": {"ms": coarse_ms, "flops": fl["coarse"],
-                                       "TFLOP_s": fl["coarse"] / (coarse_ms * 1e-3) / 1e12},
+                                       "TFLOP_s": fl["coarse"] / (coarse_ms * 1e-3) / 1e12,
+                                       "bytes": coarse_bytes(cfg, keep),
+                                       "frac_of_hbm": coarse_bytes(cfg, keep) / (coarse_ms * 1e-3) / 1e9
+                                       / peaks["hbm_gbs"]},
+                "pool_plus_coarse": {"ms": pool_ms + coarse_ms,
+                                     "bytes": pool_bytes(cfg) + coarse_bytes(cfg, keep),
+                                     "frac_of_hbm": (pool_bytes(cfg) + coarse_bytes(cfg, keep))
+                                     / ((pool_ms + coarse_ms) * 1e-3) / 1e9 / peaks["hbm_gbs"]},
                 "fine_attn_kernel": {"ms": fine_ms, "flops": fl["fine"], "TFLOP_s": fine_tflops,
                                      "kv_l2_to_smem_bytes": kv_stream_bytes(cfg, keep),
                                      "kv_l2_to_smem_TB_s": kv_stream_bytes(cfg, keep) / (fine_ms * 1e-3) / 1e12},
