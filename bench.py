@@ -297,6 +297,43 @@ def measure_capacity(heads, dev, stream, flush, steps, warmup, world, seed):
             "api": "vsa_forward_lengths captured once in a CUDA graph, lengths read on the device"}
 
 
+def measure_send_layout(op, q, k, v, g, cfg, dev, stream, flush, steps, warmup, world, seed):
+    """The forward writing each combined row through a row map into a
+    78,080-row sequence-sharded send buffer (the output all-to-all's layout),
+    against the plain forward on the same inputs; both timed with device
+    events, L2 flushed before each step. Rows must match bit for bit."""
+    from block_sparse_video_gb300.synthetic import make_row_map
+    rows = max(PRE_ROWS_IN, cfg.seq)
+    row_map = make_row_map(cfg.batch, cfg.seq, rows, seed).to(dev)
+    send = torch.empty((cfg.batch, rows, cfg.heads, 128), dtype=torch.bfloat16, device=dev)
+    plain = torch.empty(op.shape, dtype=torch.bfloat16, device=dev)
+    for _ in range(warmup):
+        op.forward_rows(q, k, v, g, send, row_map)
+        op(q, k, v, g, plain)
+    op.check()
+
+    def timed(fn):
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()
+            e0[i].record(stream)
+            fn()
+            e1[i].record(stream)
+        torch.cuda.synchronize(dev)
+        return reduce_max(statistics.mean(a.elapsed_time(b) for a, b in zip(e0, e1)), world, dev)
+
+    rows_ms = timed(lambda: op.forward_rows(q, k, v, g, send, row_map))
+    plain_ms = timed(lambda: op(q, k, v, g, plain))
+    op.check()
+    same = all(bool(torch.equal(send[b, row_map[b].long()].view(torch.int16), plain[b].view(torch.int16)))
+               for b in range(cfg.batch))
+    del send, plain, row_map
+    return {"send_rows": rows, "forward_rows_ms": rows_ms, "plain_forward_ms": plain_ms,
+            "bitwise_equal_to_plain": same,
+            "api": "vsa_forward_rows: combined rows written through a random row map into the send buffer"}
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -540,6 +577,12 @@ def run_ours(args):
     if not args.no_preprocess:
         pre = measure_preprocess(op, cfg, dev, stream, flush, steps, args.warmup, peaks, world)
 
+    # ---- the combination written into the output all-to-all's send layout (measured on its own)
+    send_layout = None
+    if not args.no_send_layout:
+        send_layout = measure_send_layout(op, q, k, v, g, cfg, dev, stream, flush, steps, args.warmup, world,
+                                          cfg.seed + 300)
+
     # ---- end to end through the host-buffer entry point
     e2e = None
     if args.e2e_steps > 0:
@@ -608,6 +651,7 @@ def run_ours(args):
             },
             "subblock": subblock,
             "capacity_graph": capacity,
+            "send_layout": send_layout,
             "clocks": clocks,
             "e2e": e2e,
             "gpu_launches": LAUNCHES_PER_FORWARD * steps,
@@ -636,6 +680,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-send-layout", action="store_true",
+                    help="skip the send-layout forward (vsa_forward_rows) measured beside the step")
     ap.add_argument("--no-capacity", action="store_true",
                     help="skip the separate capacity-bucket graph-replay measurement")
     ap.add_argument("--no-subblock", action="store_true",

@@ -153,6 +153,33 @@ def test_host_buffer_path_matches_device_path(cuda_ok, heads, subblock, pinned):
         hout.fill_(float("nan"))
 
 
+def test_exact_ties_at_the_cut_take_the_lower_tiles(cuda_ok):
+    """Scores tie exactly at the cut: every video query is the all-ones vector
+    and every key tile is constant, so s[t][j] = c_j * sqrt(128) for all t,
+    bit-equal for equal c_j on both sides. Five tiles score highest and four
+    tie for the sixth place (k = 6 of 30 tiles): no threshold separates k
+    scores, the selection takes the lowest-index tied tile (the oracle's rule),
+    and the output matches the oracle."""
+    lt, la, lv, keep = 20, 12, 64 * 30, 0.2
+    q, k, v, g = make_inputs(1, 2, lt, la, lv, 40, device="cuda")
+    t_count = lv // 64
+    c = [-(j + 1) / 64.0 for j in range(t_count)]     # distinct, all below the groups
+    for j in (20, 21, 22, 23, 24):
+        c[j] = 1.0                                       # the top five
+    for j in (2, 9, 14, 27):
+        c[j] = 0.5                                       # tied for the sixth place
+    p = lt + la
+    q[:, p:] = 1.0
+    for j in range(t_count):
+        k[:, p + 64 * j: p + 64 * (j + 1)] = c[j]
+    assert vo.keep_count(t_count, keep) == 6
+    _, _, views = run_gpu(q, k, v, g, lt, la, lv, keep)
+    expect = np.array([2, 20, 21, 22, 23, 24])
+    idx = views["tile_index"].numpy()
+    assert (idx == expect).all(), idx[0, 0, :3]
+    check_inputs(q, k, v, g, lt, la, lv, keep, "exact ties at the cut")
+
+
 def test_stage_events_time_each_kernel(cuda_ok):
     q, k, v, g = make_inputs(1, 2, 64, 64, 1024, 0, device="cuda")
     op = bsv.VSA(1, 2, 64, 64, 1024, 0.2)
