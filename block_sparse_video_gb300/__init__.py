@@ -457,8 +457,9 @@ class VSA:
         """Forward of a request whose lengths (device int64 [3]: text, audio,
         video) are read by the kernels: this object's lengths are the capacity,
         and the tensors are [B, N_cap, H, 128] with the request in rows 0 .. N - 1.
-        Capture it once in a CUDA graph and replay it for any request that fits."""
-        for name, x in (("q", q), ("k", k), ("v", v), ("gate", gate)):
+        Capture it once in a CUDA graph and replay it for any request that fits.
+        ``gate`` may be None for SubBlock routing."""
+        for name, x in (("q", q), ("k", k), ("v", v)) + ((("gate", gate),) if gate is not None else ()):
             _check_tensor(x, name, self.shape, self.device)
         if (lengths.dtype != torch.int64 or lengths.numel() != 3 or not lengths.is_contiguous()
                 or lengths.device != self.device):

@@ -29,6 +29,7 @@ struct Geometry {
 struct DeviceLengths {
   const long long* len = nullptr;  // null: the plan's own lengths
   double keep = 0.0;               // keep fraction (the actual k is derived from the actual T)
+  double sparsity = -1.0;          // >= 0: SubBlock routing's sparsity (its own rule for k)
   unsigned int* invalid = nullptr; // set to 1 when the lengths are outside the capacity
 };
 
@@ -50,9 +51,17 @@ __device__ __forceinline__ DynGeom dyn_geom(const Geometry& cap, const DeviceLen
   d.Lv = static_cast<int>(video);
   d.T = (d.Lv + kTile - 1) / kTile;
   d.TP = (d.P + kTile - 1) / kTile;
-  // "rounded to a whole number of tiles": round half up in IEEE double, clamped to [1, T]
-  int k = static_cast<int>(floor(dl.keep * static_cast<double>(d.T) + 0.5));
-  d.k = k < 1 ? 1 : (k > d.T ? d.T : k);
+  int k;
+  if (dl.sparsity >= 0.0) {
+    // SubBlock: at most floor(s T) tiles dropped (IEEE double), the kept count
+    // rounded up to a multiple of 8
+    const int need = d.T - static_cast<int>(floor(dl.sparsity * static_cast<double>(d.T)));
+    k = (need + 7) / 8 * 8;
+  } else {
+    // "rounded to a whole number of tiles": round half up in IEEE double
+    k = static_cast<int>(floor(dl.keep * static_cast<double>(d.T) + 0.5));
+  }
+  d.k = k < 1 ? 1 : (k > d.T ? d.T : k);  // clamped to [1, T]
   return d;
 }
 
@@ -99,11 +108,14 @@ cudaError_t launch_coarse_topk(const Geometry& g, const float* pooled_q, const f
 // (b, h)), then the k video key tiles of highest estimated softmax mass per
 // video query tile (tile_index int32 [B, H, T, k], ascending).
 int subblock_rows_padded(const Geometry& g);
+// With device lengths (dl.len, dl.sparsity set) g is the capacity: both
+// kernels keep its layout and work on the request's tiles.
 cudaError_t launch_subpool(const Geometry& g, const __nv_bfloat16* q, const __nv_bfloat16* k, float* sub_q,
-                           float* sub_k, void* frag_q, void* frag_k, cudaStream_t stream);
+                           float* sub_k, void* frag_q, void* frag_k, const DeviceLengths& dl, cudaStream_t stream);
 size_t subblock_router_smem_bytes(const Geometry& g, int* rows_per_cta);
 cudaError_t launch_subblock_router(const Geometry& g, const void* frag_q, const void* frag_k,
-                                   int32_t* tile_index, unsigned int* err, cudaStream_t stream);
+                                   int32_t* tile_index, unsigned int* err, const DeviceLengths& dl,
+                                   cudaStream_t stream);
 
 // Fine attention: prefix query tiles over every key, video query tiles over
 // the prefix plus their selected video tiles; epilogue adds sigmoid(gate) *

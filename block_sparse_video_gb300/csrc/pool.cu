@@ -115,8 +115,12 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
 __global__ void __launch_bounds__(kPoolThreads)
 subpool_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                float* __restrict__ pq, float* __restrict__ pk, uint4* __restrict__ fq, uint4* __restrict__ fk,
-               int H, int P, int Lv, int N, int T, int spad) {
+               Geometry cap, DeviceLengths dl, int spad) {
   constexpr int kLen = kTile / 4;
+  // the request's prefix and video length (the capacity's layout: H, N, T, spad)
+  const DynGeom dg = dyn_geom(cap, dl);
+  if (!dg.valid) return;  // reported by the router
+  const int H = cap.H, P = dg.P, Lv = dg.Lv, N = cap.N, T = cap.T;
   const int vec = blockIdx.y * kPoolThreads + threadIdx.x;  // 16-byte vector within a row
   const int row_vecs = H * (kHeadDim / 8);
   const int b = blockIdx.x / spad, run = blockIdx.x % spad;
@@ -194,12 +198,12 @@ cudaError_t launch_pool(const Geometry& g, const __nv_bfloat16* q, const __nv_bf
 int subblock_rows_padded(const Geometry& g) { return (4 * g.T + 127) / 128 * 128; }
 
 cudaError_t launch_subpool(const Geometry& g, const __nv_bfloat16* q, const __nv_bfloat16* k, float* sub_q,
-                           float* sub_k, void* frag_q, void* frag_k, cudaStream_t stream) {
+                           float* sub_k, void* frag_q, void* frag_k, const DeviceLengths& dl, cudaStream_t stream) {
   const int row_vecs = g.H * (kHeadDim / 8);
   const int spad = subblock_rows_padded(g);
   dim3 grid(g.B * spad, (row_vecs + kPoolThreads - 1) / kPoolThreads, 2);
   subpool_kernel<<<grid, kPoolThreads, 0, stream>>>(q, k, sub_q, sub_k, static_cast<uint4*>(frag_q),
-                                                    static_cast<uint4*>(frag_k), g.H, g.P, g.Lv, g.N, g.T, spad);
+                                                    static_cast<uint4*>(frag_k), g, dl, spad);
   return cudaGetLastError();
 }
 

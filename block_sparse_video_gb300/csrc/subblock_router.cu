@@ -78,10 +78,21 @@ __device__ __forceinline__ float lg2(float x) {
 template <int R, int CH>
 __global__ void __launch_bounds__(kThreads, 1)
 subblock_router_kernel(const uint4* __restrict__ frag_q, const uint4* __restrict__ frag_k,
-                       int32_t* __restrict__ tile_index, unsigned int* err, int T, int Lv, int k, int spad) {
+                       int32_t* __restrict__ tile_index, unsigned int* err, Geometry cap, DeviceLengths dl,
+                       int spad) {
   constexpr int MT = R / 4;
   constexpr int NP = CH / 16;
   constexpr int kChunkBytes = CH / 8 * kTile8Bytes;
+  // The request's tiles (the plan's own, or the device lengths'); the layouts
+  // (fragment rows spad, selections [T_cap][k_cap], shared-memory rows) are
+  // the plan's.
+  const DynGeom dg = dyn_geom(cap, dl);
+  if (!dg.valid) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *dl.invalid = 1u;
+    return;
+  }
+  const int T = dg.T, Lv = dg.Lv, k = dg.k;
+  if (static_cast<int>(blockIdx.x) * R >= T) return;  // uniform per CTA, before any copy
   const int bstride = spad / 4 + 4;                 // block-score row stride (floats)
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* s_kbuf = smem;                           // [2][kChunkBytes] key fragments
@@ -98,7 +109,7 @@ subblock_router_kernel(const uint4* __restrict__ frag_q, const uint4* __restrict
   const uint8_t* gq = reinterpret_cast<const uint8_t*>(frag_q + bh * tiles_per_bh * 256);
   const uint8_t* gk = reinterpret_cast<const uint8_t*>(frag_k + bh * tiles_per_bh * 256);
   const float scale_log2 = 0.08838834764831845f * 1.4426950408889634f;  // log2(e) / sqrt(128)
-  const int n_chunks = spad / CH;
+  const int n_chunks = (4 * T + CH - 1) / CH;       // chunks holding the request's key sub-rows
   const uint32_t bar_q = smem_u32(bars), bar_k0 = smem_u32(bars + 1);
 
   if (tid == 0) {
@@ -198,12 +209,12 @@ subblock_router_kernel(const uint4* __restrict__ frag_q, const uint4* __restrict
     return;
   }
 
-  // Key blocks T .. spad / 4 - 1 hold only empty sub-blocks and scored -inf
-  // above, as the counting select requires of a row's padding.
+  // Key blocks T .. n_chunks * CH / 4 - 1 hold only empty sub-blocks and
+  // scored -inf above, as the counting select requires of a row's padding.
   for (int r = warp; r < R; r += kWarps)
     if (q0 + r < T)
-      warp_select_topk_count(S + r * bstride, T, spad / 4, k, hist + warp * kBins,
-                             tile_index + (bh * T + q0 + r) * static_cast<size_t>(k), lane);
+      warp_select_topk_count(S + r * bstride, T, n_chunks * CH / 4, k, hist + warp * kBins,
+                             tile_index + (bh * cap.T + q0 + r) * static_cast<size_t>(cap.k), lane);
 }
 
 int sub_pad(int T) { return (4 * T + 127) / 128 * 128; }  // as subblock_rows_padded
@@ -224,14 +235,14 @@ int pick_rows(int spad) {
 
 template <int R, int CH>
 cudaError_t launch_rows(const Geometry& g, const void* frag_q, const void* frag_k, int32_t* tile_index,
-                        unsigned int* err, size_t smem, cudaStream_t stream) {
+                        unsigned int* err, const DeviceLengths& dl, size_t smem, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(subblock_router_kernel<R, CH>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid((g.T + R - 1) / R, g.B * g.H);
   subblock_router_kernel<R, CH><<<grid, kThreads, smem, stream>>>(static_cast<const uint4*>(frag_q),
                                                                   static_cast<const uint4*>(frag_k), tile_index,
-                                                                  err, g.T, g.Lv, g.k, sub_pad(g.T));
+                                                                  err, g, dl, sub_pad(g.T));
   return cudaGetLastError();
 }
 
@@ -244,13 +255,14 @@ size_t subblock_router_smem_bytes(const Geometry& g, int* rows_per_cta) {
 }
 
 cudaError_t launch_subblock_router(const Geometry& g, const void* frag_q, const void* frag_k,
-                                   int32_t* tile_index, unsigned int* err, cudaStream_t stream) {
+                                   int32_t* tile_index, unsigned int* err, const DeviceLengths& dl,
+                                   cudaStream_t stream) {
   int r = 0;
   const size_t smem = subblock_router_smem_bytes(g, &r);
   switch (r) {
-    case 16: return launch_rows<16, 64>(g, frag_q, frag_k, tile_index, err, smem, stream);
-    case 8: return launch_rows<8, 128>(g, frag_q, frag_k, tile_index, err, smem, stream);
-    case 4: return launch_rows<4, 128>(g, frag_q, frag_k, tile_index, err, smem, stream);
+    case 16: return launch_rows<16, 64>(g, frag_q, frag_k, tile_index, err, dl, smem, stream);
+    case 8: return launch_rows<8, 128>(g, frag_q, frag_k, tile_index, err, dl, smem, stream);
+    case 4: return launch_rows<4, 128>(g, frag_q, frag_k, tile_index, err, dl, smem, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -319,7 +319,6 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
                           bool pool_ready, const vsa_output_rows_t* rows = nullptr,
                           const vsa_lengths_t* lengths = nullptr) {
   if (!plan || !q || !k || !v || !out || !workspace) return VSA_ERR_INVALID_ARG;
-  if (lengths && plan->subblock) return VSA_ERR_UNSUPPORTED;
   if (lengths && !aligned(lengths, 8)) return VSA_ERR_INVALID_ARG;
   if (!gate && !plan->subblock) return VSA_ERR_INVALID_ARG;  // SubBlock routing has no gate
   if (workspace_bytes < plan->ws_bytes || !aligned(workspace, kAlign)) return VSA_ERR_INVALID_ARG;
@@ -375,6 +374,7 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
   if (lengths) {
     dl.len = reinterpret_cast<const long long*>(lengths);
     dl.keep = plan->shape.keep_fraction;
+    dl.sparsity = plan->subblock ? plan->sparsity : -1.0;
     dl.invalid = err + 9;
   }
   vsa_status_t rs = record(plan, 0, st);
@@ -384,10 +384,10 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
   if (plan->subblock) {
     NvtxRange r_sel("vsa_subpool + vsa_subblock_router");
     // sub-block means are always taken here: the preprocessing pools 64-token tiles
-    if (vsa::launch_subpool(g, qb, kb, pq, pk, ws + plan->off_fq, ws + plan->off_fk, st) != cudaSuccess)
+    if (vsa::launch_subpool(g, qb, kb, pq, pk, ws + plan->off_fq, ws + plan->off_fk, dl, st) != cudaSuccess)
       return VSA_ERR_CUDA;
     if ((rs = record(plan, 1, st)) != VSA_OK) return rs;
-    if (vsa::launch_subblock_router(g, ws + plan->off_fq, ws + plan->off_fk, idx, err, st) != cudaSuccess)
+    if (vsa::launch_subblock_router(g, ws + plan->off_fq, ws + plan->off_fk, idx, err, dl, st) != cudaSuccess)
       return VSA_ERR_CUDA;
   } else {
     NvtxRange r_sel("vsa_pool + vsa_coarse_topk");
@@ -522,10 +522,10 @@ vsa_status_t vsa_preprocess(vsa_plan_t plan, const vsa_preprocess_args_t* args, 
   a.rope_cos = x.rope_cos;
   a.rope_sin = x.rope_sin;
   if (x.lengths) {
-    if (plan->subblock) return VSA_ERR_UNSUPPORTED;
     if (!aligned(x.lengths, 8)) return VSA_ERR_INVALID_ARG;
     a.dl.len = reinterpret_cast<const long long*>(x.lengths);
     a.dl.keep = plan->shape.keep_fraction;
+    a.dl.sparsity = plan->subblock ? plan->sparsity : -1.0;
     a.dl.invalid = err + 9;
   }
   // a SubBlock plan pools 16-token sub-blocks in its forward: no tile pooling here

@@ -231,7 +231,9 @@ vsa_status_t vsa_forward_preprocessed(vsa_plan_t plan, const void* q, const void
  *     len_text + len_audio, and 1 <= len_video <= the plan's len_video.
  *     Otherwise nothing is computed, out is untouched and vsa_check reports
  *     VSA_ERR_INVALID_ARG;
- *   - k = max(1, min(T, floor(keep_fraction * T + 0.5))) for the request's T;
+ *   - k follows the plan's rule for the request's T: max(1, min(T,
+ *     floor(keep_fraction * T + 0.5))); for a SubBlock plan, the kept count
+ *     T - floor(sparsity * T) rounded up to a multiple of 8, capped at T;
  *   - rows N .. N + 63 of q, k and v (capacity padding, when it exists) must
  *     hold finite values. A ragged last tile's loads read them, and they are
  *     masked by exact zeros, so NaN or Inf there would propagate. The
@@ -241,8 +243,9 @@ vsa_status_t vsa_forward_preprocessed(vsa_plan_t plan, const void* q, const void
  *   - the workspace and its views (vsa_debug_views) keep the plan's layout:
  *     the request's tiles are the first T rows of each [T_cap] block, and
  *     its selections the first k entries of each row of k_cap.
- * SubBlock plans return VSA_ERR_UNSUPPORTED. Otherwise as vsa_forward
- * (capture-safe, five kernels). */
+ * SubBlock plans (gate may be NULL) run their four kernels the same way: the
+ * sub-block pool and the router read the lengths too. Otherwise as
+ * vsa_forward (capture-safe, five kernels). */
 vsa_status_t vsa_forward_lengths(vsa_plan_t plan, const vsa_lengths_t* lengths, const void* q, const void* k,
                                  const void* v, const void* gate, void* out, void* workspace,
                                  size_t workspace_bytes, void* stream);
@@ -281,7 +284,7 @@ vsa_status_t vsa_forward_rows(vsa_plan_t plan, const void* q, const void* k, con
  *                   rows is NULL
  *   rows          : output rows (vsa_forward_rows), or NULL
  *   lengths       : device lengths of the request (vsa_forward_lengths), or
- *                   NULL for the plan's own (SubBlock plans: NULL only)
+ *                   NULL for the plan's own
  *   preprocessed  : nonzero when q, k, v, gate and the pooled statistics come
  *                   from vsa_preprocess on this workspace and stream
  * With lengths, preprocessed and rows together, one captured graph runs the

@@ -225,8 +225,8 @@ def test_forward_ex_and_lengths_validation(lib):
         args = bsv.vsa_forward_args_t(g, 2 * g, 3 * g, 4 * g, None, None, None, 0)          # no output
         assert lib.vsa_forward_ex(plan, ctypes.byref(args), wsp, ws, None) == bsv.VSA_ERR_INVALID_ARG
         _, _, ws_sub = bsv.vsa_plan_info(sub)
-        args = bsv.vsa_forward_args_t(g, 2 * g, 3 * g, None, 6 * g, None, 12 * g, 0)       # SubBlock + lengths
-        assert lib.vsa_forward_ex(sub, ctypes.byref(args), wsp, ws_sub, None) == bsv.VSA_ERR_UNSUPPORTED
+        args = bsv.vsa_forward_args_t(g, 2 * g, 3 * g, None, 6 * g, None, 12 * g + 4, 0)   # SubBlock, misaligned lengths
+        assert lib.vsa_forward_ex(sub, ctypes.byref(args), wsp, ws_sub, None) == bsv.VSA_ERR_INVALID_ARG
         assert lib.vsa_forward_lengths(plan, None, ctypes.c_void_p(g), ctypes.c_void_p(2 * g), ctypes.c_void_p(3 * g),
                                        ctypes.c_void_p(4 * g), ctypes.c_void_p(6 * g), wsp, ws,
                                        None) == bsv.VSA_ERR_INVALID_ARG

@@ -199,3 +199,82 @@ def test_serving_step_in_one_graph(cuda_ok):
         ex.check()
         assert torch.equal(_bits(send), _bits(ex_send)), (lt, la, lv)
         assert torch.isnan(send.float()).sum() == (rows_in - n) * h * 128 * b
+
+
+SPARSITY = 0.6
+
+
+def _exact_subblock(b, h, lt, la, lv, seed):
+    q, k, v, _ = make_inputs(b, h, lt, la, lv, seed, device="cuda")
+    op = bsv.SubBlock(b, h, lt, la, lv, SPARSITY)
+    out = op(q, k, v).clone()
+    op.check()
+    return (q, k, v), out, op.debug_views()["tile_index"].clone()
+
+
+def test_subblock_requests_match_exact_shape_plans(cuda_ok):
+    """SubBlock routing in a capacity plan: the sub-block pool and the router
+    read the device lengths too (k from the request's T: T - floor(s T) rounded
+    up to 8, capped at T). Each request equals an exact-shape SubBlock plan bit
+    for bit, selections included; padding rows stay untouched."""
+    b, h, clt, cla, clv = CAP
+    cap = bsv.SubBlock(b, h, clt, cla, clv, SPARSITY)
+    n_cap = cap.seq
+    bufs = _capacity_buffers(b, h, n_cap, 54)[:3]
+    lengths = torch.empty(3, dtype=torch.int64, device="cuda")
+    for i, (lt, la, lv) in enumerate(REQUESTS):
+        n = lt + la + lv
+        ins, ref, ref_idx = _exact_subblock(b, h, lt, la, lv, 90 + i)
+        for dst, src in zip(bufs, ins):
+            dst[:, :n].copy_(src)
+        lengths.copy_(torch.tensor([lt, la, lv]))
+        out = torch.full((b, n_cap, h, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        cap.forward_lengths(lengths, *bufs, None, out)
+        cap.check()
+        t, kk = ref_idx.shape[2], ref_idx.shape[3]
+        assert torch.equal(cap.debug_views()["tile_index"][:, :, :t, :kk], ref_idx), (lt, la, lv)
+        assert torch.equal(_bits(out[:, :n]), _bits(ref)), (lt, la, lv)
+        assert torch.isnan(out[:, n:].float()).all(), (lt, la, lv)
+
+
+def test_one_captured_graph_serves_every_subblock_request(cuda_ok):
+    b, h, clt, cla, clv = CAP
+    cap = bsv.SubBlock(b, h, clt, cla, clv, SPARSITY)
+    n_cap = cap.seq
+    bufs = _capacity_buffers(b, h, n_cap, 55)[:3]
+    out = torch.full((b, n_cap, h, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lengths = torch.tensor(list(REQUESTS[0]), dtype=torch.int64, device="cuda")
+    cap.forward_lengths(lengths, *bufs, None, out)  # warm-up outside the capture
+    cap.check()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cap.forward_lengths(lengths, *bufs, None, out)
+    for i, (lt, la, lv) in enumerate(REQUESTS[::-1]):
+        n = lt + la + lv
+        ins, ref, _ = _exact_subblock(b, h, lt, la, lv, 100 + i)
+        for dst, src in zip(bufs, ins):
+            dst[:, :n].copy_(src)
+        lengths.copy_(torch.tensor([lt, la, lv]))
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        cap.check()
+        assert torch.equal(_bits(out[:, :n]), _bits(ref)), (lt, la, lv)
+        assert torch.isnan(out[:, n:].float()).all()
+
+
+@pytest.mark.parametrize("bad", [(131, 70, 64), (0, 0, 0), (0, 0, 64 * 12 + 31)])
+def test_subblock_lengths_outside_the_capacity_are_reported(cuda_ok, bad):
+    b, h, clt, cla, clv = CAP
+    cap = bsv.SubBlock(b, h, clt, cla, clv, SPARSITY)
+    bufs = _capacity_buffers(b, h, cap.seq, 56)[:3]
+    out = torch.full((b, cap.seq, h, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lengths = torch.tensor(list(bad), dtype=torch.int64, device="cuda")
+    cap.forward_lengths(lengths, *bufs, None, out)
+    with pytest.raises(bsv.VsaError) as e:
+        cap.check()
+    assert e.value.status == bsv.VSA_ERR_INVALID_ARG
+    assert torch.isnan(out.float()).all()
+    lengths.copy_(torch.tensor(list(REQUESTS[0])))   # the next valid request clears the report
+    cap.forward_lengths(lengths, *bufs, None, out)
+    cap.check()
