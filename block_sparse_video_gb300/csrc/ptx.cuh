@@ -25,10 +25,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ void mbar_inval(uint32_t bar) {
-  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -74,22 +70,6 @@ __device__ __forceinline__ void raise_error(unsigned int* words, unsigned int co
   if (atomicCAS(words, 0u, code) == 0u) words[1] = detail;
   atomicExch(words + 2, 1u);
   __threadfence();
-}
-
-// try_wait with a suspend-time hint: the waiting thread sleeps (issuing
-// nothing) until the phase completes or the hint elapses.
-constexpr uint32_t kSuspendHintNs = 500000;
-
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-      "selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
-      : "memory");
-  return ok != 0;
 }
 
 // Wait for the phase of `bar` with parity `parity` to complete. Returns false
@@ -229,18 +209,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, int a_mn, in
          | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem], issued by one thread.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// The same product issued from a converged warp: elect.sync picks one lane
-// (the lowest, so always the same lane of a full warp) inside the asm block.
+// D[tmem] (+)= A[smem] * B[smem], issued from a converged warp: elect.sync
+// picks one lane (the lowest, so always the same lane of a full warp) inside
+// the asm block.
 // Keeping the issuing loop warp-uniform keeps its descriptor arithmetic in
 // uniform registers: measured on GB300, a loop of these issues one M=128, N=64
 // MMA per ~49 cycles (the tensor pipe's rate) where the same loop run by lane 0
@@ -255,51 +226,13 @@ __device__ __forceinline__ void umma_bf16_elect(uint32_t d_tmem, uint64_t a_desc
       : "memory");
 }
 
-// Make `bar` track completion of every tcgen05 op this thread issued so far.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// umma_commit from a converged warp, by the lane elect.sync picks (the lane
+// Make `bar` track completion of every tcgen05 op the issuing lane issued so
+// far; from a converged warp, by the lane elect.sync picks (the lane
 // umma_bf16_elect issues from).
 __device__ __forceinline__ void umma_commit_elect(uint32_t bar) {
   asm volatile(
       "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar)
-      : "memory");
-}
-
-#define VSA_R32(r)                                                                              \
-  "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),           \
-      "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),    \
-      "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), \
-      "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), \
-      "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-#define VSA_W32(r)                                                                              \
-  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),       \
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),          \
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),        \
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),        \
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-
-// Warp-collective: thread i reads TMEM lane (lane field of taddr) + i,
-// 32 consecutive 32-bit columns starting at the column field of taddr.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : VSA_R32(r)
-      : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
-          taddr),
-      VSA_W32(r)
       : "memory");
 }
 
@@ -352,26 +285,6 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool p
       : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
       : "memory");
   return out != 0;
-}
-
-// d = a * b + c on two lanes at once (packed fp32).
-__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, float b0,
-                                          float b1, float c0, float c1) {
-  asm("{\n.reg .b64 ra, rb, rc, rd;\n"
-      "mov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\nmov.b64 rc, {%6, %7};\n"
-      "fma.rn.f32x2 rd, ra, rb, rc;\nmov.b64 {%0, %1}, rd;\n}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
-}
-
-// d = a + b on two lanes at once (packed fp32).
-__device__ __forceinline__ void add_f32x2(float& d0, float& d1, float a0, float a1, float b0,
-                                          float b1) {
-  asm("{\n.reg .b64 ra, rb, rd;\n"
-      "mov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\n"
-      "add.rn.f32x2 rd, ra, rb;\nmov.b64 {%0, %1}, rd;\n}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
