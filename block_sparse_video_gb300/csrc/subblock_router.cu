@@ -36,8 +36,10 @@
 // block, key block) pair; lane ^ 16 holds the other 8. The log-sum-exp is
 // lane-local plus one shuffle for the maximum and one for the sum. It runs in
 // log2 units (ex2 and lg2 on the MUFU pipe), which ranks in the same order.
-// The warp-per-row radix select of the coarse kernel then picks each row's
-// top k.
+// The coarse kernel's warp-per-row selection then picks each row's top k: the
+// counting threshold search, with the radix select where scores tie at the
+// cut. With device lengths the router scores the request's tiles only and
+// writes its selections at the plan's strides.
 #include <cmath>
 
 #include "kernels.cuh"
