@@ -194,11 +194,12 @@ void destroy_plan(vsa_plan* p);
 // The host-buffer path pipelines up to 8 head groups (host only: the streams
 // and events are created on the first call).
 // Head widths of the pipeline's groups. Up to 8 heads: two halves. Beyond:
-// 4, 6, then 8 heads per group, the last taking what remains. The ramp keeps
-// the first group's copy (which nothing hides) short, and the next groups'
-// copies no longer than the forward of the group before them; 8-head groups
-// copy 2 KB host rows, wide enough for the copy engines to run near the link
-// rate.
+// 4, 6, then 8 heads per group, the remainder last, split into (r - 2, 2)
+// when it has 4 heads or more. The ramp keeps the first group's copy-in
+// (which nothing hides) short and each later copy no longer than the forward
+// of the group before it; 8-head groups copy 2 KB host rows, wide enough for
+// the copy engines to run near the link rate. The 2-head tail keeps the last
+// copy-out (which nothing hides either) short.
 std::vector<int> head_group_widths(int H) {
   std::vector<int> w;
   if (H <= 1) return {H};
@@ -209,6 +210,10 @@ std::vector<int> head_group_widths(int H) {
     const int take = want < left ? want : left;
     w.push_back(take);
     left -= take;
+  }
+  if (w.back() >= 4) {
+    w.back() -= 2;
+    w.push_back(2);
   }
   return w;
 }

@@ -312,8 +312,8 @@ vsa_status_t vsa_forward_ex(vsa_plan_t plan, const vsa_forward_args_t* args, voi
  * output and the workspace.
  *
  * With two or more heads the work is pipelined over head groups (up to 8
- * heads: two halves; beyond, groups of 4, 6, then 8 heads, the last taking
- * the rest):
+ * heads: two halves; beyond, groups of 4, 6, then 8 heads, the rest last,
+ * split into a group and a final 2-head group when it has 4 heads or more):
  *   * each group's heads are copied in on a library-owned stream (strided
  *     copies of each host row's slice). When q, k, v (and gate) are pinned or
  *     registered host memory, the first group's slices are instead gathered by

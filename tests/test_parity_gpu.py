@@ -130,8 +130,9 @@ def test_deterministic(cuda_ok):
                                                     (11, True, False)])
 def test_host_buffer_path_matches_device_path(cuda_ok, heads, subblock, pinned):
     """The host-buffer path copies head groups in, runs each group's forward and
-    copies it out, pipelined. Group widths ramp up: 11 heads run as groups of
-    4, 6 and 1; 24 heads as 4, 6, 8 and 6; 2 heads as two of one. With pinned
+    copies it out, pipelined. Group widths ramp up and end on two heads: 11
+    heads run as groups of 4, 6 and 1; 24 heads as 4, 6, 8, 4 and 2; 2 heads as
+    two of one. With pinned
     inputs the first group is gathered by a kernel reading host memory, with
     pageable ones by strided copies. Every head's result must equal the device
     path bit for bit."""
