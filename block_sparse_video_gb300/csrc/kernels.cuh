@@ -104,18 +104,21 @@ cudaError_t launch_coarse_topk(const Geometry& g, const float* pooled_q, const f
 
 // SubBlock routing: 16-token sub-block means of q and k (fp32 [B, H, 4T, 128],
 // empty sub-blocks of a ragged last tile as 0, plus the same values split into
-// bf16 hi + lo in mma fragment order, subblock_rows_padded(g) x 512 bytes per
-// (b, h)), then the k video key tiles of highest estimated softmax mass per
-// video query tile (tile_index int32 [B, H, T, k], ascending).
+// bf16 hi + lo rows: frag_* holds hi [B, H, spad, 128] then lo [B, H, spad,
+// 128], spad = subblock_rows_padded(g), 512 bytes per sub-row in all), then
+// the k video key tiles of highest estimated softmax mass per video query tile
+// (tile_index int32 [B, H, T, k], ascending).
 int subblock_rows_padded(const Geometry& g);
 // With device lengths (dl.len, dl.sparsity set) g is the capacity: both
 // kernels keep its layout and work on the request's tiles.
 cudaError_t launch_subpool(const Geometry& g, const __nv_bfloat16* q, const __nv_bfloat16* k, float* sub_q,
                            float* sub_k, void* frag_q, void* frag_k, const DeviceLengths& dl, cudaStream_t stream);
 size_t subblock_router_smem_bytes(const Geometry& g, int* rows_per_cta);
-cudaError_t launch_subblock_router(const Geometry& g, const void* frag_q, const void* frag_k,
-                                   int32_t* tile_index, unsigned int* err, const DeviceLengths& dl,
-                                   cudaStream_t stream);
+// maps: the sub-pool's bf16 rows as TMA views {128 channels, spad rows, B H,
+// 1}, boxes of 64 channels x 64 rows, 128-byte swizzled: q hi, q lo, k hi,
+// k lo.
+cudaError_t launch_subblock_router(const Geometry& g, const CUtensorMap (&maps)[4], int32_t* tile_index,
+                                   unsigned int* err, const DeviceLengths& dl, cudaStream_t stream);
 
 // Fine attention: prefix query tiles over every key, video query tiles over
 // the prefix plus their selected video tiles; epilogue adds sigmoid(gate) *

@@ -94,24 +94,13 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
 }
 
 // 16-token sub-block means of q and k for the SubBlock router: fp32 rows
-// [B, H, 4T, 128] (runs < 4T), and the same values split into bf16 hi + lo in
-// mma.sync m16n8k16 fragment order:
-//   frag[bh][tile8][ks][lane] = uint4 {hi a, hi b, lo a, lo b}
-// for 8 fragment rows (tile8), 16 channels (ks) and lane = 4 g + t4. The
-// words are: a = channels 16 ks + 2 t4 and + 1 of fragment row g; b = the same
-// channels + 8. A tile8 is the B operand of 8 key sub-rows, and two tile8s
-// are the A operand of 16 query sub-rows.
-//
-// Sub-rows are permuted inside each group of 16 (4 blocks, 4 sub-blocks each)
-// so that one lane's m16n8 products cover whole pairs of blocks.
-//   * Query sub-block a of block j sits in tile8 a & 1, row j + 4 (a >> 1).
-//     Rows g and g + 8 of the m16 tile are then sub-blocks 2 (g >> 2) and
-//     2 (g >> 2) + 1 of block g & 3.
-//   * Key sub-block s of block j sits in tile8 s >> 1, row 2 j + (s & 1).
-//     Columns 2 t4 and 2 t4 + 1 of the two n8 tiles are then all four
-//     sub-blocks of block t4.
-// Rows are padded to spad per (b, h). Runs past the video (n <= 0) are zeros
-// in both forms.
+// [B, H, 4T, 128] (runs < 4T), and the same values split into bf16 hi + lo
+// (x ~ hi + lo, hi = bf16(x), lo = bf16(x - hi)) as two row-major bf16
+// tensors [B, H, spad, 128] (hi rows, then lo rows, in the `frag` buffer).
+// Sub-row `run` of (b, h) is sub-block `run` of the video, in token order.
+// These rows are the router's tensor-core operands, loaded by TMA. Rows are
+// padded to spad per (b, h); runs past the video (n <= 0) are zeros in both
+// forms.
 __global__ void __launch_bounds__(kPoolThreads)
 subpool_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                float* __restrict__ pq, float* __restrict__ pk, uint4* __restrict__ fq, uint4* __restrict__ fk,
@@ -127,7 +116,7 @@ subpool_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
   const __nv_bfloat16* src = blockIdx.z == 0 ? q : k;
   float* dst = blockIdx.z == 0 ? pq : pk;
   uint4* frag = blockIdx.z == 0 ? fq : fk;
-  const bool active = vec < row_vecs;  // whole lane pairs (row_vecs is even)
+  const bool active = vec < row_vecs;
   const int n = min(kLen, Lv - run * kLen);
   const int h = vec / (kHeadDim / 8);
   const int d0 = (vec % (kHeadDim / 8)) * 8;
@@ -156,32 +145,15 @@ subpool_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
     out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
-  // this thread's channels d0 .. d0 + 7 are word `half` (a or b) of lanes 4 g + 0..3;
-  // the neighbour thread (d0 + 8 or d0 - 8) holds the other word of the same lanes
+  // bf16 hi and lo rows: this thread's channels d0 .. d0 + 7 of sub-row `run`
+  if (!active) return;
   uint32_t hi[4], lo[4];
 #pragma unroll
   for (int t4 = 0; t4 < 4; ++t4) split_pair(acc[2 * t4], acc[2 * t4 + 1], hi[t4], lo[t4]);
-  const int half = (d0 / 8) & 1;
-  uint32_t ohi[4], olo[4];
-#pragma unroll
-  for (int t4 = 0; t4 < 4; ++t4) {
-    ohi[t4] = __shfl_xor_sync(0xffffffffu, hi[t4], 1);
-    olo[t4] = __shfl_xor_sync(0xffffffffu, lo[t4], 1);
-  }
-  if (!active) return;
-  const int grp = run / 16, blk = (run % 16) / 4, sb = run % 4;
-  const int tile8 = 2 * grp + (blockIdx.z == 0 ? (sb & 1) : (sb >> 1));
-  const int g = blockIdx.z == 0 ? blk + 4 * (sb >> 1) : 2 * blk + (sb & 1);
-  const int ks = d0 / 16;
-  uint4* f = frag + ((static_cast<size_t>(b) * H + h) * (spad / 8) + tile8) * 8 * 32 + ks * 32 + 4 * g;
-  // the a-word thread writes lanes 4 g + 0, 1 and the b-word thread lanes 4 g + 2, 3
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int t4 = 2 * half + j;
-    const uint32_t ha = half ? ohi[t4] : hi[t4], hb = half ? hi[t4] : ohi[t4];
-    const uint32_t la = half ? olo[t4] : lo[t4], lb = half ? lo[t4] : olo[t4];
-    f[t4] = make_uint4(ha, hb, la, lb);
-  }
+  const size_t rows = static_cast<size_t>(cap.B) * H * spad;  // hi rows, then as many lo rows
+  const size_t at = ((static_cast<size_t>(b) * H + h) * spad + run) * (kHeadDim / 8) + d0 / 8;
+  frag[at] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  frag[rows * (kHeadDim / 8) + at] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
 }
 
 }  // namespace

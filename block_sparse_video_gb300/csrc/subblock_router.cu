@@ -16,30 +16,34 @@
 //   * selection is the k largest fp32 scores, ties to the lower block,
 //     stored ascending.
 //
-// A CTA owns R query blocks (4R query sub-rows) of one (batch, head) and keeps
-// their R x T block scores in shared memory.
+// A CTA owns R query blocks (N = 4R query sub-rows) of one (batch, head) and
+// keeps their R x T block scores in shared memory.
 //
-// Operands. The sub-pool kernel leaves every sub-block mean split into bf16
-// hi + lo (x ~ hi + lo, ~2^-16 relative), already in mma.sync m16n8k16
-// fragment order. So the products are bf16 tensor-core MMAs,
-//   q . k ~ hi.hi + hi.lo + lo.hi,
-// with fp32 accumulation. That is about 2^-16 relative error on each logit,
-// against the 1e-3 tie band of the selection. No operand is converted in the
-// inner loop. The CTA's query fragments (R/2 x 4 KB) come in one bulk copy,
-// and each warp keeps its own m16 tile's fragments in registers.
-// Key fragments stream through a two-slot ring of CH-sub-row chunks, filled by
-// bulk copies that complete on mbarriers.
+// Products on the tcgen05 tensor cores. The sub-pool kernel leaves every
+// sub-block mean split into bf16 hi + lo rows (x ~ hi + lo, ~2^-16
+// relative), so q . k ~ hi.hi + hi.lo + lo.hi: three bf16 MMAs accumulating
+// in fp32 in TMEM, about 2^-16 relative error on each logit against the 1e-3
+// tie band of the selection. The product is transposed, as for the fine
+// kernel's scores:
+//   L^T[128 key sub-rows x N query sub-rows] = K_chunk . Q^T     (M = 128)
+// so a TMEM lane holds one key sub-row and a column one query sub-row.
 //
-// The sub-pool kernel permutes sub-rows inside each group of 4 blocks (see
-// pool.cu). A warp's tile is one m16 tile (4 query blocks) by two n8 tiles
-// (4 key blocks), and each lane then holds 8 of the 16 logits of one (query
-// block, key block) pair; lane ^ 16 holds the other 8. The log-sum-exp is
-// lane-local plus one shuffle for the maximum and one for the sum. It runs in
-// log2 units (ex2 and lg2 on the MUFU pipe), which ranks in the same order.
-// The coarse kernel's warp-per-row selection then picks each row's top k: the
-// counting threshold search, with the radix select where scores tie at the
-// cut. With device lengths the router scores the request's tiles only and
-// writes its selections at the plan's strides.
+// Warp roles (320 threads):
+//   * warp 8 loads by TMA the CTA's query rows (hi and lo, once) and the key
+//     chunks (each chunk's hi rows, then its lo rows) through a 3-stage ring
+//     of 32 KB;
+//   * warp 9 owns TMEM (two accumulators of N columns, alternating by chunk)
+//     and issues the MMAs, converged with one elected lane;
+//   * warps 0-7 read each accumulator (warp w: TMEM lanes 32 (w % 4) .. + 31,
+//     columns of half w / 4) and fold it into block scores: per lane (one key
+//     sub-row) and query block, the log-sum-exp of its 4 query sub-rows
+//     weighted by the sub-blocks' token counts, in log2 units (ex2 and lg2 on
+//     the MUFU pipe, which ranks in the same order); then across the 4 lanes
+//     of the key block (lanes 4j .. 4j + 3), max and sum in two shuffle steps.
+// The same 8 warps then pick each row's top k with the coarse kernel's
+// selection: the counting threshold search, with the radix select where
+// scores tie at the cut. With device lengths the router scores the
+// request's tiles only and writes its selections at the plan's strides.
 #include <cmath>
 
 #include "kernels.cuh"
@@ -49,12 +53,26 @@
 namespace vsa {
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
-constexpr int kTile8Bytes = 8 * 32 * 16;          // fragments of 8 sub-rows x 128 channels: 4 KB
-constexpr size_t kSmemBudget = 220 * 1024;
-constexpr int kSub = 16;                          // tokens per sub-block
-constexpr unsigned int kDetailRouterQ = 0x700, kDetailRouterK = 0x710;
+constexpr int kSub = 16;                                      // tokens per sub-block
+constexpr int kChunkRows = 128;                               // key sub-rows per chunk: the MMA's M
+constexpr uint32_t kStageBytes = kChunkRows * kHeadDim * 2;   // a chunk's hi or lo rows: 32 KB
+constexpr int kStages = 3;
+constexpr uint32_t kQBytes = 64 * kHeadDim * 2;               // a 64-row box pair, hi or lo: 16 KB
+constexpr int kEpiWarps = 8;
+constexpr int kWarpTma = kEpiWarps, kWarpMma = kEpiWarps + 1;
+constexpr int kThreads = 32 * (kEpiWarps + 2);
+constexpr size_t kSmemBudget = 225 * 1024;
+constexpr unsigned int kDetailQ = 0x700, kDetailK = 0x710, kDetailKEmpty = 0x720, kDetailAcc = 0x730,
+                       kDetailAccEmpty = 0x740;
+// shared memory, from a 1024-byte aligned base: Q hi, Q lo, the K ring, the
+// block scores [R][bstride], then the barriers and the TMEM slot
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + 2 * kQBytes;
+constexpr uint32_t kOffS = kOffK + kStages * kStageBytes;
+constexpr int kBarQ = 0, kBarKFull = 1, kBarKEmpty = kBarKFull + kStages, kBarAccFull = kBarKEmpty + kStages,
+              kBarAccEmpty = kBarAccFull + 2, kNumBars = kBarAccEmpty + 2;
+constexpr uint32_t kTailBytes = kNumBars * 8 + 16;
+static_assert(kEpiWarps * kBins * 4 <= kStages * kStageBytes, "selection histograms fit over the K ring");
 
 // log2(number of valid tokens of sub-block s), -inf for an empty one
 __device__ __forceinline__ float lg_count(int s, int Lv) {
@@ -74,177 +92,206 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
-// R query blocks per CTA (R/4 m16 tiles), CH key sub-rows per chunk (CH/16
-// n-pairs). Warp w takes m16 tile w / (CH/16) and n-pair w % (CH/16) of each
-// chunk; warps past R/4 m16 tiles idle.
-template <int R, int CH>
+template <int R>
 __global__ void __launch_bounds__(kThreads, 1)
-subblock_router_kernel(const uint4* __restrict__ frag_q, const uint4* __restrict__ frag_k,
+subblock_router_kernel(const __grid_constant__ CUtensorMap map_q_hi, const __grid_constant__ CUtensorMap map_q_lo,
+                       const __grid_constant__ CUtensorMap map_k_hi, const __grid_constant__ CUtensorMap map_k_lo,
                        int32_t* __restrict__ tile_index, unsigned int* err, Geometry cap, DeviceLengths dl,
                        int spad) {
-  constexpr int MT = R / 4;
-  constexpr int NP = CH / 16;
-  constexpr int kChunkBytes = CH / 8 * kTile8Bytes;
+  constexpr int N = 4 * R;                             // query sub-rows per CTA: the MMA's N
+  constexpr int kCols = N / 2;                         // accumulator columns per epilogue thread
+  constexpr uint32_t kTmemCols = 2 * N < 32 ? 32 : 2 * N;
+  static_assert(kCols % 16 == 0 && N <= 64, "epilogue loads of 16 columns; query rows within one box");
   // The request's tiles (the plan's own, or the device lengths'); the layouts
-  // (fragment rows spad, selections [T_cap][k_cap], shared-memory rows) are
-  // the plan's.
+  // (sub-rows spad, selections [T_cap][k_cap]) are the plan's.
   const DynGeom dg = dyn_geom(cap, dl);
   if (!dg.valid) {
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *dl.invalid = 1u;
     return;
   }
   const int T = dg.T, Lv = dg.Lv, k = dg.k;
-  if (static_cast<int>(blockIdx.x) * R >= T) return;  // uniform per CTA, before any copy
-  const int bstride = spad / 4 + 4;                 // block-score row stride (floats)
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* s_kbuf = smem;                           // [2][kChunkBytes] key fragments
-  uint8_t* s_q = smem + 2 * kChunkBytes;            // [R/2 tile8][kTile8Bytes] query fragments
-  float* S = reinterpret_cast<float*>(s_q + (R / 2) * kTile8Bytes);  // [R][bstride] block scores
-  uint64_t* bars = reinterpret_cast<uint64_t*>(S + R * bstride);     // q, k slot 0, k slot 1
-  int* hist = reinterpret_cast<int*>(smem);         // [kWarps][kBins], over the key ring after the products
+  const int q0 = blockIdx.x * R;                       // first query block of this CTA
+  if (q0 >= T) return;                                 // uniform per CTA, before any barrier or copy
+  const int bstride = spad / 4 + 4;                    // block-score row stride (floats)
+  const int n_chunks = (4 * T + kChunkRows - 1) / kChunkRows;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  float* S = reinterpret_cast<float*>(smem + kOffS);
+  const uint32_t bar0 = sbase + kOffS + static_cast<uint32_t>(R * bstride * 4);
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffS + R * bstride * 4 + kNumBars * 8);
+  int* hist = reinterpret_cast<int*>(smem + kOffK);    // [kEpiWarps][kBins], once the products are done
 
-  const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
-  const int g = lane >> 2, t4 = lane & 3;
-  const int q0 = blockIdx.x * R;                    // first query block of this CTA
-  const size_t bh = blockIdx.y;
-  const size_t tiles_per_bh = static_cast<size_t>(spad) / 8;
-  const uint8_t* gq = reinterpret_cast<const uint8_t*>(frag_q + bh * tiles_per_bh * 256);
-  const uint8_t* gk = reinterpret_cast<const uint8_t*>(frag_k + bh * tiles_per_bh * 256);
-  const float scale_log2 = 0.08838834764831845f * 1.4426950408889634f;  // log2(e) / sqrt(128)
-  const int n_chunks = (4 * T + CH - 1) / CH;       // chunks holding the request's key sub-rows
-  const uint32_t bar_q = smem_u32(bars), bar_k0 = smem_u32(bars + 1);
-
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int bh = blockIdx.y;
   if (tid == 0) {
-    mbar_init(bar_q, 1);
-    mbar_init(bar_k0, 1);
-    mbar_init(bar_k0 + 8, 1);
+    mbar_init(bar(kBarQ), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kBarKFull + s), 1);
+      mbar_init(bar(kBarKEmpty + s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar(kBarAccFull + a), 1);
+      mbar_init(bar(kBarAccEmpty + a), kEpiWarps);
+    }
     fence_barrier_init();
   }
+  if (warp == kWarpMma) tmem_alloc(smem_u32(tslot), kTmemCols);
+  tc_fence_before();
   __syncthreads();
-  int issued = 0;  // key chunks whose copy thread 0 has issued
-  if (tid == 0) {
-    // query sub-rows 4 q0 .. 4 q0 + 4R: R/2 tile8s, contiguous (within spad for every CTA)
-    mbar_arrive_expect_tx(bar_q, (R / 2) * kTile8Bytes);
-    bulk_load(smem_u32(s_q), gq + static_cast<size_t>(q0 / 2) * kTile8Bytes, (R / 2) * kTile8Bytes, bar_q);
-    for (; issued < 2 && issued < n_chunks; ++issued) {
-      mbar_arrive_expect_tx(bar_k0 + 8 * issued, kChunkBytes);
-      bulk_load(smem_u32(s_kbuf + issued * kChunkBytes), gk + static_cast<size_t>(issued) * kChunkBytes,
-                kChunkBytes, bar_k0 + 8 * issued);
-    }
-  }
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  bool ok = true;
 
-  const int m = warp / NP, np = warp % NP;
-  const bool has_work = m < MT;
-  // this lane's pair: query block 4 m + (g & 3) of the CTA, key block 4 np + t4 of each chunk;
-  // its query sub-blocks are a0 = 2 (g >> 2) (row g) and a0 + 1 (row g + 8)
-  const int qsub = 4 * (q0 + 4 * m + (g & 3)) + 2 * (g >> 2);
-  const float lq0 = lg_count(qsub, Lv), lq1 = lg_count(qsub + 1, Lv);
-  const uint32_t qa = smem_u32(s_q + (2 * m) * kTile8Bytes) + lane * 16;
-
-  bool ok = mbar_wait(bar_q, 0, err, kDetailRouterQ);
-  // this warp's m16 tile is the same for every chunk: its A fragments stay in registers
-  uint4 aq[kHeadDim / 16][2];
-#pragma unroll
-  for (int ks = 0; ks < kHeadDim / 16; ++ks) {
-    aq[ks][0] = (ok && has_work) ? lds128(qa + ks * 512) : make_uint4(0, 0, 0, 0);                // rows g
-    aq[ks][1] = (ok && has_work) ? lds128(qa + kTile8Bytes + ks * 512) : make_uint4(0, 0, 0, 0);  // rows g + 8
-  }
-  for (int c = 0; c < n_chunks; ++c) {
-    const int slot = c & 1;
-    ok = ok && mbar_wait(bar_k0 + 8 * slot, (c >> 1) & 1, err, kDetailRouterK);
-    if (ok && has_work) {
-      const int kblk = c * (CH / 4) + 4 * np + t4;  // key block of this lane
-      float lk[4];
-#pragma unroll
-      for (int sb = 0; sb < 4; ++sb) lk[sb] = lg_count(4 * kblk + sb, Lv);
-      const uint32_t kb = smem_u32(s_kbuf + slot * kChunkBytes + (2 * np) * kTile8Bytes) + lane * 16;
-      float acc[2][4];
-#pragma unroll
-      for (int ni = 0; ni < 2; ++ni) acc[ni][0] = acc[ni][1] = acc[ni][2] = acc[ni][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < kHeadDim / 16; ++ks) {
-        const uint4 t0 = aq[ks][0], t1 = aq[ks][1];
-#pragma unroll
-        for (int ni = 0; ni < 2; ++ni) {
-          const uint4 bf = lds128(kb + ni * kTile8Bytes + ks * 512);  // {hi b0, hi b1, lo b0, lo b1}
-          mma_bf16x3(acc[ni], t0, t1, bf);
+  if (warp == kWarpTma) {
+    // ------------------------------------------------------------ TMA loads (one lane)
+    if (lane == 0) {
+      int issued = 0;  // K stages issued
+      mbar_arrive_expect_tx(bar(kBarQ), 2 * kQBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int half = 0; half < 2; ++half)
+          tma_load_4d(sbase + kOffQ + t * kQBytes + half * 8192, t ? &map_q_lo : &map_q_hi, 64 * half, 4 * q0, bh, 0,
+                      bar(kBarQ));
+      for (int i = 0; i < 2 * n_chunks; ++i) {
+        const int st = i % kStages;
+        // the stage's previous use (stage i - kStages) must have been read by its MMAs
+        if (i >= kStages && !mbar_wait(bar(kBarKEmpty + st), ((i / kStages) - 1) & 1, err, kDetailKEmpty)) {
+          ok = false;
+          break;
         }
+        mbar_arrive_expect_tx(bar(kBarKFull + st), kStageBytes);
+        const CUtensorMap* m = (i & 1) ? &map_k_lo : &map_k_hi;
+        const int row0 = kChunkRows * (i / 2);
+        for (int half = 0; half < 2; ++half)
+          for (int rg = 0; rg < 2; ++rg)
+            tma_load_4d(sbase + kOffK + st * kStageBytes + half * 16384 + rg * 8192, m, 64 * half, row0 + 64 * rg,
+                        bh, 0, bar(kBarKFull + st));
+        issued = i + 1;
       }
-      // acc[ni][e] (e < 2): row g, key sub-block 2 ni + e; acc[ni][2 + e]: row g + 8
-      float x[8];
+      if (!ok) {
+        // gave up: let the copies already issued land before the CTA ends
+        mbar_wait_drain(bar(kBarQ), 0, kWaitLimitNs);
+        for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+          mbar_wait_drain(bar(kBarKFull + i % kStages), (i / kStages) & 1, kWaitLimitNs);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issue (converged warp)
+    const uint32_t idesc = idesc_bf16_f32(128, N, 0, 0);
+    const uint64_t dq_hi = smem_desc_sw128(sbase + kOffQ, 16, 1024);
+    const uint64_t dq_lo = smem_desc_sw128(sbase + kOffQ + kQBytes, 16, 1024);
+    ok = mbar_wait_warp(bar(kBarQ), 0, err, kDetailQ);
+    for (int c = 0; c < n_chunks && ok; ++c) {
+      const int a = c & 1;
+      // accumulator a was last read by the epilogue of chunk c - 2
+      if (c >= 2) ok = mbar_wait_warp(bar(kBarAccEmpty + a), ((c / 2) - 1) & 1, err, kDetailAccEmpty);
+      const uint32_t d = tbase + static_cast<uint32_t>(a * N);
+      for (int part = 0; part < 2 && ok; ++part) {  // the chunk's hi rows, then its lo rows
+        const int i = 2 * c + part, st = i % kStages;
+        ok = mbar_wait_warp(bar(kBarKFull + st), (i / kStages) & 1, err, kDetailK);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t dk = smem_desc_sw128(sbase + kOffK + st * kStageBytes, 16, 1024);
 #pragma unroll
-      for (int ni = 0; ni < 2; ++ni)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          x[4 * ni + e] = fmaf(acc[ni][e], scale_log2, lq0 + lk[2 * ni + e]);
-          x[4 * ni + 2 + e] = fmaf(acc[ni][2 + e], scale_log2, lq1 + lk[2 * ni + e]);
+        for (int s = 0; s < kHeadDim / 16; ++s) {
+          const uint32_t koff = ((s >> 2) * 16384 + (s & 3) * 32) >> 4;
+          const uint32_t qoff = ((s >> 2) * 8192 + (s & 3) * 32) >> 4;
+          if (part == 0) {
+            umma_bf16_elect(d, dk + koff, dq_hi + qoff, idesc, s > 0 ? 1u : 0u);  // hi . hi
+            umma_bf16_elect(d, dk + koff, dq_lo + qoff, idesc, 1u);               // hi . lo
+          } else {
+            umma_bf16_elect(d, dk + koff, dq_hi + qoff, idesc, 1u);               // lo . hi
+          }
         }
-      float mx = x[0];
-#pragma unroll
-      for (int i = 1; i < 8; ++i) mx = fmaxf(mx, x[i]);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      float sum = 0.f;
-      if (mx > -INFINITY) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) sum += ex2(x[i] - mx);
+        umma_commit_elect(bar(kBarKEmpty + st));  // the stage may be refilled
       }
-      sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-      if (g < 4)
-        S[(4 * m + g) * bstride + kblk] = mx > -INFINITY ? mx + lg2(sum) : -INFINITY;
+      if (ok) umma_commit_elect(bar(kBarAccFull + a));
     }
-    __syncthreads();  // every warp is done with this slot
-    if (tid == 0 && ok && c + 2 < n_chunks) {
-      mbar_arrive_expect_tx(bar_k0 + 8 * slot, kChunkBytes);
-      bulk_load(smem_u32(s_kbuf + slot * kChunkBytes), gk + static_cast<size_t>(c + 2) * kChunkBytes,
-                kChunkBytes, bar_k0 + 8 * slot);
-      ++issued;
+  } else {
+    // ------------------------------------------------------------ block scores (warps 0-7)
+    const unsigned full = 0xffffffffu;
+    const int quarter = warp % 4, col0 = (warp / 4) * kCols;
+    const int r = 32 * quarter + lane;                 // key sub-row within a chunk (TMEM lane)
+    const uint32_t taddr = tbase + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(col0);
+    const float scale_log2 = 0.08838834764831845f * 1.4426950408889634f;  // log2(e) / sqrt(128)
+    float lq[kCols];                                   // log2 token counts of this thread's query sub-rows
+#pragma unroll
+    for (int j = 0; j < kCols; ++j) lq[j] = lg_count(4 * q0 + col0 + j, Lv);
+    for (int c = 0; c < n_chunks && ok; ++c) {
+      const int a = c & 1;
+      ok = mbar_wait_warp(bar(kBarAccFull + a), (c / 2) & 1, err, kDetailAcc);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v[kCols];
+#pragma unroll
+      for (int j = 0; j < kCols; j += 16)
+        tmem_ld16(taddr + static_cast<uint32_t>(a * N + j), *reinterpret_cast<uint32_t(*)[16]>(v + j));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarAccEmpty + a));  // the MMAs of chunk c + 2 may overwrite it
+      const float lk = lg_count(kChunkRows * c + r, Lv);
+#pragma unroll
+      for (int jb = 0; jb < kCols / 4; ++jb) {
+        float x[4], m = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          x[t] = fmaf(__uint_as_float(v[4 * jb + t]), scale_log2, lq[4 * jb + t] + lk);
+          m = fmaxf(m, x[t]);
+        }
+        float s = 0.f;
+        if (m > -INFINITY) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t) s += ex2(x[t] - m);
+        }
+        float mb = fmaxf(m, __shfl_xor_sync(full, m, 1));
+        mb = fmaxf(mb, __shfl_xor_sync(full, mb, 2));
+        float w = m > -INFINITY ? s * ex2(m - mb) : 0.f;
+        w += __shfl_xor_sync(full, w, 1);
+        w += __shfl_xor_sync(full, w, 2);
+        if ((lane & 3) == 0)
+          S[(col0 / 4 + jb) * bstride + (kChunkRows / 4) * c + r / 4] = mb > -INFINITY ? mb + lg2(w) : -INFINITY;
+      }
     }
   }
-  if (!__syncthreads_and(ok)) {
-    // gave up: let the copies already issued land before the CTA ends. Thread 0
-    // issued them all; the last two chunks are the latest phase of each slot.
-    if (tid == 0) {
-      mbar_wait_drain(bar_q, 0, kWaitLimitNs);
-      for (int c = max(0, issued - 2); c < issued; ++c)
-        mbar_wait_drain(bar_k0 + 8 * (c & 1), (c >> 1) & 1, kWaitLimitNs);
-    }
-    return;
+  // every product and score is done; the K ring is idle and holds the histograms
+  ok = __syncthreads_and(ok);
+  if (ok && warp < kEpiWarps) {
+    // key blocks T .. n_chunks * 32 - 1 hold only empty sub-blocks and scored
+    // -inf above, as the counting select requires of a row's padding
+    for (int rq = warp; rq < R; rq += kEpiWarps)
+      if (q0 + rq < T)
+        warp_select_topk_count(S + rq * bstride, T, n_chunks * (kChunkRows / 4), k, hist + warp * kBins,
+                               tile_index + (static_cast<size_t>(bh) * cap.T + q0 + rq) * cap.k, lane);
   }
-
-  // Key blocks T .. n_chunks * CH / 4 - 1 hold only empty sub-blocks and
-  // scored -inf above, as the counting select requires of a row's padding.
-  for (int r = warp; r < R; r += kWarps)
-    if (q0 + r < T)
-      warp_select_topk_count(S + r * bstride, T, n_chunks * CH / 4, k, hist + warp * kBins,
-                             tile_index + (bh * cap.T + q0 + r) * static_cast<size_t>(cap.k), lane);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) tmem_dealloc(tbase, kTmemCols);
 }
 
 int sub_pad(int T) { return (4 * T + 127) / 128 * 128; }  // as subblock_rows_padded
 
-// chunk length for R query blocks per CTA: enough n-pairs to give each of the 16 warps a tile
-int chunk_for(int r) { return r == 16 ? 64 : 128; }
-
 size_t smem_for(int r, int spad) {
-  return 2 * static_cast<size_t>(chunk_for(r) / 8) * kTile8Bytes + static_cast<size_t>(r / 2) * kTile8Bytes +
-         static_cast<size_t>(r) * (spad / 4 + 4) * sizeof(float) + 4 * sizeof(uint64_t);
+  return 1024 + kOffS + static_cast<size_t>(r) * (spad / 4 + 4) * sizeof(float) + kTailBytes;
 }
 
 int pick_rows(int spad) {
-  for (int r = 16; r >= 4; r /= 2)
+  for (int r = 16; r >= 8; r /= 2)
     if (smem_for(r, spad) <= kSmemBudget) return r;
   return 0;
 }
 
-template <int R, int CH>
-cudaError_t launch_rows(const Geometry& g, const void* frag_q, const void* frag_k, int32_t* tile_index,
-                        unsigned int* err, const DeviceLengths& dl, size_t smem, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(subblock_router_kernel<R, CH>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+template <int R>
+cudaError_t launch_rows(const Geometry& g, const CUtensorMap (&maps)[4], int32_t* tile_index, unsigned int* err,
+                        const DeviceLengths& dl, size_t smem, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(subblock_router_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid((g.T + R - 1) / R, g.B * g.H);
-  subblock_router_kernel<R, CH><<<grid, kThreads, smem, stream>>>(static_cast<const uint4*>(frag_q),
-                                                                  static_cast<const uint4*>(frag_k), tile_index,
-                                                                  err, g, dl, sub_pad(g.T));
+  subblock_router_kernel<R><<<grid, kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], tile_index, err,
+                                                              g, dl, sub_pad(g.T));
   return cudaGetLastError();
 }
 
@@ -256,15 +303,13 @@ size_t subblock_router_smem_bytes(const Geometry& g, int* rows_per_cta) {
   return r ? smem_for(r, sub_pad(g.T)) : 0;
 }
 
-cudaError_t launch_subblock_router(const Geometry& g, const void* frag_q, const void* frag_k,
-                                   int32_t* tile_index, unsigned int* err, const DeviceLengths& dl,
-                                   cudaStream_t stream) {
+cudaError_t launch_subblock_router(const Geometry& g, const CUtensorMap (&maps)[4], int32_t* tile_index,
+                                   unsigned int* err, const DeviceLengths& dl, cudaStream_t stream) {
   int r = 0;
   const size_t smem = subblock_router_smem_bytes(g, &r);
   switch (r) {
-    case 16: return launch_rows<16, 64>(g, frag_q, frag_k, tile_index, err, dl, smem, stream);
-    case 8: return launch_rows<8, 128>(g, frag_q, frag_k, tile_index, err, dl, smem, stream);
-    case 4: return launch_rows<4, 128>(g, frag_q, frag_k, tile_index, err, dl, smem, stream);
+    case 16: return launch_rows<16>(g, maps, tile_index, err, dl, smem, stream);
+    case 8: return launch_rows<8>(g, maps, tile_index, err, dl, smem, stream);
     default: return cudaErrorInvalidValue;
   }
 }

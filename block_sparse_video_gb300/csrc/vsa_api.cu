@@ -55,6 +55,23 @@ bool encode_bnhd(CUtensorMap* map, const void* ptr, const vsa::Geometry& g) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map over `rows` bf16 rows of 128 channels per (batch, head), for B H
+// of them ({128, rows, B H, 1}); one box = 64 channels x 64 rows, 128-byte
+// swizzled. Rows past `rows` read as zeros.
+bool encode_rows(CUtensorMap* map, const void* ptr, int rows, int bh) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(vsa::kHeadDim), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(bh), 1};
+  const cuuint64_t row = static_cast<cuuint64_t>(vsa::kHeadDim) * 2;
+  const cuuint64_t strides[3] = {row, row * rows, row * rows * static_cast<cuuint64_t>(bh)};
+  const cuuint32_t box[4] = {64, 64, 1, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
@@ -392,7 +409,16 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
     if (vsa::launch_subpool(g, qb, kb, pq, pk, ws + plan->off_fq, ws + plan->off_fk, dl, st) != cudaSuccess)
       return VSA_ERR_CUDA;
     if ((rs = record(plan, 1, st)) != VSA_OK) return rs;
-    if (vsa::launch_subblock_router(g, ws + plan->off_fq, ws + plan->off_fk, idx, err, dl, st) != cudaSuccess)
+    // the sub-pool's bf16 rows: hi then lo, spad rows per (b, h), in each of the q and k buffers
+    const int spad = vsa::subblock_rows_padded(g);
+    const size_t lo_off = static_cast<size_t>(g.B) * g.H * spad * vsa::kHeadDim * 2;
+    CUtensorMap maps[4];
+    if (!encode_rows(&maps[0], ws + plan->off_fq, spad, g.B * g.H) ||
+        !encode_rows(&maps[1], ws + plan->off_fq + lo_off, spad, g.B * g.H) ||
+        !encode_rows(&maps[2], ws + plan->off_fk, spad, g.B * g.H) ||
+        !encode_rows(&maps[3], ws + plan->off_fk + lo_off, spad, g.B * g.H))
+      return VSA_ERR_CUDA;
+    if (vsa::launch_subblock_router(g, maps, idx, err, dl, st) != cudaSuccess)
       return VSA_ERR_CUDA;
   } else {
     NvtxRange r_sel("vsa_pool + vsa_coarse_topk");
