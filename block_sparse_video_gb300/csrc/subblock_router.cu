@@ -28,19 +28,21 @@
 //   L^T[128 key sub-rows x N query sub-rows] = K_chunk . Q^T     (M = 128)
 // so a TMEM lane holds one key sub-row and a column one query sub-row.
 //
-// Warp roles (320 threads):
-//   * warp 8 loads by TMA the CTA's query rows (hi and lo, once) and the key
+// Warp roles (E = N / 4 score warps, then two more):
+//   * warp E loads by TMA the CTA's query rows (hi and lo, once) and the key
 //     chunks (each chunk's hi rows, then its lo rows) through a 3-stage ring
 //     of 32 KB;
-//   * warp 9 owns TMEM (two accumulators of N columns, alternating by chunk)
-//     and issues the MMAs, converged with one elected lane;
-//   * warps 0-7 read each accumulator (warp w: TMEM lanes 32 (w % 4) .. + 31,
-//     columns of half w / 4) and fold it into block scores: per lane (one key
-//     sub-row) and query block, the log-sum-exp of its 4 query sub-rows
-//     weighted by the sub-blocks' token counts, in log2 units (ex2 and lg2 on
-//     the MUFU pipe, which ranks in the same order); then across the 4 lanes
-//     of the key block (lanes 4j .. 4j + 3), max and sum in two shuffle steps.
-// The same 8 warps then pick each row's top k with the coarse kernel's
+//   * warp E + 1 owns TMEM (two accumulators of N columns, alternating by
+//     chunk) and issues the MMAs, converged with one elected lane;
+//   * warps 0 .. E - 1 read each accumulator (warp w: TMEM lanes 32 (w % 4)
+//     .. + 31, the 16 columns of group w / 4: 4 query blocks) and fold it into
+//     block scores, in log2 units (ex2 and lg2 on the MUFU pipe, which ranks
+//     in the same order). Per query block, the 4 lanes of a key block (lanes
+//     4j .. 4j + 3, one key sub-row each) first agree on the maximum logit
+//     (two shuffle steps), then each sums 2^(x - max) over its 4 query
+//     sub-rows and the sums meet in two more shuffle steps: no branch, and
+//     an all-empty block (every x = -inf) ends at -inf.
+// The same warps then pick each row's top k with the coarse kernel's
 // selection: the counting threshold search, with the radix select where
 // scores tie at the cut. With device lengths the router scores the
 // request's tiles only and writes its selections at the plan's strides.
@@ -58,9 +60,6 @@ constexpr int kChunkRows = 128;                               // key sub-rows pe
 constexpr uint32_t kStageBytes = kChunkRows * kHeadDim * 2;   // a chunk's hi or lo rows: 32 KB
 constexpr int kStages = 3;
 constexpr uint32_t kQBytes = 64 * kHeadDim * 2;               // a 64-row box pair, hi or lo: 16 KB
-constexpr int kEpiWarps = 8;
-constexpr int kWarpTma = kEpiWarps, kWarpMma = kEpiWarps + 1;
-constexpr int kThreads = 32 * (kEpiWarps + 2);
 constexpr size_t kSmemBudget = 225 * 1024;
 constexpr unsigned int kDetailQ = 0x700, kDetailK = 0x710, kDetailKEmpty = 0x720, kDetailAcc = 0x730,
                        kDetailAccEmpty = 0x740;
@@ -72,7 +71,6 @@ constexpr uint32_t kOffS = kOffK + kStages * kStageBytes;
 constexpr int kBarQ = 0, kBarKFull = 1, kBarKEmpty = kBarKFull + kStages, kBarAccFull = kBarKEmpty + kStages,
               kBarAccEmpty = kBarAccFull + 2, kNumBars = kBarAccEmpty + 2;
 constexpr uint32_t kTailBytes = kNumBars * 8 + 16;
-static_assert(kEpiWarps * kBins * 4 <= kStages * kStageBytes, "selection histograms fit over the K ring");
 
 // log2(number of valid tokens of sub-block s), -inf for an empty one
 __device__ __forceinline__ float lg_count(int s, int Lv) {
@@ -93,15 +91,23 @@ __device__ __forceinline__ float lg2(float x) {
 }
 
 template <int R>
-__global__ void __launch_bounds__(kThreads, 1)
+__host__ __device__ constexpr int score_warps() { return R; }  // N / 4: one warp per 16 accumulator columns and lane quarter
+template <int R>
+__host__ __device__ constexpr int router_threads() { return 32 * (score_warps<R>() + 2); }
+
+template <int R>
+__global__ void __launch_bounds__(router_threads<R>(), 1)
 subblock_router_kernel(const __grid_constant__ CUtensorMap map_q_hi, const __grid_constant__ CUtensorMap map_q_lo,
                        const __grid_constant__ CUtensorMap map_k_hi, const __grid_constant__ CUtensorMap map_k_lo,
                        int32_t* __restrict__ tile_index, unsigned int* err, Geometry cap, DeviceLengths dl,
                        int spad) {
   constexpr int N = 4 * R;                             // query sub-rows per CTA: the MMA's N
-  constexpr int kCols = N / 2;                         // accumulator columns per epilogue thread
+  constexpr int kEpiWarps = score_warps<R>();
+  constexpr int kWarpTma = kEpiWarps, kWarpMma = kEpiWarps + 1;
+  constexpr int kCols = 16;                            // accumulator columns per score thread: 4 query blocks
   constexpr uint32_t kTmemCols = 2 * N < 32 ? 32 : 2 * N;
-  static_assert(kCols % 16 == 0 && N <= 64, "epilogue loads of 16 columns; query rows within one box");
+  static_assert(kEpiWarps * kCols == 4 * N && N <= 64, "16 columns per score warp; query rows within one box");
+  static_assert(kEpiWarps * kBins * 4 <= kStages * kStageBytes, "selection histograms fit over the K ring");
   // The request's tiles (the plan's own, or the device lengths'); the layouts
   // (sub-rows spad, selections [T_cap][k_cap]) are the plan's.
   const DynGeom dg = dyn_geom(cap, dl);
@@ -210,7 +216,7 @@ subblock_router_kernel(const __grid_constant__ CUtensorMap map_q_hi, const __gri
       if (ok) umma_commit_elect(bar(kBarAccFull + a));
     }
   } else {
-    // ------------------------------------------------------------ block scores (warps 0-7)
+    // ------------------------------------------------------------ block scores (warps 0 .. E - 1)
     const unsigned full = 0xffffffffu;
     const int quarter = warp % 4, col0 = (warp / 4) * kCols;
     const int r = 32 * quarter + lane;                 // key sub-row within a chunk (TMEM lane)
@@ -225,34 +231,28 @@ subblock_router_kernel(const __grid_constant__ CUtensorMap map_q_hi, const __gri
       if (!ok) break;
       tc_fence_after();
       uint32_t v[kCols];
-#pragma unroll
-      for (int j = 0; j < kCols; j += 16)
-        tmem_ld16(taddr + static_cast<uint32_t>(a * N + j), *reinterpret_cast<uint32_t(*)[16]>(v + j));
+      tmem_ld16(taddr + static_cast<uint32_t>(a * N), v);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarAccEmpty + a));  // the MMAs of chunk c + 2 may overwrite it
+      // logit x = acc / sqrt(128) + log2 n_q + log2 n_k, in log2 units; the key
+      // sub-row's count is added to the maximum, not to every element
       const float lk = lg_count(kChunkRows * c + r, Lv);
+      float* srow = S + (col0 / 4) * bstride + (kChunkRows / 4) * c + r / 4;
 #pragma unroll
       for (int jb = 0; jb < kCols / 4; ++jb) {
-        float x[4], m = -INFINITY;
+        float x[4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          x[t] = fmaf(__uint_as_float(v[4 * jb + t]), scale_log2, lq[4 * jb + t] + lk);
-          m = fmaxf(m, x[t]);
-        }
-        float s = 0.f;
-        if (m > -INFINITY) {
-#pragma unroll
-          for (int t = 0; t < 4; ++t) s += ex2(x[t] - m);
-        }
-        float mb = fmaxf(m, __shfl_xor_sync(full, m, 1));
+        for (int t = 0; t < 4; ++t) x[t] = fmaf(__uint_as_float(v[4 * jb + t]), scale_log2, lq[4 * jb + t]);
+        float mb = fmax3(x[0], x[1], fmaxf(x[2], x[3])) + lk;
+        mb = fmaxf(mb, __shfl_xor_sync(full, mb, 1));
         mb = fmaxf(mb, __shfl_xor_sync(full, mb, 2));
-        float w = m > -INFINITY ? s * ex2(m - mb) : 0.f;
+        const float off = (mb > -INFINITY ? mb : 0.f) - lk;   // an all-empty block: 2^-inf = 0 below
+        float w = (ex2(x[0] - off) + ex2(x[1] - off)) + (ex2(x[2] - off) + ex2(x[3] - off));
         w += __shfl_xor_sync(full, w, 1);
         w += __shfl_xor_sync(full, w, 2);
-        if ((lane & 3) == 0)
-          S[(col0 / 4 + jb) * bstride + (kChunkRows / 4) * c + r / 4] = mb > -INFINITY ? mb + lg2(w) : -INFINITY;
+        if ((lane & 3) == 0) srow[jb * bstride] = (mb > -INFINITY ? mb : 0.f) + lg2(w);
       }
     }
   }
@@ -290,7 +290,7 @@ cudaError_t launch_rows(const Geometry& g, const CUtensorMap (&maps)[4], int32_t
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid((g.T + R - 1) / R, g.B * g.H);
-  subblock_router_kernel<R><<<grid, kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], tile_index, err,
+  subblock_router_kernel<R><<<grid, router_threads<R>(), smem, stream>>>(maps[0], maps[1], maps[2], maps[3], tile_index, err,
                                                               g, dl, sub_pad(g.T));
   return cudaGetLastError();
 }
