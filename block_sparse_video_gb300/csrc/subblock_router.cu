@@ -29,11 +29,12 @@
 // so a TMEM lane holds one key sub-row and a column one query sub-row.
 //
 // Warp roles (E = N / 4 score warps, then two more):
-//   * warp E loads by TMA the CTA's query rows (hi and lo, once) and the key
-//     chunks (each chunk's hi rows, then its lo rows) through a 3-stage ring
-//     of 32 KB;
-//   * warp E + 1 owns TMEM (two accumulators of N columns, alternating by
-//     chunk) and issues the MMAs, converged with one elected lane;
+//   * warp E loads by TMA (four issuing lanes, one 8 KB box each) the CTA's
+//     query rows (hi and lo, once) and the key chunks (each chunk's hi rows,
+//     then its lo rows) through a 3-stage ring of 32 KB;
+//   * warp E + 1 owns TMEM (four accumulators of N columns, taken by chunk
+//     in turn, so the products run up to three chunks ahead of the scores)
+//     and issues the MMAs, converged with one elected lane;
 //   * warps 0 .. E - 1 read each accumulator (warp w: TMEM lanes 32 (w % 4)
 //     .. + 31, the 16 columns of group w / 4: 4 query blocks) and fold it into
 //     block scores, in log2 units (ex2 and lg2 on the MUFU pipe, which ranks
@@ -59,6 +60,7 @@ constexpr int kSub = 16;                                      // tokens per sub-
 constexpr int kChunkRows = 128;                               // key sub-rows per chunk: the MMA's M
 constexpr uint32_t kStageBytes = kChunkRows * kHeadDim * 2;   // a chunk's hi or lo rows: 32 KB
 constexpr int kStages = 3;
+constexpr int kAcc = 4;                                       // TMEM accumulators, by chunk
 constexpr uint32_t kQBytes = 64 * kHeadDim * 2;               // a 64-row box pair, hi or lo: 16 KB
 constexpr size_t kSmemBudget = 225 * 1024;
 constexpr unsigned int kDetailQ = 0x700, kDetailK = 0x710, kDetailKEmpty = 0x720, kDetailAcc = 0x730,
@@ -69,7 +71,7 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + 2 * kQBytes;
 constexpr uint32_t kOffS = kOffK + kStages * kStageBytes;
 constexpr int kBarQ = 0, kBarKFull = 1, kBarKEmpty = kBarKFull + kStages, kBarAccFull = kBarKEmpty + kStages,
-              kBarAccEmpty = kBarAccFull + 2, kNumBars = kBarAccEmpty + 2;
+              kBarAccEmpty = kBarAccFull + kAcc, kNumBars = kBarAccEmpty + kAcc;
 constexpr uint32_t kTailBytes = kNumBars * 8 + 16;
 
 // log2(number of valid tokens of sub-block s), -inf for an empty one
@@ -105,7 +107,8 @@ subblock_router_kernel(const __grid_constant__ CUtensorMap map_q_hi, const __gri
   constexpr int kEpiWarps = score_warps<R>();
   constexpr int kWarpTma = kEpiWarps, kWarpMma = kEpiWarps + 1;
   constexpr int kCols = 16;                            // accumulator columns per score thread: 4 query blocks
-  constexpr uint32_t kTmemCols = 2 * N < 32 ? 32 : 2 * N;
+  constexpr uint32_t kTmemCols = kAcc * N < 32 ? 32 : kAcc * N;
+  static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "TMEM allocation");
   static_assert(kEpiWarps * kCols == 4 * N && N <= 64, "16 columns per score warp; query rows within one box");
   static_assert(kEpiWarps * kBins * 4 <= kStages * kStageBytes, "selection histograms fit over the K ring");
   // The request's tiles (the plan's own, or the device lengths'); the layouts
@@ -138,7 +141,7 @@ subblock_router_kernel(const __grid_constant__ CUtensorMap map_q_hi, const __gri
       mbar_init(bar(kBarKFull + s), 1);
       mbar_init(bar(kBarKEmpty + s), 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kAcc; ++a) {
       mbar_init(bar(kBarAccFull + a), 1);
       mbar_init(bar(kBarAccEmpty + a), kEpiWarps);
     }
@@ -152,14 +155,20 @@ subblock_router_kernel(const __grid_constant__ CUtensorMap map_q_hi, const __gri
   bool ok = true;
 
   if (warp == kWarpTma) {
-    // ------------------------------------------------------------ TMA loads (one lane)
-    if (lane == 0) {
+    // ------------------------------------------------------------ TMA loads (lanes 0-3)
+    // Each of lanes 0-3 issues one 8 KB box of every stage (channel half
+    // lane >> 1, row group lane & 1): one issuing thread keeps too few bytes
+    // in flight to feed the products. Each lane waits for the stage itself;
+    // lane 0 arms the full barrier. A box may land before the arming: the
+    // transaction count may run negative until the arrive, and the phase
+    // cannot complete before it.
+    if (lane < 4) {
+      const int half = lane >> 1, rg = lane & 1;
       int issued = 0;  // K stages issued
-      mbar_arrive_expect_tx(bar(kBarQ), 2 * kQBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int half = 0; half < 2; ++half)
-          tma_load_4d(sbase + kOffQ + t * kQBytes + half * 8192, t ? &map_q_lo : &map_q_hi, 64 * half, 4 * q0, bh, 0,
-                      bar(kBarQ));
+      if (lane == 0) mbar_arrive_expect_tx(bar(kBarQ), 2 * kQBytes);
+      // Q: lane l loads channel half l & 1 of the hi (l < 2) or lo rows
+      tma_load_4d(sbase + kOffQ + (lane >> 1) * kQBytes + (lane & 1) * 8192, (lane >> 1) ? &map_q_lo : &map_q_hi,
+                  64 * (lane & 1), 4 * q0, bh, 0, bar(kBarQ));
       for (int i = 0; i < 2 * n_chunks; ++i) {
         const int st = i % kStages;
         // the stage's previous use (stage i - kStages) must have been read by its MMAs
@@ -167,13 +176,10 @@ subblock_router_kernel(const __grid_constant__ CUtensorMap map_q_hi, const __gri
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(bar(kBarKFull + st), kStageBytes);
+        if (lane == 0) mbar_arrive_expect_tx(bar(kBarKFull + st), kStageBytes);
         const CUtensorMap* m = (i & 1) ? &map_k_lo : &map_k_hi;
-        const int row0 = kChunkRows * (i / 2);
-        for (int half = 0; half < 2; ++half)
-          for (int rg = 0; rg < 2; ++rg)
-            tma_load_4d(sbase + kOffK + st * kStageBytes + half * 16384 + rg * 8192, m, 64 * half, row0 + 64 * rg,
-                        bh, 0, bar(kBarKFull + st));
+        tma_load_4d(sbase + kOffK + st * kStageBytes + half * 16384 + rg * 8192, m, 64 * half,
+                    kChunkRows * (i / 2) + 64 * rg, bh, 0, bar(kBarKFull + st));
         issued = i + 1;
       }
       if (!ok) {
@@ -190,9 +196,9 @@ subblock_router_kernel(const __grid_constant__ CUtensorMap map_q_hi, const __gri
     const uint64_t dq_lo = smem_desc_sw128(sbase + kOffQ + kQBytes, 16, 1024);
     ok = mbar_wait_warp(bar(kBarQ), 0, err, kDetailQ);
     for (int c = 0; c < n_chunks && ok; ++c) {
-      const int a = c & 1;
-      // accumulator a was last read by the epilogue of chunk c - 2
-      if (c >= 2) ok = mbar_wait_warp(bar(kBarAccEmpty + a), ((c / 2) - 1) & 1, err, kDetailAccEmpty);
+      const int a = c % kAcc;
+      // accumulator a was last read by the epilogue of chunk c - kAcc
+      if (c >= kAcc) ok = mbar_wait_warp(bar(kBarAccEmpty + a), ((c / kAcc) - 1) & 1, err, kDetailAccEmpty);
       const uint32_t d = tbase + static_cast<uint32_t>(a * N);
       for (int part = 0; part < 2 && ok; ++part) {  // the chunk's hi rows, then its lo rows
         const int i = 2 * c + part, st = i % kStages;
@@ -226,8 +232,8 @@ subblock_router_kernel(const __grid_constant__ CUtensorMap map_q_hi, const __gri
 #pragma unroll
     for (int j = 0; j < kCols; ++j) lq[j] = lg_count(4 * q0 + col0 + j, Lv);
     for (int c = 0; c < n_chunks && ok; ++c) {
-      const int a = c & 1;
-      ok = mbar_wait_warp(bar(kBarAccFull + a), (c / 2) & 1, err, kDetailAcc);
+      const int a = c % kAcc;
+      ok = mbar_wait_warp(bar(kBarAccFull + a), (c / kAcc) & 1, err, kDetailAcc);
       if (!ok) break;
       tc_fence_after();
       uint32_t v[kCols];
@@ -235,7 +241,7 @@ subblock_router_kernel(const __grid_constant__ CUtensorMap map_q_hi, const __gri
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarAccEmpty + a));  // the MMAs of chunk c + 2 may overwrite it
+      if (lane == 0) mbar_arrive(bar(kBarAccEmpty + a));  // the MMAs of chunk c + kAcc may overwrite it
       // logit x = acc / sqrt(128) + log2 n_q + log2 n_k, in log2 units; the key
       // sub-row's count is added to the maximum, not to every element
       const float lk = lg_count(kChunkRows * c + r, Lv);
