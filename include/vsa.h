@@ -120,7 +120,7 @@ vsa_status_t vsa_plan_info(vsa_plan_t plan, int64_t* n_tiles, int64_t* k, size_t
  *                   coarse output and the error words; contents on entry are
  *                   ignored (the forward clears what must start at zero)
  *   stream        : cudaStream_t to launch on (NULL = legacy default stream)
- * Enqueues five kernels (tile pool; the pooled V in tensor-core fragment form;
+ * Enqueues five kernels (tile pool; the pooled K and V in tensor-core fragment form;
  * coarse attention + top-k; fine attention with the gated combination fused
  * into its epilogue; the fine attention's exact pass over the query tiles whose
  * fast pass left its numeric range, which returns at once when there are none)
