@@ -22,6 +22,7 @@ pytestmark = pytest.mark.gpu
 
 CAP = (2, 3, 130, 70, 64 * 12 + 30)   # batch, heads, text, audio, video
 KEEP = 0.25
+SPARSITY = 0.6
 REQUESTS = [
     (100, 50, 64 * 9 + 5),     # ragged prefix and ragged last tile
     (0, 0, 64 * 5),            # no prefix
@@ -144,19 +145,25 @@ def test_page_requests_in_the_10s_capacity_buffer(cuda_ok):
         torch.cuda.empty_cache()
 
 
-def test_serving_step_in_one_graph(cuda_ok):
+@pytest.mark.parametrize("subblock", [False, True])
+def test_serving_step_in_one_graph(cuda_ok, subblock):
     """The serving step of one layer replayed from a single captured graph for
     requests of different lengths (device-side lengths throughout):
       1. vsa_preprocess packs and normalises the request from a capacity-padded
          projection buffer through its row map;
-      2. vsa_forward_ex attends over the packed tensors;
+      2. vsa_forward_ex attends over the packed tensors (VSA selection, or the
+         SubBlock router with no gate);
       3. it writes each combined row back to its sequence position, the output
          all-to-all's send layout.
     Each replay equals the same chain on an exact-shape plan, bit for bit."""
     from block_sparse_video_gb300.synthetic import make_norm_weights, make_projections, make_rope_tables, make_row_map
     b, h = 1, 4
     cap_lt, cap_la, cap_lv = 100, 60, 64 * 12 + 5
-    cap = bsv.VSA(b, h, cap_lt, cap_la, cap_lv, KEEP)
+
+    def plan(lt, la, lv):
+        return bsv.SubBlock(b, h, lt, la, lv, SPARSITY) if subblock else bsv.VSA(b, h, lt, la, lv, KEEP)
+
+    cap = plan(cap_lt, cap_la, cap_lv)
     n_cap = cap.seq
     rows_in = n_cap + 64
     proj = torch.zeros((b, rows_in, 4, h, 128), dtype=torch.bfloat16, device="cuda")
@@ -171,7 +178,8 @@ def test_serving_step_in_one_graph(cuda_ok):
 
     def step():
         cap.preprocess(*ins, wq, wk, cos, sin, 96, True, 1e-6, src, out=packed, lengths=lengths)
-        cap.forward_ex(*packed, out=send, out_row_map=src, lengths=lengths, preprocessed=True)
+        cap.forward_ex(*packed[:3], None if subblock else packed[3], out=send, out_row_map=src, lengths=lengths,
+                       preprocessed=True)
 
     step()
     cap.check()
@@ -191,17 +199,15 @@ def test_serving_step_in_one_graph(cuda_ok):
         torch.cuda.synchronize()
         cap.check()
         # the exact-shape chain on the same data
-        ex = bsv.VSA(b, h, lt, la, lv, KEEP)
+        ex = plan(lt, la, lv)
         ex_send = torch.full_like(send, float("nan"))
         ex_src = src[:, :n].contiguous()
         pk = ex.preprocess(*ins, wq, wk, cos[:n].contiguous(), sin[:n].contiguous(), 96, True, 1e-6, ex_src)
-        ex.forward_rows(*pk, ex_send, ex_src, preprocessed=True)
+        ex.forward_rows(*pk[:3], None if subblock else pk[3], ex_send, ex_src, preprocessed=True)
         ex.check()
         assert torch.equal(_bits(send), _bits(ex_send)), (lt, la, lv)
         assert torch.isnan(send.float()).sum() == (rows_in - n) * h * 128 * b
 
-
-SPARSITY = 0.6
 
 
 def _exact_subblock(b, h, lt, la, lv, seed):
