@@ -140,17 +140,6 @@ struct FineArgs {
   int* work_counters;  // 2 counters, zero before the launch
   DeviceLengths dl;
 };
-// Row gather from device-accessible (pinned) host memory into packed device
-// rows, for up to four tensors in one launch.
-struct HostGather {
-  const uint8_t* src[4];  // device-side addresses of host memory
-  uint8_t* dst[4];        // device memory, rows packed at `width` bytes
-  size_t src_pitch = 0;   // bytes between consecutive source rows
-  size_t width = 0;       // bytes per row
-  size_t rows = 0;
-  int tensors = 0;
-};
-cudaError_t launch_gather_host_rows(const HostGather& a, int num_sms, cudaStream_t stream);
 
 size_t fine_smem_bytes();
 cudaError_t launch_fine(const Geometry& g, const CUtensorMap& map_q, const CUtensorMap& map_k,

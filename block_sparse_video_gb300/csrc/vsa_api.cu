@@ -11,6 +11,7 @@
 #include "kernels.cuh"
 #include "vsa.h"
 
+#include "host_rows.cuh"
 #include "plan.h"
 
 namespace {
@@ -646,8 +647,9 @@ vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, con
   // host row) are copied in on s_in, its forward runs on the caller's stream,
   // and its output is copied out on s_out, two groups' buffers alternating.
   // The first group's rows are gathered by a kernel reading the host memory
-  // when every input is pinned; the rest go through strided copies that hide
-  // under the previous group's forward.
+  // when every input is pinned, and the last group's output is written by a
+  // kernel when `out` is pinned; the rest go through strided copies that hide
+  // under the neighbouring groups' forwards.
   vsa_status_t rs = ensure_streams(pipe);
   if (rs != VSA_OK) return rs;
   if (plan->num_sms == 0 &&
@@ -666,6 +668,8 @@ vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, con
     dev_in[i] = device_view_of_host(hin[i]);
     gather_first = dev_in[i] && reinterpret_cast<uintptr_t>(dev_in[i]) % 16 == 0;
   }
+  uint8_t* dev_out = const_cast<uint8_t*>(device_view_of_host(out));
+  const bool scatter_last = dev_out && reinterpret_cast<uintptr_t>(dev_out) % 16 == 0;
   auto cuda = [](cudaError_t e) { return e == cudaSuccess; };
   if (!cuda(cudaEventRecord(pipe->entry, st)) || !cuda(cudaStreamWaitEvent(pipe->s_in, pipe->entry, 0)))
     return VSA_ERR_CUDA;
@@ -680,16 +684,17 @@ vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, con
     // inputs: slot s is free once the forward of group gi - 2 has read it
     if (gi >= 2 && !cuda(cudaStreamWaitEvent(pipe->s_in, pipe->fwd_done[s], 0))) return VSA_ERR_CUDA;
     if (gi == 0 && gather_first) {
-      vsa::HostGather a{};
+      vsa::HostRows a{};
       for (int i = 0; i < n_in; ++i) {
         a.src[i] = dev_in[i] + h0 * 256;
         a.dst[i] = base + i * tslot;
       }
       a.src_pitch = host_pitch;
+      a.dst_pitch = width;
       a.width = width;
       a.rows = rows;
       a.tensors = n_in;
-      if (!cuda(vsa::launch_gather_host_rows(a, plan->num_sms, pipe->s_in))) return VSA_ERR_CUDA;
+      if (!cuda(vsa::launch_copy_host_rows(a, plan->num_sms, pipe->s_in))) return VSA_ERR_CUDA;
     } else {
       for (int i = 0; i < n_in; ++i)
         if (!cuda(cudaMemcpy2DAsync(base + i * tslot, width, static_cast<const uint8_t*>(hin[i]) + h0 * 256,
@@ -704,12 +709,23 @@ vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, con
                      base + 4 * tslot, ws, ws_bytes, stream);
     if (rs != VSA_OK) return rs;
     if (!cuda(cudaEventRecord(pipe->fwd_done[s], st))) return VSA_ERR_CUDA;
-    // output
-    if (!cuda(cudaStreamWaitEvent(pipe->s_out, pipe->fwd_done[s], 0)) ||
-        !cuda(cudaMemcpy2DAsync(static_cast<uint8_t*>(out) + h0 * 256, host_pitch, base + 4 * tslot, width, width,
-                                rows, cudaMemcpyDeviceToHost, pipe->s_out)) ||
-        !cuda(cudaEventRecord(pipe->out_done[s], pipe->s_out)))
+    // output; the last group's, which nothing hides, is written by a kernel when `out` is pinned
+    if (!cuda(cudaStreamWaitEvent(pipe->s_out, pipe->fwd_done[s], 0))) return VSA_ERR_CUDA;
+    if (gi == groups - 1 && scatter_last) {
+      vsa::HostRows a{};
+      a.src[0] = base + 4 * tslot;
+      a.dst[0] = dev_out + h0 * 256;
+      a.src_pitch = width;
+      a.dst_pitch = host_pitch;
+      a.width = width;
+      a.rows = rows;
+      a.tensors = 1;
+      if (!cuda(vsa::launch_copy_host_rows(a, plan->num_sms, pipe->s_out))) return VSA_ERR_CUDA;
+    } else if (!cuda(cudaMemcpy2DAsync(static_cast<uint8_t*>(out) + h0 * 256, host_pitch, base + 4 * tslot, width,
+                                       width, rows, cudaMemcpyDeviceToHost, pipe->s_out))) {
       return VSA_ERR_CUDA;
+    }
+    if (!cuda(cudaEventRecord(pipe->out_done[s], pipe->s_out))) return VSA_ERR_CUDA;
   }
   for (int s = 0; s < 2 && s < groups; ++s)
     if (!cuda(cudaStreamWaitEvent(st, pipe->out_done[s], 0))) return VSA_ERR_CUDA;

@@ -319,7 +319,8 @@ vsa_status_t vsa_forward_ex(vsa_plan_t plan, const vsa_forward_args_t* args, voi
  *     registered host memory, the first group's slices are instead gathered by
  *     a kernel that reads the host memory directly;
  *   * the group's forward runs on `stream`;
- *   * its output is copied out on a second library-owned stream;
+ *   * its output is copied out on a second library-owned stream (the last
+ *     group's, when out is pinned, by a kernel writing the host memory);
  *   * two groups' device buffers alternate.
  * The results equal vsa_forward's bit for bit. The two streams and their
  * events are created on the first call and released by vsa_plan_destroy.
