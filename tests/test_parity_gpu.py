@@ -127,15 +127,16 @@ def test_deterministic(cuda_ok):
 
 @pytest.mark.parametrize("heads,subblock,pinned", [(2, False, True), (11, False, True), (11, True, True),
                                                     (1, False, True), (24, False, True), (24, False, False),
-                                                    (11, True, False)])
+                                                    (11, True, False), (24, False, "inputs")])
 def test_host_buffer_path_matches_device_path(cuda_ok, heads, subblock, pinned):
     """The host-buffer path copies head groups in, runs each group's forward and
     copies it out, pipelined. Group widths ramp up and end on two heads: 11
     heads run as groups of 4, 6 and 1; 24 heads as 4, 6, 8, 4 and 2; 2 heads as
-    two of one. With pinned
-    inputs the first group is gathered by a kernel reading host memory, with
-    pageable ones by strided copies. Every head's result must equal the device
-    path bit for bit."""
+    two of one. With pinned inputs the first group is gathered by a kernel
+    reading host memory, and with a pinned output the last group is written by
+    a kernel; pageable buffers (all of them, or the output alone) go through
+    strided copies. Every head's result must equal the device path bit for
+    bit."""
     lt, la, lv = 64, 37, 1000
     q, k, v, g = make_inputs(1, heads, lt, la, lv, 0, device="cuda")
     op = bsv.SubBlock(1, heads, lt, la, lv, 0.6) if subblock else bsv.VSA(1, heads, lt, la, lv, 0.2)
@@ -145,7 +146,8 @@ def test_host_buffer_path_matches_device_path(cuda_ok, heads, subblock, pinned):
     hout = torch.full_like(host[0], float("nan"))
     if pinned:
         host = [x.pin_memory() for x in host]
-        hout = hout.pin_memory()
+        if pinned is True:
+            hout = hout.pin_memory()
     hq, hk, hv, hg = host
     buf = torch.empty(bsv.vsa_plan_host_path_bytes(op.plan), dtype=torch.uint8, device="cuda")
     for _ in range(2):  # the second call reuses the pipeline's streams and events
