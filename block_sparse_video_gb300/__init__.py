@@ -4,8 +4,8 @@ Thin Python binding over the C ABI in ``include/vsa.h`` (``libvsa.so``, built
 in-tree by ``block_sparse_video_gb300.build``). The functions keep the C names
 and only marshal arguments: torch tensors are used for device memory and
 streams; every step of the computation runs in the library's CUDA kernels.
-If the library has not been built, importing the binding raises: there is no
-fallback path.
+If the library has not been built, the first call into it raises: there is
+no fallback path.
 """
 from __future__ import annotations
 
