@@ -32,11 +32,14 @@
 //   * warp E loads by TMA (four issuing lanes, one 8 KB box each) the CTA's
 //     query rows (hi and lo, once) and the key chunks (each chunk's hi rows,
 //     then its lo rows) through a 3-stage ring of 32 KB;
-//   * warp E + 1 owns TMEM (four accumulators of N columns, taken by chunk
-//     in turn, so the products run up to three chunks ahead of the scores)
-//     and issues the MMAs, converged with one elected lane;
-//   * warps 0 .. E - 1 read each accumulator (warp w: TMEM lanes 32 (w % 4)
-//     .. + 31, the 16 columns of group w / 4: 4 query blocks) and fold it into
+//   * warps E + 1 and E + 2 issue the MMAs, converged with one elected lane
+//     each: every chunk's 24 products split between them, each into its own
+//     accumulator of N columns (two interleaving issuers keep the tensor pipe
+//     busy where one leaves it idle between N = 64 MMAs); warp E + 1 owns TMEM
+//     (two such accumulator pairs, taken by chunk in turn);
+//   * warps 0 .. E - 1 read each accumulator pair (warp w: TMEM lanes 32 (w %
+//     4) .. + 31, the 16 columns of group w / 4: 4 query blocks), add its two
+//     halves and fold them into
 //     block scores, in log2 units (ex2 and lg2 on the MUFU pipe, which ranks
 //     in the same order). Per query block, the 4 lanes of a key block (lanes
 //     4j .. 4j + 3, one key sub-row each) first agree on the maximum logit
@@ -60,7 +63,7 @@ constexpr int kSub = 16;                                      // tokens per sub-
 constexpr int kChunkRows = 128;                               // key sub-rows per chunk: the MMA's M
 constexpr uint32_t kStageBytes = kChunkRows * kHeadDim * 2;   // a chunk's hi or lo rows: 32 KB
 constexpr int kStages = 3;
-constexpr int kAcc = 4;                                       // TMEM accumulators, by chunk
+constexpr int kAcc = 2;                                       // TMEM accumulator pairs, by chunk
 constexpr uint32_t kQBytes = 64 * kHeadDim * 2;               // a 64-row box pair, hi or lo: 16 KB
 constexpr size_t kSmemBudget = 225 * 1024;
 constexpr unsigned int kDetailQ = 0x700, kDetailK = 0x710, kDetailKEmpty = 0x720, kDetailAcc = 0x730,
@@ -95,7 +98,7 @@ __device__ __forceinline__ float lg2(float x) {
 template <int R>
 __host__ __device__ constexpr int score_warps() { return R; }  // N / 4: one warp per 16 accumulator columns and lane quarter
 template <int R>
-__host__ __device__ constexpr int router_threads() { return 32 * (score_warps<R>() + 2); }
+__host__ __device__ constexpr int router_threads() { return 32 * (score_warps<R>() + 3); }
 
 template <int R>
 __global__ void __launch_bounds__(router_threads<R>(), 1)
@@ -105,9 +108,9 @@ subblock_router_kernel(const __grid_constant__ CUtensorMap map_q_hi, const __gri
                        int spad) {
   constexpr int N = 4 * R;                             // query sub-rows per CTA: the MMA's N
   constexpr int kEpiWarps = score_warps<R>();
-  constexpr int kWarpTma = kEpiWarps, kWarpMma = kEpiWarps + 1;
+  constexpr int kWarpTma = kEpiWarps, kWarpMma = kEpiWarps + 1;  // MMA issuers: kWarpMma and kWarpMma + 1
   constexpr int kCols = 16;                            // accumulator columns per score thread: 4 query blocks
-  constexpr uint32_t kTmemCols = kAcc * N < 32 ? 32 : kAcc * N;
+  constexpr uint32_t kTmemCols = 2 * kAcc * N < 32 ? 32 : 2 * kAcc * N;  // per chunk: one accumulator per issuer
   static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "TMEM allocation");
   static_assert(kEpiWarps * kCols == 4 * N && N <= 64, "16 columns per score warp; query rows within one box");
   static_assert(kEpiWarps * kBins * 4 <= kStages * kStageBytes, "selection histograms fit over the K ring");
@@ -139,10 +142,10 @@ subblock_router_kernel(const __grid_constant__ CUtensorMap map_q_hi, const __gri
     mbar_init(bar(kBarQ), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarKFull + s), 1);
-      mbar_init(bar(kBarKEmpty + s), 1);
+      mbar_init(bar(kBarKEmpty + s), 2);  // both MMA issuers read every stage
     }
     for (int a = 0; a < kAcc; ++a) {
-      mbar_init(bar(kBarAccFull + a), 1);
+      mbar_init(bar(kBarAccFull + a), 2);  // one commit per issuer
       mbar_init(bar(kBarAccEmpty + a), kEpiWarps);
     }
     fence_barrier_init();
@@ -189,35 +192,47 @@ subblock_router_kernel(const __grid_constant__ CUtensorMap map_q_hi, const __gri
           mbar_wait_drain(bar(kBarKFull + i % kStages), (i / kStages) & 1, kWaitLimitNs);
       }
     }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issue (converged warp)
+  } else if (warp == kWarpMma || warp == kWarpMma + 1) {
+    // ------------------------------------------------------------ MMA issue (two converged warps)
+    // The chunk's 24 products split over two issuing warps, each into its own
+    // accumulator of the pair (the score warps add the two): a single issuer
+    // leaves the tensor pipe idle between its N = 64 MMAs, two interleave.
+    //   issuer 0: hi . hi over k-steps 0-7, then lo . hi over k-steps 0-3;
+    //   issuer 1: hi . lo over k-steps 0-7, then lo . hi over k-steps 4-7.
+    const int w = warp - kWarpMma;
     const uint32_t idesc = idesc_bf16_f32(128, N, 0, 0);
     const uint64_t dq_hi = smem_desc_sw128(sbase + kOffQ, 16, 1024);
     const uint64_t dq_lo = smem_desc_sw128(sbase + kOffQ + kQBytes, 16, 1024);
+    const uint64_t dq_b = w == 0 ? dq_hi : dq_lo;  // the B rows of this issuer's hi-stage products
     ok = mbar_wait_warp(bar(kBarQ), 0, err, kDetailQ);
     for (int c = 0; c < n_chunks && ok; ++c) {
       const int a = c % kAcc;
-      // accumulator a was last read by the epilogue of chunk c - kAcc
+      // accumulator pair a was last read by the epilogue of chunk c - kAcc
       if (c >= kAcc) ok = mbar_wait_warp(bar(kBarAccEmpty + a), ((c / kAcc) - 1) & 1, err, kDetailAccEmpty);
-      const uint32_t d = tbase + static_cast<uint32_t>(a * N);
+      const uint32_t d = tbase + static_cast<uint32_t>((2 * a + w) * N);
       for (int part = 0; part < 2 && ok; ++part) {  // the chunk's hi rows, then its lo rows
         const int i = 2 * c + part, st = i % kStages;
         ok = mbar_wait_warp(bar(kBarKFull + st), (i / kStages) & 1, err, kDetailK);
         if (!ok) break;
         tc_fence_after();
         const uint64_t dk = smem_desc_sw128(sbase + kOffK + st * kStageBytes, 16, 1024);
+        if (part == 0) {
 #pragma unroll
-        for (int s = 0; s < kHeadDim / 16; ++s) {
-          const uint32_t koff = ((s >> 2) * 16384 + (s & 3) * 32) >> 4;
-          const uint32_t qoff = ((s >> 2) * 8192 + (s & 3) * 32) >> 4;
-          if (part == 0) {
-            umma_bf16_elect(d, dk + koff, dq_hi + qoff, idesc, s > 0 ? 1u : 0u);  // hi . hi
-            umma_bf16_elect(d, dk + koff, dq_lo + qoff, idesc, 1u);               // hi . lo
-          } else {
-            umma_bf16_elect(d, dk + koff, dq_hi + qoff, idesc, 1u);               // lo . hi
+          for (int s = 0; s < kHeadDim / 16; ++s) {
+            const uint32_t koff = ((s >> 2) * 16384 + (s & 3) * 32) >> 4;
+            const uint32_t qoff = ((s >> 2) * 8192 + (s & 3) * 32) >> 4;
+            umma_bf16_elect(d, dk + koff, dq_b + qoff, idesc, s > 0 ? 1u : 0u);  // hi . hi or hi . lo
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < kHeadDim / 32; ++j) {
+            const int s = 4 * w + j;
+            const uint32_t koff = ((s >> 2) * 16384 + (s & 3) * 32) >> 4;
+            const uint32_t qoff = ((s >> 2) * 8192 + (s & 3) * 32) >> 4;
+            umma_bf16_elect(d, dk + koff, dq_hi + qoff, idesc, 1u);  // lo . hi, half of the k-steps
           }
         }
-        umma_commit_elect(bar(kBarKEmpty + st));  // the stage may be refilled
+        umma_commit_elect(bar(kBarKEmpty + st));  // the stage may be refilled once both issuers are done
       }
       if (ok) umma_commit_elect(bar(kBarAccFull + a));
     }
@@ -236,8 +251,9 @@ subblock_router_kernel(const __grid_constant__ CUtensorMap map_q_hi, const __gri
       ok = mbar_wait_warp(bar(kBarAccFull + a), (c / kAcc) & 1, err, kDetailAcc);
       if (!ok) break;
       tc_fence_after();
-      uint32_t v[kCols];
-      tmem_ld16(taddr + static_cast<uint32_t>(a * N), v);
+      uint32_t v[kCols], v1[kCols];
+      tmem_ld16(taddr + static_cast<uint32_t>(2 * a * N), v);
+      tmem_ld16(taddr + static_cast<uint32_t>((2 * a + 1) * N), v1);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
@@ -250,7 +266,8 @@ subblock_router_kernel(const __grid_constant__ CUtensorMap map_q_hi, const __gri
       for (int jb = 0; jb < kCols / 4; ++jb) {
         float x[4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) x[t] = fmaf(__uint_as_float(v[4 * jb + t]), scale_log2, lq[4 * jb + t]);
+        for (int t = 0; t < 4; ++t)
+          x[t] = fmaf(__uint_as_float(v[4 * jb + t]) + __uint_as_float(v1[4 * jb + t]), scale_log2, lq[4 * jb + t]);
         float mb = fmax3(x[0], x[1], fmaxf(x[2], x[3])) + lk;
         mb = fmaxf(mb, __shfl_xor_sync(full, mb, 1));
         mb = fmaxf(mb, __shfl_xor_sync(full, mb, 2));
