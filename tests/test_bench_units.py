@@ -72,3 +72,16 @@ def test_subblock_counts_and_router_flops_10s():
         assert kk == k
         assert fine == 4 * D * H * (LV * (P + 64 * k) + P * (P + LV))
         assert router == 2 * D * H * (4 * T) ** 2   # every pair of 16-token sub-blocks
+
+
+def test_clock_rejection_rule():
+    """A timed region with a hardware or thermal slowdown, or SM clocks stuck
+    well below maximum with no reason, is rejected; the power cap alone is kept."""
+    ok = {"sm_mhz": 2010.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    assert not bench.clocks_rejected(ok)
+    assert not bench.clocks_rejected({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []})
+    for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
+        assert bench.clocks_rejected({"sm_mhz": 2000.0, "sm_max_mhz": 2070.0, "reasons": [r, "sw_power_cap"]})
+    assert bench.clocks_rejected({"sm_mhz": 1200.0, "sm_max_mhz": 2070.0, "reasons": []})
+    assert not bench.clocks_rejected({"sm_mhz": 1200.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]})
+    assert not bench.clocks_rejected({"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]})
