@@ -2,6 +2,7 @@
 """Benchmark of the VSA forward at the 10 s FastH3 shape on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload tiny|medium|5s|10s|ragged] [--keep F]
 
 A step is one VSA forward of one DiT attention layer (tile pool, coarse
 attention + top-k, fine attention with the gated combination) over the
@@ -13,7 +14,10 @@ value = effective TFLOP/s: the FLOPs the sparse pattern requires (fine
 attention over the keys each query attends to, plus the coarse branch),
 divided by the device time of the step, inputs resident in HBM; L2 is flushed
 between timed steps. e2e = the same metric through vsa_forward_host (pinned
-host buffers, host<->device copies inside the timed region).
+host buffers, host<->device copies inside the timed region), the mean over its
+steps; its output is compared bit for bit with the device forward's, and a
+mismatch voids the number. --workload and --keep select the other seeded
+configs (tiny, medium, 5 s, and the ragged sweep at keep 0.1, 0.2 or 0.4).
 
 Under torchrun every rank runs its own full problem (weak scaling, no
 collective in the data path); the step time is the max over ranks.
@@ -441,28 +445,35 @@ def barrier(world):
 
 # ----------------------------------------------------------------- CPU oracle sample
 
-def oracle_sample(n_video_tiles=256, n_prefix_rows=256, seed=None):
+def oracle_sample(n_video_tiles=256, n_prefix_rows=256, seed=None, cfg=None, keep=None):
     """Time the CPU oracle on one head of the workload: pooling, tile scores,
     selection and coarse branch for all tiles, plus fine attention for a seeded
-    sample of video query tiles and prefix rows. Returns (flops, seconds, text)."""
+    sample of video query tiles and prefix rows (None: all of them). Returns
+    (flops, seconds, text)."""
     from oracle import vsa_oracle as vo
-    cfg = CFG
+    cfg = CFG if cfg is None else cfg
+    keep = cfg.keep[0] if keep is None else keep
     seed = cfg.seed if seed is None else seed
     q, k, v, g = make_inputs(1, 1, cfg.len_text, cfg.len_audio, cfg.len_video, seed, device="cpu")
     bits = [bf16_bits(x)[0, :, 0] for x in (q, k, v, g)]
     t = cfg.n_video_tiles
     rng = np.random.default_rng(seed)
-    tiles = np.sort(rng.choice(t, size=min(t, n_video_tiles), replace=False))
-    prows = np.sort(rng.choice(cfg.prefix, size=min(cfg.prefix, n_prefix_rows), replace=False))
+    nt = t if n_video_tiles is None else min(t, n_video_tiles)
+    npr = cfg.prefix if n_prefix_rows is None else min(cfg.prefix, n_prefix_rows)
+    tiles = np.sort(rng.choice(t, size=nt, replace=False))
+    prows = np.sort(rng.choice(cfg.prefix, size=npr, replace=False)) if npr else np.zeros(0, dtype=np.int64)
     t0 = time.perf_counter()
-    r = vo.vsa_head(*bits, cfg.prefix, cfg.len_video, cfg.keep[0], video_tiles=tiles, prefix_rows=prows)
+    r = vo.vsa_head(*bits, cfg.prefix, cfg.len_video, keep, video_tiles=tiles, prefix_rows=prows)
     secs = time.perf_counter() - t0
     kk = r["k"]
-    flops = 4 * 128 * (t * t + len(tiles) * 64 * (cfg.prefix + 64 * kk) + len(prows) * cfg.seq)
+    n_tok = np.full(t, 64)
+    n_tok[-1] = cfg.len_video - 64 * (t - 1)
+    video_pairs = sum(int(n_tok[j]) * (cfg.prefix + int(n_tok[r["index"][j]].sum())) for j in tiles)
+    flops = 4 * 128 * (t * t + video_pairs + len(prows) * cfg.seq)
     text = (f"1 of {cfg.heads} heads of the {cfg.name} shape (synthetic, same recipe, own seed): pool, "
             f"tile scores, top-{kk} selection and coarse branch over all {t} tiles, fine attention "
-            f"for {len(tiles)} sampled video query tiles and {len(prows)} sampled prefix rows; "
-            f"rate = FLOPs of that work / its wall time")
+            f"for {len(tiles)} {'sampled ' if nt < t else ''}video query tiles and {len(prows)} "
+            f"{'sampled ' if npr < cfg.prefix else ''}prefix rows; rate = FLOPs of that work / its wall time")
     return float(flops), secs, text
 
 
@@ -485,7 +496,7 @@ def run_reference(args):
     rates, secs_all = [], []
     text = ""
     for step in range(args.warmup + args.steps):
-        flops, secs, text = oracle_sample(n_video_tiles=24, n_prefix_rows=64, seed=CFG.seed + step)
+        flops, secs, text = oracle_sample(n_video_tiles=24, n_prefix_rows=64, seed=CFG.seed + step, keep=args.keep)
         if step >= args.warmup:
             rates.append(flops / secs / 1e12)
             secs_all.append(secs)
@@ -495,7 +506,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs_all),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(),
+        "data": "synthetic", "config": workload_config(CFG, args.keep),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": text},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -516,7 +527,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     init_dist(world, "nccl")
     cfg = CFG
-    keep = cfg.keep[0]
+    keep = cfg.keep[0] if args.keep is None else args.keep
     peaks, peak_src = read_peaks()
     bsv.load_library()  # fails loudly if the library is not built
 
@@ -526,11 +537,14 @@ def run_ours(args):
     out = torch.empty_like(q)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    fl = effective_flops(cfg, keep)
 
     for _ in range(args.warmup):
         op(q, k, v, g, out)
     op.check()
+    # a partial last tile needs the selection to count the keys attended
+    sel = None if cfg.len_video % 64 == 0 else op.debug_views()["tile_index"].cpu().numpy()
+    fl = effective_flops(cfg, keep, tile_index=sel)
+    del sel
 
     steps = args.steps
 
@@ -569,7 +583,7 @@ def run_ours(args):
     total_flops = reduce_sum(fl["total"], world, dev)
     value = total_flops / (ms * 1e-3) / 1e12
 
-    pool_ms, coarse_ms, fine_ms = (statistics.mean(x) for x in stage_ms)
+    pool_ms, coarse_ms, fine_ms = (reduce_max(statistics.mean(x), world, dev) for x in stage_ms)
     fine_tflops = fl["fine"] / (fine_ms * 1e-3) / 1e12
     sustained = peaks["bf16_tflops_sustained"]
     burst = peaks["bf16_tflops"]
@@ -585,31 +599,36 @@ def run_ours(args):
         except Exception:
             traffic = None
 
+    # the lines measured beside the step belong to the benchmark workload only
+    side = cfg.name == "10s" and args.keep is None
+
     # ---- SubBlock-routed forwards on the same inputs (measured on their own)
     subblock = None
-    if not args.no_subblock:
+    if not args.no_subblock and side:
         subblock = [measure_subblock(q, k, v, cfg, dev, stream, flush, steps, args.warmup, peaks, world, s)
                     for s in SUBBLOCK_SPARSITY]
 
     # ---- the capacity bucket served from one graph (measured on its own)
     capacity = None
-    if not args.no_capacity and cfg.name == "10s":
+    if not args.no_capacity and side:
         capacity = measure_capacity(cfg.heads, dev, stream, flush, steps, args.warmup, world, cfg.seed + 200)
 
     # ---- fused preprocessing, measured on its own (not part of the forward step above)
     pre = None
-    if not args.no_preprocess:
+    if not args.no_preprocess and side:
         pre = measure_preprocess(op, cfg, dev, stream, flush, steps, args.warmup, peaks, world)
 
     # ---- the combination written into the output all-to-all's send layout (measured on its own)
     send_layout = None
-    if not args.no_send_layout:
+    if not args.no_send_layout and side:
         send_layout = measure_send_layout(op, q, k, v, g, cfg, dev, stream, flush, steps, args.warmup, world,
                                           cfg.seed + 300)
 
     # ---- end to end through the host-buffer entry point
     e2e = None
     if args.e2e_steps > 0:
+        # the device forward's output on the same inputs, to check the host path against
+        dev_out = out.cpu()
         hq, hk, hv, hg = [x.cpu().pin_memory() for x in (q, k, v, g)]
         hout = torch.empty_like(hq).pin_memory()
         del out, q, k, v, g
@@ -620,26 +639,36 @@ def run_ours(args):
         barrier(world)
         times = []
         for _ in range(args.e2e_steps):
+            hout.fill_(float("nan"))  # outside the timed call: every step must write the whole output
             t0 = time.perf_counter()
             bsv.vsa_forward_host(op.plan, hq, hk, hv, hg, hout, dbuf)
             times.append(time.perf_counter() - t0)
-        # host wall clock: an occasional call takes several times as long as the others while the
-        # device time does not change, so the value is the median over the steps; mean, min and max
-        # are reported beside it
-        e2e_s = reduce_max(statistics.median(times), world, dev)
+        # the last step's output, bit for bit against the device forward (outside the timed region)
+        same = bool(torch.equal(hout.view(torch.int16), dev_out.view(torch.int16)))
+        same = reduce_max(0.0 if same else 1.0, world, dev) == 0.0
+        # host wall clock, the mean over the steps; an occasional call stalls on the host while
+        # the device time does not change, so the median, min and max are reported beside it
+        e2e_s = reduce_max(statistics.mean(times), world, dev)
         tb = hq.numel() * hq.element_size()
-        e2e = {"value": total_flops / e2e_s / 1e12, "unit": UNIT, "ms_per_step": e2e_s * 1e3,
-               "statistic": f"median of {len(times)} steps",
-               "mean_ms": statistics.mean(times) * 1e3, "min_ms": min(times) * 1e3, "max_ms": max(times) * 1e3,
+        e2e = {"value": total_flops / e2e_s / 1e12 if same else None, "unit": UNIT, "ms_per_step": e2e_s * 1e3,
+               "statistic": f"mean of {len(times)} steps",
+               "median_ms": statistics.median(times) * 1e3, "min_ms": min(times) * 1e3,
+               "max_ms": max(times) * 1e3,
+               "bitwise_equal_to_device_forward": same,
                "h2d_bytes_per_step": 4 * tb, "d2h_bytes_per_step": tb,
                "api": "vsa_forward_host (C ABI), pinned host buffers, synchronous; "
                       "head groups pipelined: copy-in, forward and copy-out overlap"}
+        del dev_out, hq, hk, hv, hg, hout, dbuf
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        flops, secs, text = oracle_sample()
-        cpu = {"value": flops / secs / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-               "sample": text, "seconds": secs}
+        # small workloads: the oracle on one whole head; large ones: a bounded sample of one head
+        whole = cfg.seq * cfg.n_video_tiles <= 10_000 * 160
+        flops, secs, text = oracle_sample(None if whole else 256, None if whole else 256, cfg=cfg, keep=keep)
+        rate = flops / secs / 1e12
+        cpu = {"value": rate, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+               "sample": text, "seconds": secs,
+               "s_per_layer_at_this_rate": fl["total"] / (rate * 1e12)}
 
     if rank == 0:
         line = {
@@ -651,10 +680,12 @@ def run_ours(args):
             "effective_flops_per_step": fl["total"],
             "frac_of_bf16_peak": {"sustained": value / world / sustained, "burst": value / world / burst,
                                   "source": peak_src},
+            # the fine kernel is timed per launch by its own events: the burst peak applies
             "roofline": {"bound": "tensor", "kernel": "fine_attn_kernel", "achieved": fine_tflops,
-                         "peak": sustained, "unit": "TFLOP/s", "frac": fine_tflops / sustained,
-                         "traffic": traffic, "peak_kind": f"bf16 dense, sustained ({peak_src})",
-                         "frac_of_burst": fine_tflops / burst,
+                         "peak": burst, "unit": "TFLOP/s", "frac": fine_tflops / burst,
+                         "traffic": traffic if cfg.name == "10s" and args.keep is None else None,
+                         "peak_kind": f"bf16 dense, burst ({peak_src})",
+                         "frac_of_sustained": fine_tflops / sustained, "sustained_peak": sustained,
                          "algorithmic_flops_per_launch": fl["fine"], "ms_per_launch": fine_ms},
             "kernels": {
                 "pool_kernel": {"ms": pool_ms, "bytes": pool_bytes(cfg), "GB_s": pool_gbs,
@@ -702,7 +733,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-send-layout", action="store_true",
                     help="skip the send-layout forward (vsa_forward_rows) measured beside the step")
@@ -712,8 +743,10 @@ def main(argv=None):
                     help="skip the separate SubBlock-routed forward measurements")
     ap.add_argument("--no-preprocess", action="store_true",
                     help="skip the separate fused-preprocessing measurement")
-    ap.add_argument("--workload", choices=["10s", "5s", "medium"], default="10s",
-                    help="10s is the benchmark; the smaller ones serve profiler captures")
+    ap.add_argument("--workload", choices=list(CONFIGS), default="10s",
+                    help="10s is the benchmark; the others are the seeded configs measured beside it")
+    ap.add_argument("--keep", type=float, default=None,
+                    help="keep fraction (default: the workload's first; the ragged sweep uses 0.1, 0.2, 0.4)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     world, _, _ = dist_info()

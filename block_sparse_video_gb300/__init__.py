@@ -117,6 +117,9 @@ def load_library(path: str = LIB_PATH):
         "vsa_forward_ex": (i32, [vp, ctypes.POINTER(vsa_forward_args_t), vp, sz, vp]),
         "vsa_forward_preprocessed": (i32, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "vsa_plan_host_path_bytes": (i32, [vp, ctypes.POINTER(sz)]),
+        "vsa_plan_host_path_group": (i32, [vp, i32, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                           ctypes.POINTER(sz), ctypes.POINTER(sz), ctypes.POINTER(sz),
+                                           ctypes.POINTER(sz)]),
         "vsa_forward_host": (i32, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "vsa_debug_views": (i32, [vp, vp] + [ctypes.POINTER(vp)] * 5),
         "vsa_check": (i32, [vp, vp, vp]),
@@ -194,6 +197,20 @@ def vsa_plan_host_path_bytes(plan):
     n = ctypes.c_size_t()
     _check(load_library().vsa_plan_host_path_bytes(plan, ctypes.byref(n)), "vsa_plan_host_path_bytes")
     return n.value
+
+
+def vsa_plan_host_path_group(plan, group):
+    """Layout of one head group of the host path (see vsa.h): a dict with
+    n_groups, first_head, heads, offsets (q, k, v, gate, out), tensor_bytes,
+    workspace_offset and workspace_bytes. Host only."""
+    ng, h0, nh = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    offs = (ctypes.c_size_t * 5)()
+    tb, wo, wb = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load_library().vsa_plan_host_path_group(plan, int(group), ctypes.byref(ng), ctypes.byref(h0),
+                                                   ctypes.byref(nh), offs, ctypes.byref(tb), ctypes.byref(wo),
+                                                   ctypes.byref(wb)), "vsa_plan_host_path_group")
+    return {"n_groups": ng.value, "first_head": h0.value, "heads": nh.value, "offsets": list(offs),
+            "tensor_bytes": tb.value, "workspace_offset": wo.value, "workspace_bytes": wb.value}
 
 
 def vsa_plan_destroy(plan):

@@ -570,20 +570,41 @@ vsa_status_t vsa_preprocess(vsa_plan_t plan, const vsa_preprocess_args_t* args, 
 
 namespace {
 
-// Device bytes of one head group's five tensors (q, k, v, gate, out), each 256-byte aligned.
-size_t group_slot_bytes(const vsa_plan* sub) { return 5 * align_up(sub->tensor_bytes); }
+// Layout of head group gi inside the host path's device buffer. Groups
+// alternate between two slots; every group lays its five tensors out at the
+// widest group's tensor stride, whatever its own width, so a group's inputs
+// never overlap the output region of the group two before it (which the
+// copy-out stream may still be reading while those inputs are copied in).
+struct GroupLayout {
+  int first_head, heads, slot;
+  size_t off[5];        // q, k, v, gate, out
+  size_t tensor_bytes;  // this group's tensors
+  size_t ws_off, ws_bytes;
+};
 
-size_t pipe_ws_bytes(const HostPipe* pipe) {
+GroupLayout group_layout(const vsa_plan* p, int gi) {
+  const HostPipe* pipe = p->pipe;
+  GroupLayout L{};
+  const size_t tstride = align_up(pipe->sub[pipe->max_width]->tensor_bytes);
+  const size_t slot_bytes = 5 * tstride;
+  for (int i = 0; i < gi; ++i) L.first_head += pipe->widths[i];
+  L.heads = pipe->widths[gi];
+  L.slot = gi & 1;
+  for (int i = 0; i < 5; ++i) L.off[i] = L.slot * slot_bytes + i * tstride;
+  L.tensor_bytes = pipe->sub[L.heads]->tensor_bytes;
+  L.ws_off = 2 * slot_bytes;
   size_t ws = 0;
   for (const vsa_plan* sub : pipe->sub)
     if (sub && sub->ws_bytes > ws) ws = sub->ws_bytes;
-  return ws;
+  L.ws_bytes = ws;
+  return L;
 }
 
 size_t pipe_bytes(const vsa_plan* p) {
   const HostPipe* pipe = p->pipe;
   if (!pipe || pipe->widths.size() == 1) return 5 * align_up(p->tensor_bytes) + p->ws_bytes;
-  return 2 * group_slot_bytes(pipe->sub[pipe->max_width]) + pipe_ws_bytes(pipe);
+  const GroupLayout L = group_layout(p, 0);
+  return L.ws_off + L.ws_bytes;
 }
 
 // Device-side address of host memory the device can read (pinned or
@@ -615,6 +636,37 @@ vsa_status_t ensure_streams(HostPipe* pipe) {
 vsa_status_t vsa_plan_host_path_bytes(vsa_plan_t plan, size_t* bytes) {
   if (!plan || !bytes) return VSA_ERR_INVALID_ARG;
   *bytes = pipe_bytes(plan);
+  return VSA_OK;
+}
+
+vsa_status_t vsa_plan_host_path_group(vsa_plan_t plan, int32_t group, int32_t* n_groups, int32_t* first_head,
+                                      int32_t* heads, size_t* offsets, size_t* tensor_bytes,
+                                      size_t* workspace_offset, size_t* workspace_bytes) {
+  if (!plan) return VSA_ERR_INVALID_ARG;
+  const HostPipe* pipe = plan->pipe;
+  const bool piped = pipe && pipe->widths.size() > 1;
+  const int32_t ng = piped ? static_cast<int32_t>(pipe->widths.size()) : 1;
+  if (n_groups) *n_groups = ng;
+  if (!n_groups || !first_head || !heads || !offsets || !tensor_bytes || !workspace_offset || !workspace_bytes)
+    return VSA_ERR_INVALID_ARG;
+  if (group < 0 || group >= ng) return VSA_ERR_INVALID_ARG;
+  if (!piped) {
+    const size_t slot = align_up(plan->tensor_bytes);
+    *first_head = 0;
+    *heads = plan->g.H;
+    for (int i = 0; i < 5; ++i) offsets[i] = i * slot;
+    *tensor_bytes = plan->tensor_bytes;
+    *workspace_offset = 5 * slot;
+    *workspace_bytes = plan->ws_bytes;
+    return VSA_OK;
+  }
+  const GroupLayout L = group_layout(plan, group);
+  *first_head = L.first_head;
+  *heads = L.heads;
+  for (int i = 0; i < 5; ++i) offsets[i] = L.off[i];
+  *tensor_bytes = L.tensor_bytes;
+  *workspace_offset = L.ws_off;
+  *workspace_bytes = L.ws_bytes;
   return VSA_OK;
 }
 
@@ -658,9 +710,6 @@ vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, con
   const vsa::Geometry& g = plan->g;
   const size_t rows = static_cast<size_t>(g.B) * g.N;
   const size_t host_pitch = static_cast<size_t>(g.H) * vsa::kHeadDim * 2;
-  const size_t slot_bytes = group_slot_bytes(pipe->sub[pipe->max_width]);
-  uint8_t* ws = d + 2 * slot_bytes;
-  const size_t ws_bytes = pipe_ws_bytes(pipe);
   const int n_in = gate ? 4 : 3;
   const uint8_t* dev_in[4] = {nullptr, nullptr, nullptr, nullptr};
   bool gather_first = true;
@@ -673,21 +722,27 @@ vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, con
   auto cuda = [](cudaError_t e) { return e == cudaSuccess; };
   if (!cuda(cudaEventRecord(pipe->entry, st)) || !cuda(cudaStreamWaitEvent(pipe->s_in, pipe->entry, 0)))
     return VSA_ERR_CUDA;
+  // Ordering (each stream runs in issue order): the copy-in of group gi waits
+  // for the forward of gi - 2 (the last reader of its slot's inputs); the
+  // forward of gi waits for its copy-in and for the copy-out of gi - 2 (the
+  // last reader of its slot's output); the copy-out of gi waits for its
+  // forward. The copy-out of gi - 2 may still run during the copy-in of gi,
+  // which is why group_layout keeps inputs and outputs apart in every slot.
   const int groups = static_cast<int>(pipe->widths.size());
-  int h0 = 0;
-  for (int gi = 0; gi < groups; h0 += pipe->widths[gi], ++gi) {
-    const int s = gi & 1;
-    vsa_plan* sub = pipe->sub[pipe->widths[gi]];
+  for (int gi = 0; gi < groups; ++gi) {
+    const GroupLayout L = group_layout(plan, gi);
+    const int s = L.slot, h0 = L.first_head;
+    vsa_plan* sub = pipe->sub[L.heads];
     const size_t width = static_cast<size_t>(sub->g.H) * vsa::kHeadDim * 2;
-    const size_t tslot = align_up(sub->tensor_bytes);
-    uint8_t* base = d + s * slot_bytes;
+    uint8_t* const t[5] = {d + L.off[0], d + L.off[1], d + L.off[2], d + L.off[3], d + L.off[4]};
+    uint8_t* ws = d + L.ws_off;
     // inputs: slot s is free once the forward of group gi - 2 has read it
     if (gi >= 2 && !cuda(cudaStreamWaitEvent(pipe->s_in, pipe->fwd_done[s], 0))) return VSA_ERR_CUDA;
     if (gi == 0 && gather_first) {
       vsa::HostRows a{};
       for (int i = 0; i < n_in; ++i) {
         a.src[i] = dev_in[i] + h0 * 256;
-        a.dst[i] = base + i * tslot;
+        a.dst[i] = t[i];
       }
       a.src_pitch = host_pitch;
       a.dst_pitch = width;
@@ -697,7 +752,7 @@ vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, con
       if (!cuda(vsa::launch_copy_host_rows(a, plan->num_sms, pipe->s_in))) return VSA_ERR_CUDA;
     } else {
       for (int i = 0; i < n_in; ++i)
-        if (!cuda(cudaMemcpy2DAsync(base + i * tslot, width, static_cast<const uint8_t*>(hin[i]) + h0 * 256,
+        if (!cuda(cudaMemcpy2DAsync(t[i], width, static_cast<const uint8_t*>(hin[i]) + h0 * 256,
                                     host_pitch, width, rows, cudaMemcpyHostToDevice, pipe->s_in)))
           return VSA_ERR_CUDA;
     }
@@ -705,15 +760,14 @@ vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, con
     // forward: after its inputs, and after group gi - 2's output left slot s
     if (!cuda(cudaStreamWaitEvent(st, pipe->in_ready[s], 0))) return VSA_ERR_CUDA;
     if (gi >= 2 && !cuda(cudaStreamWaitEvent(st, pipe->out_done[s], 0))) return VSA_ERR_CUDA;
-    rs = vsa_forward(sub, base, base + tslot, base + 2 * tslot, gate ? base + 3 * tslot : nullptr,
-                     base + 4 * tslot, ws, ws_bytes, stream);
+    rs = vsa_forward(sub, t[0], t[1], t[2], gate ? t[3] : nullptr, t[4], ws, L.ws_bytes, stream);
     if (rs != VSA_OK) return rs;
     if (!cuda(cudaEventRecord(pipe->fwd_done[s], st))) return VSA_ERR_CUDA;
     // output; the last group's, which nothing hides, is written by a kernel when `out` is pinned
     if (!cuda(cudaStreamWaitEvent(pipe->s_out, pipe->fwd_done[s], 0))) return VSA_ERR_CUDA;
     if (gi == groups - 1 && scatter_last) {
       vsa::HostRows a{};
-      a.src[0] = base + 4 * tslot;
+      a.src[0] = t[4];
       a.dst[0] = dev_out + h0 * 256;
       a.src_pitch = width;
       a.dst_pitch = host_pitch;
@@ -721,7 +775,7 @@ vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, con
       a.rows = rows;
       a.tensors = 1;
       if (!cuda(vsa::launch_copy_host_rows(a, plan->num_sms, pipe->s_out))) return VSA_ERR_CUDA;
-    } else if (!cuda(cudaMemcpy2DAsync(static_cast<uint8_t*>(out) + h0 * 256, host_pitch, base + 4 * tslot, width,
+    } else if (!cuda(cudaMemcpy2DAsync(static_cast<uint8_t*>(out) + h0 * 256, host_pitch, t[4], width,
                                        width, rows, cudaMemcpyDeviceToHost, pipe->s_out))) {
       return VSA_ERR_CUDA;
     }

@@ -327,6 +327,25 @@ vsa_status_t vsa_forward_ex(vsa_plan_t plan, const vsa_forward_args_t* args, voi
  * Synchronises `stream` before returning; device-side errors are not reported
  * here. */
 vsa_status_t vsa_plan_host_path_bytes(vsa_plan_t plan, size_t* bytes);
+
+/* Where vsa_forward_host places head group `group` in its device buffer
+ * (host only; touches no GPU). *n_groups receives the number of groups.
+ * Group `group` covers heads [*first_head, *first_head + *heads); its q, k,
+ * v, gate and output are bf16 [batch, N, *heads, 128] tensors of
+ * *tensor_bytes bytes at byte offsets offsets[0..4] (5 entries, caller
+ * storage); the workspace its forward uses is [*workspace_offset,
+ * *workspace_offset + *workspace_bytes), shared by every group. Groups
+ * alternate between two slots and each slot keeps inputs and output apart at
+ * the widest group's tensor stride. The call order behind the layout: the
+ * copy-in of group g waits for the forward of group g - 2; the forward of g
+ * waits for its own copy-in and for the copy-out of g - 2; the copy-out of g
+ * waits for the forward of g; each of the three streams runs in order.
+ * Returns VSA_ERR_INVALID_ARG for a NULL pointer or a group outside
+ * [0, *n_groups) (*n_groups is still set when n_groups is non-NULL). */
+vsa_status_t vsa_plan_host_path_group(vsa_plan_t plan, int32_t group, int32_t* n_groups, int32_t* first_head,
+                                      int32_t* heads, size_t* offsets, size_t* tensor_bytes,
+                                      size_t* workspace_offset, size_t* workspace_bytes);
+
 vsa_status_t vsa_forward_host(vsa_plan_t plan, const void* q, const void* k, const void* v,
                               const void* gate, void* out, void* device_buffer,
                               size_t device_buffer_bytes, void* stream);
