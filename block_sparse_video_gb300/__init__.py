@@ -521,7 +521,8 @@ class VSA:
 
 
 class SubBlock(VSA):
-    """Owner of a SubBlock-routed plan ("How SubBlock Sparse Attention Works"):
+    """Owner of a SubBlock-routed plan (SGLang Diffusion benchmark page, section
+    "How SubBlock Sparse Attention Works"):
     video query tiles keep the k video key tiles of highest estimated softmax
     mass; no coarse branch and no gate. ``sparsity`` is the fraction of key
     tiles that may be dropped."""

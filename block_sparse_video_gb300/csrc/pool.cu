@@ -2,8 +2,8 @@
 // of Q, K and V over the tile's valid tokens, in fp32 ("UniServe: serving
 // FastH3 at its fastest", section "Fused attention preprocessing": tile
 // pooling over valid tokens into FP32 pooled statistics). A second kernel
-// takes 16-token runs of Q and K for the SubBlock router (section "How
-// SubBlock Sparse Attention Works": four 16-token sub-blocks per 64-token
+// takes 16-token runs of Q and K for the SubBlock router (the SGLang Diffusion benchmark page (MiniMax-H3 on 8x H200),
+// section "How SubBlock Sparse Attention Works": four 16-token sub-blocks per 64-token
 // block); a run past the end of a ragged last block is empty and its mean is
 // written as 0.
 //

@@ -9,8 +9,8 @@
 //   * the FP32 tile pooling of the packed Q, K and V over each video tile's
 //     valid tokens.
 // The packed bf16 tensors and the pooled statistics land directly in the
-// buffers the coarse and fine kernels read. Section "The Kernel Layer" fixes
-// two details: the normalised value is rounded to bf16 before RoPE is applied,
+// buffers the coarse and fine kernels read. Section "The Kernel Layer" of
+// the SGLang Diffusion benchmark page (MiniMax-H3 on 8x H200) fixes two details: the normalised value is rounded to bf16 before RoPE is applied,
 // and the rotary width (96 of 128 channels there).
 //
 // Conventions where the page is silent:

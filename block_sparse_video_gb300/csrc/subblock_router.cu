@@ -1,5 +1,5 @@
-// SubBlock router: the block-sparse selection of "UniServe: serving FastH3 at
-// its fastest", section "How SubBlock Sparse Attention Works". Each 64-token
+// SubBlock router: the block-sparse selection of the SGLang Diffusion benchmark page (MiniMax-H3 on 8x H200),
+// section "How SubBlock Sparse Attention Works". Each 64-token
 // block is split into four 16-token sub-blocks on the query and key side
 // (n_q = n_k = 4). A pooled log-sum-exp score estimates each key block's
 // unnormalised softmax mass for each query block and head, and the router

@@ -81,8 +81,8 @@ typedef struct vsa_plan* vsa_plan_t; /* opaque, host memory, owned by the librar
  * On success *out receives a plan to release with vsa_plan_destroy. */
 vsa_status_t vsa_plan_create(const vsa_shape_t* shape, int device, vsa_plan_t* out);
 
-/* A plan whose selection is the SubBlock router ("UniServe: serving FastH3 at
- * its fastest", section "How SubBlock Sparse Attention Works") in place of the
+/* A plan whose selection is the SubBlock router (the SGLang Diffusion benchmark page (MiniMax-H3 on 8x H200),
+ * section "How SubBlock Sparse Attention Works") in place of the
  * coarse branch. Each 64-token tile splits into four 16-token sub-blocks on
  * the query and key side. The estimated softmax mass of video key tile j for
  * video query tile i is
@@ -140,7 +140,8 @@ typedef struct {
 } vsa_lengths_t;
 
 /* Fused attention preprocessing ("UniServe: serving FastH3 at its fastest",
- * section "Fused attention preprocessing"; section "The Kernel Layer" gives the
+ * section "Fused attention preprocessing"; section "The Kernel Layer" of
+ * the SGLang Diffusion benchmark page (MiniMax-H3 on 8x H200) gives the
  * rotary width of 96 channels and the rounding of the normalised value before
  * RoPE). One pass over the projected Q/K/V/gate rows does the following:
  *   - packs each attention token's row into the [batch, N, num_heads, 128]

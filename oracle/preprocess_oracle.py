@@ -16,7 +16,8 @@ does the following:
   step;
 * copying the gate.
 
-Section "The Kernel Layer" gives the RoPE width used there (96 of the 128
+Section "The Kernel Layer" of the SGLang Diffusion benchmark page (MiniMax-H3 on 8x H200)
+gives the RoPE width used there (96 of the 128
 channels of a head). It also says that the fused norm + RoPE kernel rounds the
 normalised value before applying RoPE.
 

@@ -4,8 +4,8 @@ TEST INFRASTRUCTURE ONLY. Only the test suite, ``__graft_entry__.smoke()`` and
 ``bench.py``'s CPU-baseline leg may import or run it; the library never does.
 It shares no code with the CUDA path.
 
-What it computes follows "UniServe: serving FastH3 at its fastest", section
-"How SubBlock Sparse Attention Works":
+What it computes follows the SGLang Diffusion benchmark page (MiniMax-H3 on 8x H200),
+section "How SubBlock Sparse Attention Works":
 * the sequence is cut into 64-token query and key blocks, and each block into
   four 16-token sub-blocks on both sides (n_q = n_k = 4);
 * a pooling and log-sum-exp score estimates each key block's unnormalised

@@ -1,5 +1,5 @@
-"""GPU parity of the SubBlock-routed forward ("UniServe: serving FastH3 at its
-fastest", section "How SubBlock Sparse Attention Works") against the CPU
+"""GPU parity of the SubBlock-routed forward (the SGLang Diffusion benchmark page (MiniMax-H3 on 8x H200),
+section "How SubBlock Sparse Attention Works") against the CPU
 oracle, through the C ABI.
 
 Bars:

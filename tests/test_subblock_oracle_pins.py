@@ -1,5 +1,5 @@
-"""Pins for the SubBlock router oracle ("UniServe: serving FastH3 at its
-fastest", section "How SubBlock Sparse Attention Works"). Each test ties the
+"""Pins for the SubBlock router oracle (the SGLang Diffusion benchmark page (MiniMax-H3 on 8x H200),
+section "How SubBlock Sparse Attention Works"). Each test ties the
 oracle to something other than itself:
 * a hand-worked budget table;
 * brute-force sub-block means;
