@@ -568,7 +568,7 @@ __all__ = [
     "VSA", "SubBlock", "VsaError", "vsa_plan_create_subblock", "load_library", "header_functions", "vsa_plan_create", "vsa_plan_info",
     "vsa_forward", "vsa_forward_host", "vsa_preprocess", "vsa_forward_preprocessed", "vsa_forward_rows",
     "vsa_output_rows_t", "vsa_forward_lengths", "vsa_forward_ex", "vsa_forward_args_t",
-    "vsa_preprocess_args_t", "vsa_plan_host_path_bytes", "vsa_debug_views", "vsa_check",
+    "vsa_preprocess_args_t", "vsa_plan_host_path_bytes", "vsa_plan_host_path_group", "vsa_debug_views", "vsa_check",
     "vsa_plan_set_stage_events", "vsa_plan_destroy", "vsa_status_string",
     "vsa_forward_static_workspace", "vsa_diag_wait_timeout",
 ]

@@ -104,7 +104,11 @@ constexpr int kBarPEmpty = kBarPFull + kNumP;
 constexpr int kBarOEmpty = kBarPEmpty + kNumP;
 constexpr int kBarItemFull = kBarOEmpty + kNumO;
 constexpr int kBarItemEmpty = kBarItemFull + kItemSlots;
-constexpr int kNumBars = kBarItemEmpty + kItemSlots;
+// Device lengths: a V box that reaches rows past the request's tokens lands
+// here first; the V loader clears those rows, then completes the slot's full
+// barrier itself.
+constexpr int kBarVClear = kBarItemEmpty + kItemSlots;
+constexpr int kNumBars = kBarVClear + 1;
 static_assert(kNumBars * 8 <= 512, "barrier area");
 static_assert(kColO + kNumO * 64 <= kTmemCols, "TMEM columns");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -257,6 +261,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       mbar_init(bar(kBarItemFull + s), 1);
       mbar_init(bar(kBarItemEmpty + s), kItemReaders);
     }
+    mbar_init(bar(kBarVClear), 1);
     fence_barrier_init();
   }
   if (warp == kWarpMmaS) tmem_alloc(smem_u32(tslot), kTmemCols);
@@ -303,6 +308,17 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     const uint32_t box_off = box_half * 16384 + box_tile * 8192;
     int slot = 0;        // ring slot of the next block (counting over all items)
     uint32_t g = 0;      // blocks loaded so far, over all items
+    uint32_t n_clear = 0;  // V blocks that went through the clearing barrier
+    // With device lengths, rows past the request's N (up to the buffer's rows)
+    // are capacity padding with arbitrary contents. Their key lanes are masked
+    // (P = 0), but 0 * NaN is NaN in the P.V product, so V rows past N are
+    // cleared in shared memory before the product reads them. Only the
+    // ragged last prefix tile and the ragged last video tile can reach them.
+    // (Without device lengths those rows are outside the tensor map and read
+    // as zeros.)
+    const bool clear_v = v_warp && p.dl.len != nullptr;
+    const int n_req = G.P + G.Lv;
+    auto kept_rows = [&](int row) { return (!clear_v || row >= p.N) ? kTile : max(0, min(kTile, n_req - row)); };
     for (int n = 0; ok; ++n) {
       int item;
       if (!v_warp) {
@@ -370,17 +386,39 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         const uint32_t gp = g - static_cast<uint32_t>(nstage);  // wraps for the first nstage blocks
         const int rel_bar = v_warp ? kBarPEmpty + gp % kNumP : kBarSFull + gp % kNumS;
         const uint32_t rel_par = v_warp ? (gp / kNumP) & 1u : (gp / kNumS) & 1u;
+        const int keep_a = kept_rows(ra), keep_b = kept_rows(rb);
+        const bool clear = keep_a < kTile || keep_b < kTile;  // warp-uniform
+        const uint32_t land = clear ? bar(kBarVClear) : bar(bar_full + slot);
         bool lane_ok = true;
         if (lane < 4) {
           if (g >= static_cast<uint32_t>(nstage))
             lane_ok = mbar_wait(bar(rel_bar), rel_par, err, v_warp ? 0x200u : 0x100u);
           if (lane_ok) {
-            if (lane == 0) mbar_arrive_expect_tx(bar(bar_full + slot), kKVBytes);
-            tma_load_4d(ring + slot * kKVBytes + box_off, map, 64 * box_half, it.h, box_tile ? rb : ra, it.b,
-                        bar(bar_full + slot));
+            if (lane == 0) mbar_arrive_expect_tx(land, kKVBytes);
+            tma_load_4d(ring + slot * kKVBytes + box_off, map, 64 * box_half, it.h, box_tile ? rb : ra, it.b, land);
           }
         }
         if (!__all_sync(0xffffffffu, lane_ok)) { ok = false; break; }
+        if (clear) {
+          // every lane observes the boxes landing before it overwrites rows of them
+          lane_ok = mbar_wait(bar(kBarVClear), n_clear & 1u, err, 0x210u);
+          ++n_clear;
+          if (!__all_sync(0xffffffffu, lane_ok)) { ok = false; break; }
+          // a row is 128 bytes whatever the swizzle: clear rows keep .. 63 of each
+          // affected tile, in both channel halves, 16 bytes per store
+          for (int tb = 0; tb < 2; ++tb) {
+            const int keep = tb ? keep_b : keep_a;
+            const int chunks = (kTile - keep) * 8;  // per channel half
+            for (int c = lane; c < 2 * chunks; c += 32) {
+              const int half = c >= chunks ? 1 : 0, rem = c - half * chunks;
+              st_shared_v4(ring + slot * kKVBytes + half * 16384 + tb * 8192 + (keep + rem / 8) * 128 + (rem % 8) * 16,
+                           0u, 0u, 0u, 0u);
+            }
+          }
+          fence_proxy_async_smem();  // the products read shared memory through the async proxy
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(bar_full + slot));  // no bytes pending: completes the phase
+        }
         if (++slot == nstage) slot = 0;
         ++g;
       }
@@ -700,11 +738,14 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       // The fast mode is valid while every P stayed below kFastLimitSum: P >= 0,
       // so one larger P (or an overflow to inf) leaves a partial row sum at or
       // above that bound (a NaN fails the comparison too).
+      // Only the item's valid query columns count: the others are never stored
+      // (with device lengths their Q rows may be padding with any contents).
       bool overflow = false;
       if (!kExact) {
 #pragma unroll
         for (int j = 0; j < kCols / 2; ++j)
-          overflow = overflow || !(l2[j].x < kFastLimitSum) || !(l2[j].y < kFastLimitSum);
+          overflow = overflow || (col0 + 2 * j < it.q_valid && !(l2[j].x < kFastLimitSum)) ||
+                     (col0 + 2 * j + 1 < it.q_valid && !(l2[j].y < kFastLimitSum));
       }
       if (named_bar_or(kBarSoftmaxAll, 32 * kSoftmaxWarps, failed)) break;
       if (!kExact && named_bar_or(kBarSoftmaxAll, 32 * kSoftmaxWarps, overflow) && tid == 32 * kWarpSoftmax0) {

@@ -235,11 +235,11 @@ vsa_status_t vsa_forward_preprocessed(vsa_plan_t plan, const void* q, const void
  *   - k follows the plan's rule for the request's T: max(1, min(T,
  *     floor(keep_fraction * T + 0.5))); for a SubBlock plan, the kept count
  *     T - floor(sparsity * T) rounded up to a multiple of 8, capped at T;
- *   - rows N .. N + 63 of q, k and v (capacity padding, when it exists) must
- *     hold finite values. A ragged last tile's loads read them, and they are
- *     masked by exact zeros, so NaN or Inf there would propagate. The
- *     preprocessing writes real rows only; clearing the padding once at
- *     allocation is enough;
+ *   - rows N .. N_cap - 1 of q, k, v and gate (capacity padding) may hold
+ *     anything, NaN and Inf included: a ragged tile's 64-row loads read
+ *     some of them, and the forward masks their keys, clears their V rows in
+ *     shared memory before the P.V product, and never stores or votes on
+ *     their query rows, so no padding value reaches the output;
  *   - rows N .. N_cap - 1 of out are not written;
  *   - the workspace and its views (vsa_debug_views) keep the plan's layout:
  *     the request's tiles are the first T rows of each [T_cap] block, and
