@@ -19,14 +19,18 @@ steps; its output is compared bit for bit with the device forward's, and a
 mismatch voids the number. --workload and --keep select the other seeded
 configs (tiny, medium, 5 s, and the ragged sweep at keep 0.1, 0.2 or 0.4).
 
-Under torchrun every rank runs its own full problem (weak scaling, no
-collective in the data path); the step time is the max over ranks.
+Under torchrun the ranks split the layer's heads (contiguous ranges, as the
+page's 4-way head sharding does; strong scaling, no collective in the data
+path): each rank reads its heads in place from the full-width projections and
+writes them into the same heads of the output. The step time is the max over
+ranks and value counts the whole layer's FLOPs.
 --impl reference times the CPU oracle on a bounded sample of the same
 workload (rank 0 only).
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -42,6 +46,7 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
+from block_sparse_video_gb300.sharding import head_ranges  # noqa: E402
 from block_sparse_video_gb300.synthetic import CONFIGS, bf16_bits, make_config_inputs, make_inputs  # noqa: E402
 
 METRIC = "VSA fwd ms/layer & effective TFLOP/s (frac of BF16 peak), 10s FastH3 shape"
@@ -65,7 +70,7 @@ def workload_config(cfg=None, keep=None):
         "seed": cfg.seed,
         "l2": (f"flushed between timed steps (512 MB write); inputs "
                f"{4 * cfg.batch * (cfg.prefix + cfg.len_video) * cfg.heads * 128 * 2 / 1e9:.2f} GB"),
-        "parallelism": "one full problem per GPU (weak scaling)",
+        "parallelism": "heads split across GPUs (contiguous ranges; 1 GPU: all heads)",
     }
 
 
@@ -505,7 +510,7 @@ def run_reference(args):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs_all),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(CFG, args.keep),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": text},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -531,19 +536,31 @@ def run_ours(args):
     peaks, peak_src = read_peaks()
     bsv.load_library()  # fails loudly if the library is not built
 
+    # Every rank holds the whole layer's projections (same seed) and attends for its own
+    # contiguous range of heads, read in place from the full-width rows and written into
+    # the same heads of the full-width output; one rank takes all heads.
+    h0, hr = head_ranges(cfg.heads, world)[rank]
+    rcfg = dataclasses.replace(cfg, heads=hr)
     q, k, v, g = make_inputs(cfg.batch, cfg.heads, cfg.len_text, cfg.len_audio, cfg.len_video,
-                             cfg.seed + rank, device=dev)
-    op = bsv.VSA(cfg.batch, cfg.heads, cfg.len_text, cfg.len_audio, cfg.len_video, keep, device=dev)
+                             cfg.seed, device=dev)
+    op = bsv.VSA(cfg.batch, hr, cfg.len_text, cfg.len_audio, cfg.len_video, keep, device=dev)
     out = torch.empty_like(q)
+    hs = slice(h0, h0 + hr)
+    ins = (q[:, :, hs], k[:, :, hs], v[:, :, hs], g[:, :, hs])
+    out_slice = out[:, :, hs]
+
+    def forward():
+        op.forward_ex(*ins, out=out_slice)
+
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(args.warmup):
-        op(q, k, v, g, out)
+        forward()
     op.check()
     # a partial last tile needs the selection to count the keys attended
     sel = None if cfg.len_video % 64 == 0 else op.debug_views()["tile_index"].cpu().numpy()
-    fl = effective_flops(cfg, keep, tile_index=sel)
+    fl = effective_flops(rcfg, keep, tile_index=sel)  # this rank's heads
     del sel
 
     steps = args.steps
@@ -562,7 +579,7 @@ def run_ours(args):
             flush.zero_()
             bsv.vsa_plan_set_stage_events(op.plan, ev[s])
             starts[s].record(stream)
-            op(q, k, v, g, out)
+            forward()
             ends[s].record(stream)
         torch.cuda.synchronize(dev)
         clk = sampler.stop()
@@ -584,10 +601,11 @@ def run_ours(args):
     value = total_flops / (ms * 1e-3) / 1e12
 
     pool_ms, coarse_ms, fine_ms = (reduce_max(statistics.mean(x), world, dev) for x in stage_ms)
+    # per GPU: rank 0 holds the largest head share, timed against the slowest rank's kernel
     fine_tflops = fl["fine"] / (fine_ms * 1e-3) / 1e12
     sustained = peaks["bf16_tflops_sustained"]
     burst = peaks["bf16_tflops"]
-    pool_gbs = pool_bytes(cfg) / (pool_ms * 1e-3) / 1e9
+    pool_gbs = pool_bytes(rcfg) / (pool_ms * 1e-3) / 1e9
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "fine_attn_traffic.json")
     if os.path.exists(tpath):
@@ -599,8 +617,8 @@ def run_ours(args):
         except Exception:
             traffic = None
 
-    # the lines measured beside the step belong to the benchmark workload only
-    side = cfg.name == "10s" and args.keep is None
+    # the lines measured beside the step belong to the single-GPU benchmark workload only
+    side = cfg.name == "10s" and args.keep is None and world == 1
 
     # ---- SubBlock-routed forwards on the same inputs (measured on their own)
     subblock = None
@@ -627,11 +645,12 @@ def run_ours(args):
     # ---- end to end through the host-buffer entry point
     e2e = None
     if args.e2e_steps > 0:
-        # the device forward's output on the same inputs, to check the host path against
-        dev_out = out.cpu()
-        hq, hk, hv, hg = [x.cpu().pin_memory() for x in (q, k, v, g)]
+        # this rank's heads as they arrive on the host (contiguous, pinned), and the device
+        # forward's output of the same heads to check the host path against
+        dev_out = out_slice.contiguous().cpu()
+        hq, hk, hv, hg = [x.contiguous().cpu().pin_memory() for x in ins]
         hout = torch.empty_like(hq).pin_memory()
-        del out, q, k, v, g
+        del out, out_slice, ins, q, k, v, g
         torch.cuda.empty_cache()
         dbuf = torch.empty(bsv.vsa_plan_host_path_bytes(op.plan), dtype=torch.uint8, device=dev)
         for _ in range(2):
@@ -640,14 +659,15 @@ def run_ours(args):
         times = []
         for _ in range(args.e2e_steps):
             hout.fill_(float("nan"))  # outside the timed call: every step must write the whole output
+            barrier(world)
             t0 = time.perf_counter()
             bsv.vsa_forward_host(op.plan, hq, hk, hv, hg, hout, dbuf)
             times.append(time.perf_counter() - t0)
         # the last step's output, bit for bit against the device forward (outside the timed region)
         same = bool(torch.equal(hout.view(torch.int16), dev_out.view(torch.int16)))
         same = reduce_max(0.0 if same else 1.0, world, dev) == 0.0
-        # host wall clock, the mean over the steps; an occasional call stalls on the host while
-        # the device time does not change, so the median, min and max are reported beside it
+        # host wall clock, the mean over the steps (max over ranks); the median, min and max are
+        # reported beside it
         e2e_s = reduce_max(statistics.mean(times), world, dev)
         tb = hq.numel() * hq.element_size()
         e2e = {"value": total_flops / e2e_s / 1e12 if same else None, "unit": UNIT, "ms_per_step": e2e_s * 1e3,
@@ -655,8 +675,9 @@ def run_ours(args):
                "median_ms": statistics.median(times) * 1e3, "min_ms": min(times) * 1e3,
                "max_ms": max(times) * 1e3,
                "bitwise_equal_to_device_forward": same,
-               "h2d_bytes_per_step": 4 * tb, "d2h_bytes_per_step": tb,
-               "api": "vsa_forward_host (C ABI), pinned host buffers, synchronous; "
+               "h2d_bytes_per_step": int(reduce_sum(4 * tb, world, dev)),
+               "d2h_bytes_per_step": int(reduce_sum(tb, world, dev)),
+               "api": "vsa_forward_host (C ABI), pinned host buffers of this rank's heads, synchronous; "
                       "head groups pipelined: copy-in, forward and copy-out overlap"}
         del dev_out, hq, hk, hv, hg, hout, dbuf
 
@@ -673,11 +694,11 @@ def run_ours(args):
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "strong",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; no checkpoint)",
             "config": workload_config(cfg, keep),
             "ms_per_layer": ms,
-            "effective_flops_per_step": fl["total"],
+            "effective_flops_per_step": total_flops,
             "frac_of_bf16_peak": {"sustained": value / world / sustained, "burst": value / world / burst,
                                   "source": peak_src},
             # the fine kernel is timed per launch by its own events: the burst peak applies
@@ -688,20 +709,20 @@ def run_ours(args):
                          "frac_of_sustained": fine_tflops / sustained, "sustained_peak": sustained,
                          "algorithmic_flops_per_launch": fl["fine"], "ms_per_launch": fine_ms},
             "kernels": {
-                "pool_kernel": {"ms": pool_ms, "bytes": pool_bytes(cfg), "GB_s": pool_gbs,
+                "pool_kernel": {"ms": pool_ms, "bytes": pool_bytes(rcfg), "GB_s": pool_gbs,
                                 "frac_of_hbm": pool_gbs / peaks["hbm_gbs"]},
                 "coarse_topk_kernel": {"ms": coarse_ms, "flops": fl["coarse"],
                                        "TFLOP_s": fl["coarse"] / (coarse_ms * 1e-3) / 1e12,
-                                       "bytes": coarse_bytes(cfg, keep),
-                                       "frac_of_hbm": coarse_bytes(cfg, keep) / (coarse_ms * 1e-3) / 1e9
+                                       "bytes": coarse_bytes(rcfg, keep),
+                                       "frac_of_hbm": coarse_bytes(rcfg, keep) / (coarse_ms * 1e-3) / 1e9
                                        / peaks["hbm_gbs"]},
                 "pool_plus_coarse": {"ms": pool_ms + coarse_ms,
-                                     "bytes": pool_bytes(cfg) + coarse_bytes(cfg, keep),
-                                     "frac_of_hbm": (pool_bytes(cfg) + coarse_bytes(cfg, keep))
+                                     "bytes": pool_bytes(rcfg) + coarse_bytes(rcfg, keep),
+                                     "frac_of_hbm": (pool_bytes(rcfg) + coarse_bytes(rcfg, keep))
                                      / ((pool_ms + coarse_ms) * 1e-3) / 1e9 / peaks["hbm_gbs"]},
                 "fine_attn_kernel": {"ms": fine_ms, "flops": fl["fine"], "TFLOP_s": fine_tflops,
-                                     "kv_l2_to_smem_bytes": kv_stream_bytes(cfg, keep),
-                                     "kv_l2_to_smem_TB_s": kv_stream_bytes(cfg, keep) / (fine_ms * 1e-3) / 1e12},
+                                     "kv_l2_to_smem_bytes": kv_stream_bytes(rcfg, keep),
+                                     "kv_l2_to_smem_TB_s": kv_stream_bytes(rcfg, keep) / (fine_ms * 1e-3) / 1e12},
                 "preprocess_kernel": pre,
             },
             "subblock": subblock,

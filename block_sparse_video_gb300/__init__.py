@@ -89,6 +89,7 @@ class vsa_forward_args_t(ctypes.Structure):
         ("rows", ctypes.POINTER(vsa_output_rows_t)),
         ("lengths", ctypes.c_void_p),
         ("preprocessed", ctypes.c_int32),
+        ("in_row_stride", ctypes.c_int64),
     ]
 
 
@@ -230,6 +231,18 @@ def _check_tensor(x, name, shape, device=None):
         raise ValueError(f"{name}: expected contiguous bf16 {tuple(shape)}, got {x.dtype} {tuple(x.shape)}")
     if device is not None and x.device != device:
         raise ValueError(f"{name}: expected a tensor on {device}, got {x.device}")
+
+
+def _check_head_slice(x, name, shape, device):
+    """A bf16 [B, N, H, 128] tensor whose token rows may be wider than H x 128
+    channels (a head slice of a wider projection). Returns its row stride in
+    elements."""
+    if (x.dtype != torch.bfloat16 or tuple(x.shape) != tuple(shape) or x.device != device
+            or x.stride(3) != 1 or x.stride(2) != 128):
+        raise ValueError(f"{name}: expected bf16 {tuple(shape)} on {device} with contiguous heads of 128 channels")
+    if shape[0] > 1 and x.stride(0) != shape[1] * x.stride(1):
+        raise ValueError(f"{name}: batches must be N * row stride elements apart")
+    return x.stride(1)
 
 
 def vsa_forward(plan, q, k, v, gate, out, workspace, stream=None):
@@ -450,9 +463,14 @@ class VSA:
         """The general forward (vsa_forward_ex). ``out``: the packed [B, N, H, 128]
         output, or with ``out_row_map`` (or a non-packed ``out``) output rows as in
         forward_rows; ``lengths``: device int64 [3] of a request inside this
-        plan's capacity; ``preprocessed``: the inputs come from ``preprocess``."""
-        for name, x in (("q", q), ("k", k), ("v", v)) + ((("gate", gate),) if gate is not None else ()):
-            _check_tensor(x, name, self.shape, self.device)
+        plan's capacity; ``preprocessed``: the inputs come from ``preprocess``.
+        q, k, v and gate may be head slices of wider rows (e.g. ``x[:, :, h0:h0 + H]``
+        of a projection with more heads); they must share one row stride."""
+        strides = {_check_head_slice(x, name, self.shape, self.device)
+                   for name, x in (("q", q), ("k", k), ("v", v)) + ((("gate", gate),) if gate is not None else ())}
+        if len(strides) != 1:
+            raise ValueError("q, k, v and gate must share one row stride")
+        row_stride = strides.pop()
         if out is None:
             out = torch.empty(self.shape, dtype=torch.bfloat16, device=self.device)
         rows = None
@@ -466,7 +484,8 @@ class VSA:
         args = vsa_forward_args_t(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out),
                                   ctypes.pointer(rows) if rows is not None else None,
                                   _ptr(_check_lengths(lengths, self.device)) if lengths is not None else None,
-                                  1 if preprocessed else 0)
+                                  1 if preprocessed else 0,
+                                  0 if row_stride == self.num_heads * 128 else row_stride)
         vsa_forward_ex(self.plan, args, self.workspace, stream)
         return out
 

@@ -128,6 +128,7 @@ struct FineParams {
   const int32_t* out_row_map;  // null: token n of batch b -> out row b * N + n; else row b * out_rows + map[b * N + n]
   long long out_rows;          // output rows per batch
   long long out_row_stride;    // elements between output rows
+  long long in_row_stride;     // elements between token rows of the gate (and of q, k, v via the tensor maps)
   const int32_t* tile_index;
   unsigned int* err;
   int* work_counter;    // next work index to hand out (zeroed before the launch)
@@ -520,7 +521,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     // Blocks that may hold masked key lanes: the one with the ragged last prefix
     // tile, and the last block (an absent second tile, or ragged video tile T-1).
     const int ragged_prefix_blk = (G.TP > 0 && prefix_tail < kTile) ? (G.TP - 1) / 2 : -1;
-    const size_t row_stride = static_cast<size_t>(p.H) * kHeadDim;
+    const size_t row_stride = static_cast<size_t>(p.in_row_stride);
     bool failed = false;
     uint32_t gs = 0;  // blocks consumed so far, over all items
     for (int n = 0;; ++n) {
@@ -822,6 +823,7 @@ cudaError_t launch_fine(const Geometry& g, const CUtensorMap& map_q, const CUten
   p.out_row_map = a.out_row_map;
   p.out_rows = a.out_row_map ? a.out_rows : g.N;
   p.out_row_stride = a.out_row_stride > 0 ? a.out_row_stride : static_cast<long long>(g.H) * kHeadDim;
+  p.in_row_stride = input_row_stride(g);
   p.coarse = a.coarse;
   p.tile_index = a.tile_index;
   p.err = a.err;

@@ -20,7 +20,15 @@ struct Geometry {
   int T = 0;   // video tiles, ceil(Lv / 64)
   int TP = 0;  // prefix tiles, ceil(P / 64)
   int k = 0;   // kept video tiles per video query tile
+  // Elements between consecutive token rows of q, k, v and gate; 0 means
+  // H * 128 (packed). A larger stride reads H heads out of a wider row, e.g.
+  // one rank's head slice of the full projection.
+  long long row_stride = 0;
 };
+
+__host__ __device__ __forceinline__ long long input_row_stride(const Geometry& g) {
+  return g.row_stride > 0 ? g.row_stride : static_cast<long long>(g.H) * kHeadDim;
+}
 
 // Lengths read on the device (a capacity plan's forward): the plan's geometry
 // is the capacity (buffer rows per batch N, tiles T, kept tiles k: the layout

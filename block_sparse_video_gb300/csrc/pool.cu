@@ -60,7 +60,7 @@ pool_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict
     out[0] = out[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
-  const size_t row_stride = static_cast<size_t>(row_vecs);  // in uint4 units
+  const size_t row_stride = static_cast<size_t>(input_row_stride(cap) / 8);  // in uint4 units
   const uint4* base = reinterpret_cast<const uint4*>(src) +
                       (static_cast<size_t>(b) * N + P + static_cast<size_t>(t) * kLen) * row_stride +
                       vec;
@@ -124,7 +124,7 @@ subpool_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   if (active && n > 0) {
-    const size_t row_stride = static_cast<size_t>(row_vecs);  // in uint4 units
+    const size_t row_stride = static_cast<size_t>(input_row_stride(cap) / 8);  // in uint4 units
     const uint4* base = reinterpret_cast<const uint4*>(src) +
                         (static_cast<size_t>(b) * N + P + static_cast<size_t>(run) * kLen) * row_stride + vec;
     int r = 0;

@@ -47,8 +47,9 @@ bool encode_bnhd(CUtensorMap* map, const void* ptr, const vsa::Geometry& g) {
   if (!enc) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(vsa::kHeadDim), static_cast<cuuint64_t>(g.H),
                               static_cast<cuuint64_t>(g.N), static_cast<cuuint64_t>(g.B)};
-  const cuuint64_t row = static_cast<cuuint64_t>(vsa::kHeadDim) * 2;
-  const cuuint64_t strides[3] = {row, row * g.H, row * g.H * static_cast<cuuint64_t>(g.N)};
+  const cuuint64_t head = static_cast<cuuint64_t>(vsa::kHeadDim) * 2;
+  const cuuint64_t row = static_cast<cuuint64_t>(vsa::input_row_stride(g)) * 2;  // bytes between token rows
+  const cuuint64_t strides[3] = {head, row, row * static_cast<cuuint64_t>(g.N)};
   const cuuint32_t box[4] = {64, 1, 64, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
@@ -337,16 +338,25 @@ namespace {
 // the pooled statistics and word 7 come from vsa_preprocess and are kept).
 // Output layout: null `rows` means the packed [B, N, H, 128] tensor `out`.
 // Lengths: null means the plan's own; otherwise device memory read by the kernels.
+// in_row_stride: elements between token rows of q, k, v and gate (0: packed, H * 128).
 vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const void* v, const void* gate,
                           void* out, void* workspace, size_t workspace_bytes, void* stream,
                           bool pool_ready, const vsa_output_rows_t* rows = nullptr,
-                          const vsa_lengths_t* lengths = nullptr) {
+                          const vsa_lengths_t* lengths = nullptr, int64_t in_row_stride = 0) {
   if (!plan || !q || !k || !v || !out || !workspace) return VSA_ERR_INVALID_ARG;
   if (lengths && !aligned(lengths, 8)) return VSA_ERR_INVALID_ARG;
   if (!gate && !plan->subblock) return VSA_ERR_INVALID_ARG;  // SubBlock routing has no gate
   if (workspace_bytes < plan->ws_bytes || !aligned(workspace, kAlign)) return VSA_ERR_INVALID_ARG;
+  if (in_row_stride < 0 || (in_row_stride > 0 && (in_row_stride < static_cast<int64_t>(plan->g.H) * vsa::kHeadDim ||
+                                                   in_row_stride % 8 != 0)))
+    return VSA_ERR_INVALID_ARG;
+  if (in_row_stride > (int64_t(1) << 24)) return VSA_ERR_UNSUPPORTED;
   const void* ins[4] = {q, k, v, gate};
-  const size_t tb = plan->tensor_bytes;
+  // bytes one input spans: B * N rows of in_row_stride elements, the last one read up to its H * 128 channels
+  const size_t tb = in_row_stride == 0 ? plan->tensor_bytes
+                                       : (static_cast<size_t>(plan->g.B) * plan->g.N - 1) *
+                                                 static_cast<size_t>(in_row_stride) * 2 +
+                                             static_cast<size_t>(plan->g.H) * vsa::kHeadDim * 2;
   // bytes the output spans: the packed tensor, or B * out_rows rows of out_row_stride elements
   size_t out_span = tb;
   if (rows) {
@@ -370,7 +380,8 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
   DeviceGuard guard(plan->device);
   if (!guard.ok) return VSA_ERR_CUDA;
   NvtxRange range(plan->subblock ? "vsa_forward (SubBlock)" : "vsa_forward");
-  const vsa::Geometry& g = plan->g;
+  vsa::Geometry g = plan->g;
+  g.row_stride = in_row_stride;
   CUtensorMap mq, mk, mv, mg;
   // without a gate (SubBlock routing) the gate map points at q; the kernel never reads it
   if (!encode_bnhd(&mq, q, g) || !encode_bnhd(&mk, k, g) || !encode_bnhd(&mv, v, g) ||
@@ -490,7 +501,7 @@ vsa_status_t vsa_forward_ex(vsa_plan_t plan, const vsa_forward_args_t* a, void* 
   if (!a) return VSA_ERR_INVALID_ARG;
   void* out = a->rows ? a->rows->out : a->out;
   return forward_impl(plan, a->q, a->k, a->v, a->gate, out, workspace, workspace_bytes, stream, a->preprocessed != 0,
-                      a->rows, a->lengths);
+                      a->rows, a->lengths, a->in_row_stride);
 }
 
 vsa_status_t vsa_forward_rows(vsa_plan_t plan, const void* q, const void* k, const void* v, const void* gate,

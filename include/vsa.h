@@ -280,7 +280,8 @@ vsa_status_t vsa_forward_rows(vsa_plan_t plan, const void* q, const void* k, con
                               size_t workspace_bytes, void* stream);
 
 /* The general forward: every option of the entry points above in one call.
- *   q, k, v, gate : as vsa_forward (gate may be NULL for a SubBlock plan)
+ *   q, k, v, gate : as vsa_forward (gate may be NULL for a SubBlock plan), or
+ *                   head slices of wider rows (in_row_stride)
  *   out           : packed bf16 [batch, N, num_heads, 128] output, used when
  *                   rows is NULL
  *   rows          : output rows (vsa_forward_rows), or NULL
@@ -288,6 +289,18 @@ vsa_status_t vsa_forward_rows(vsa_plan_t plan, const void* q, const void* k, con
  *                   NULL for the plan's own
  *   preprocessed  : nonzero when q, k, v, gate and the pooled statistics come
  *                   from vsa_preprocess on this workspace and stream
+ *   in_row_stride : elements between consecutive token rows of q, k, v and
+ *                   gate; 0 means num_heads * 128 (packed). Otherwise a
+ *                   multiple of 8, >= num_heads * 128 and <= 2^24: channel c
+ *                   of head h of token n of batch b is read at
+ *                   x + (b * N + n) * in_row_stride + h * 128 + c. This is the
+ *                   head split of "UniServe: serving FastH3 at its fastest",
+ *                   section "The FastH3 workload" (each of 4 GPUs attends for
+ *                   14 of the 56 heads): a plan of num_heads = 14 given
+ *                   q + 14 r * 128 and in_row_stride = 56 * 128 computes heads
+ *                   14 r .. 14 r + 13 of a 56-head projection in place, and
+ *                   rows (out_row_stride = 56 * 128, out + 14 r * 128) writes
+ *                   them into the matching head slice of a 56-head output.
  * With lengths, preprocessed and rows together, one captured graph runs the
  * whole serving step: pack and normalise a request from its capacity-padded
  * projection buffer, attend, and write the combined rows into the all-to-all
@@ -301,6 +314,7 @@ typedef struct {
   const vsa_output_rows_t* rows;
   const vsa_lengths_t* lengths;
   int32_t preprocessed;
+  int64_t in_row_stride;
 } vsa_forward_args_t;
 
 vsa_status_t vsa_forward_ex(vsa_plan_t plan, const vsa_forward_args_t* args, void* workspace,

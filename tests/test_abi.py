@@ -227,6 +227,16 @@ def test_forward_ex_and_lengths_validation(lib):
         _, _, ws_sub = bsv.vsa_plan_info(sub)
         args = bsv.vsa_forward_args_t(g, 2 * g, 3 * g, None, 6 * g, None, 12 * g + 4, 0)   # SubBlock, misaligned lengths
         assert lib.vsa_forward_ex(sub, ctypes.byref(args), wsp, ws_sub, None) == bsv.VSA_ERR_INVALID_ARG
+        # input row stride: below H x 128, not a multiple of 8, negative; beyond 2^24 is unsupported
+        for bad in (255, 260, -8):
+            args = bsv.vsa_forward_args_t(g, 2 * g, 3 * g, 4 * g, 6 * g, None, None, 0, bad)
+            assert lib.vsa_forward_ex(plan, ctypes.byref(args), wsp, ws, None) == bsv.VSA_ERR_INVALID_ARG, bad
+        args = bsv.vsa_forward_args_t(g, 2 * g, 3 * g, 4 * g, 6 * g, None, None, 0, (1 << 24) + 8)
+        assert lib.vsa_forward_ex(plan, ctypes.byref(args), wsp, ws, None) == bsv.VSA_ERR_UNSUPPORTED
+        # a wider input row makes the input span larger: an output right after the packed size now overlaps it
+        tb = (64 + 64 + 1024) * 2 * 128 * 2
+        args = bsv.vsa_forward_args_t(g, 2 * g, 3 * g, 4 * g, g + tb, None, None, 0, 4 * 128)
+        assert lib.vsa_forward_ex(plan, ctypes.byref(args), wsp, ws, None) == bsv.VSA_ERR_INVALID_ARG
         assert lib.vsa_forward_lengths(plan, None, ctypes.c_void_p(g), ctypes.c_void_p(2 * g), ctypes.c_void_p(3 * g),
                                        ctypes.c_void_p(4 * g), ctypes.c_void_p(6 * g), wsp, ws,
                                        None) == bsv.VSA_ERR_INVALID_ARG
