@@ -35,12 +35,13 @@
 // raised, and the row sums and O^T are rescaled. Row sums are per-lane
 // partials, reduced once per item.
 //
-// Warp roles (640 threads): warp 0 fetches the items and issues the TMA loads
-// of the K blocks (3-stage ring), warp 19 those of the V blocks (2-stage ring),
-// four lanes each issuing one 8 KB box; warp 1 owns TMEM, loads Q (one buffer,
-// reloaded once the item's last S^T product has completed) and issues the S^T
-// products, warp 18 the O^T products (two TMEM accumulators, alternating by
-// item), each MMA warp converged with one elected lane issuing; warps 2-17
+// Warp roles (640 threads): warp 0 fetches the items, loads each item's Q tile
+// as soon as it has fetched it (two buffers, alternating by item) and issues
+// the TMA loads of the K blocks (3-stage ring), warp 19 those of the V blocks
+// (2-stage ring), four lanes each issuing one 8 KB box; warp 1 owns TMEM and
+// issues the S^T products, warp 18 the O^T products (two TMEM accumulators,
+// alternating by item; P^T in a 2-stage ring), each MMA warp converged with
+// one elected lane issuing; warps 2-17
 // are four softmax warpgroups (16 query columns each) that also run the
 // epilogue. Every wait is bounded (see ptx.cuh); a named barrier
 // is always reached by all of its threads.
@@ -62,12 +63,13 @@ constexpr int kSoftmaxWarps = 4 * kSoftmaxWGs;
 static_assert(kCols == 16, "the softmax code below is written for 16 columns per warpgroup");
 constexpr int kNumK = 3;
 constexpr int kNumV = 2;
+constexpr int kNumQ = 2;                           // Q buffers, alternating by item
 constexpr uint32_t kQBytes = 64 * kHeadDim * 2;    // 16 KB
 constexpr uint32_t kKVBytes = 128 * kHeadDim * 2;  // 32 KB, one 128-key block
 constexpr uint32_t kPBytes = 128 * 64 * 2;         // 16 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr int kNumS = 3;                 // S^T buffers in TMEM
-constexpr int kNumP = 3;                 // P^T buffers in shared memory
+constexpr int kNumP = 2;                 // P^T buffers in shared memory
 constexpr int kNumO = 2;                 // O^T accumulators in TMEM, alternating by item
 constexpr uint32_t kColS1 = 64;          // S^T buffer b at column b * kColS1
 constexpr uint32_t kColO = kNumS * kColS1;  // O^T accumulator a at column kColO + 64 a
@@ -78,7 +80,7 @@ constexpr float kFastLimitSum = 18446744073709551616.0f;  // 2^64: fast-mode bou
 constexpr uint32_t kBarSoftmaxAll = 1 + kSoftmaxWGs;  // named barrier over all softmax warps
 
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kQBytes;
+constexpr uint32_t kOffK = kOffQ + kNumQ * kQBytes;
 constexpr uint32_t kOffV = kOffK + kNumK * kKVBytes;
 constexpr uint32_t kOffP = kOffV + kNumV * kKVBytes;
 constexpr uint32_t kOffBar = kOffP + kNumP * kPBytes;
@@ -89,13 +91,13 @@ constexpr uint32_t kOffGeo = kOffSlot + 16;            // this forward's geometr
 constexpr uint32_t kSmemBytes = kOffGeo + 32 + 1024;   // + 1024-byte alignment slack
 
 // barrier indices
-constexpr int kBarQFull = 0;
-constexpr int kBarQEmpty = 1;
+constexpr int kBarQFull = 0;              // + item % kNumQ
+constexpr int kBarQEmpty = kBarQFull + kNumQ;
 // A K slot is released by the S-full barrier of the block that read it (the
 // same commit, so no separate barrier), a V slot by the P-empty barrier of its
 // block: one commit per MMA group. Each loader waits on those barriers in
 // block order, so none of its parity waits can fall two phases behind.
-constexpr int kBarKFull = 2;
+constexpr int kBarKFull = kBarQEmpty + kNumQ;
 constexpr int kBarVFull = kBarKFull + kNumK;
 constexpr int kBarSFull = kBarVFull + kNumV;
 constexpr int kBarSEmpty = kBarSFull + kNumS;
@@ -245,8 +247,10 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
 
   if (tid == 0) {
     *s_geo = geo;
-    mbar_init(bar(kBarQFull), 1);
-    mbar_init(bar(kBarQEmpty), 1);
+    for (int s = 0; s < kNumQ; ++s) {
+      mbar_init(bar(kBarQFull + s), 1);
+      mbar_init(bar(kBarQEmpty + s), 1);
+    }
     for (int s = 0; s < kNumK; ++s) mbar_init(bar(kBarKFull + s), 1);
     for (int s = 0; s < kNumV; ++s) mbar_init(bar(kBarVFull + s), 1);
     for (int s = 0; s < kNumS; ++s) {
@@ -334,6 +338,20 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             items[s] = item;
             mbar_arrive(bar(kBarItemFull + s));
           }
+          // The item's Q tile, into buffer n % kNumQ as soon as the item is
+          // known: that buffer was last read by the S^T products of item
+          // n - kNumQ, which completed before this warp could load the K
+          // blocks of item n - 1 (the S^T products run in item order).
+          if (ok && item >= 0) {
+            const int qb = n % kNumQ;
+            if (n >= kNumQ) ok = mbar_wait(bar(kBarQEmpty + qb), ((n - kNumQ) / kNumQ) & 1, err, 0x510u, 64);
+            if (ok) {
+              const Item qi = decode_item(p, G, item);
+              mbar_arrive_expect_tx(bar(kBarQFull + qb), kQBytes);
+              for (int c = 0; c < 2; ++c)
+                tma_load_4d(sQ + qb * kQBytes + c * 8192, &map_q, 64 * c, qi.h, qi.q_row0, qi.b, bar(kBarQFull + qb));
+            }
+          }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         item = __shfl_sync(0xffffffffu, item, 0);
@@ -344,11 +362,8 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       const Item it = decode_item(p, G, item);
       const int nblk = (it.n_kv + 1) / 2;
       if (!v_warp && lane == 0) {
-        // Into L2 ahead of use: the item's Q tile (loaded once its S^T products
-        // start) and, for a video item, its gate tile and coarse row (read by
-        // the epilogue, an item's duration later).
-        tma_prefetch_l2_4d(&map_q, 0, it.h, it.q_row0, it.b);
-        tma_prefetch_l2_4d(&map_q, 64, it.h, it.q_row0, it.b);
+        // Into L2 ahead of use: for a video item, its gate tile and coarse
+        // row (read by the epilogue, an item's duration later).
         if (it.video && p.coarse) {
           tma_prefetch_l2_4d(&map_g, 0, it.h, it.q_row0, it.b);
           tma_prefetch_l2_4d(&map_g, 64, it.h, it.q_row0, it.b);
@@ -425,29 +440,22 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       }
     }
   } else if (warp == kWarpMmaS) {
-    // ------------------------------------------------------------ Q loads, S^T = K Q^T issuer
+    // ------------------------------------------------------------ S^T = K Q^T issuer
     // The whole warp runs the loop (warp-uniform descriptors); one elected lane
-    // issues the products and commits, lane 0 the Q loads.
+    // issues the products and commits. Item n reads Q buffer n % kNumQ (loaded
+    // by the item-fetching warp) and releases it after its last S^T product.
     bool ok = true;
-    int item = read_item(0, ok);
     const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
     const uint64_t dk0 = smem_desc_sw128(sK, 16, 1024);
-    const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
-    auto load_q = [&](int itm) {
-      if (lane == 0) {
-        const Item qi = decode_item(p, G, itm);
-        mbar_arrive_expect_tx(bar(kBarQFull), kQBytes);
-        for (int c = 0; c < 2; ++c)
-          tma_load_4d(sQ + c * 8192, &map_q, 64 * c, qi.h, qi.q_row0, qi.b, bar(kBarQFull));
-      }
-      __syncwarp();
-    };
-    if (ok && item >= 0) load_q(item);
     uint32_t g = 0;  // blocks issued so far, over all items
-    for (int n = 0; ok && item >= 0; ++n) {
+    for (int n = 0; ok; ++n) {
+      const int item = read_item(n, ok);
+      if (!ok || item < 0) break;
       const Item it = decode_item(p, G, item);
       const int nblk = (it.n_kv + 1) / 2;
-      ok = mbar_wait_warp(bar(kBarQFull), n & 1, err, 0x500u, 64);
+      const int qb = n % kNumQ;
+      const uint64_t dq0 = smem_desc_sw128(sQ + qb * kQBytes, 16, 1024);
+      ok = mbar_wait_warp(bar(kBarQFull + qb), (n / kNumQ) & 1, err, 0x500u, 64);
       for (int i = 0; i < nblk && ok; ++i, ++g) {
         const int ks = g % kNumK, sb = g % kNumS;
         ok = mbar_wait_warp(bar(kBarKFull + ks), (g / kNumK) & 1, err, 0x600u, 64) &&
@@ -464,13 +472,8 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         umma_commit_elect(bar(kBarSFull + sb));  // also releases K slot ks
       }
       if (!ok) break;
-      // Q stays in use until the item's last S^T product completes
-      umma_commit_elect(bar(kBarQEmpty));
-      item = read_item(n + 1, ok);
-      if (ok && item >= 0) {
-        ok = mbar_wait_warp(bar(kBarQEmpty), n & 1, err, 0x510u, 64);
-        if (ok) load_q(item);
-      }
+      // Q buffer qb stays in use until the item's last S^T product completes
+      umma_commit_elect(bar(kBarQEmpty + qb));
     }
   } else if (warp == kWarpMmaPV) {
     // ------------------------------------------------------------ O^T += V^T P^T issuer
