@@ -25,7 +25,7 @@ VSA_ERR_UNSUPPORTED = 2
 VSA_ERR_CUDA = 3
 VSA_ERR_DEVICE_TIMEOUT = 4
 VSA_ERR_INTERNAL = 5
-STATIC_WORKSPACE_BYTES = 32 * 1024 * 1024  # VSA_STATIC_WORKSPACE_BYTES in include/vsa.h
+STATIC_WORKSPACE_BYTES = 64 * 1024 * 1024  # VSA_STATIC_WORKSPACE_BYTES in include/vsa.h
 
 
 class VsaError(RuntimeError):

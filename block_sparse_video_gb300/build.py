@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libvsa.so")
-SOURCES = ["pool.cu", "preprocess.cu", "coarse_topk.cu", "subblock_router.cu", "fine_attn.cu", "host_rows.cu", "vsa_api.cu", "vsa_static.cu", "vsa_diag.cu"]
+SOURCES = ["pool.cu", "preprocess.cu", "coarse_topk.cu", "coarse_tc.cu", "subblock_router.cu", "fine_attn.cu", "host_rows.cu", "vsa_api.cu", "vsa_static.cu", "vsa_diag.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,630 @@
+// Coarse tile attention fused with the top-k tile selection, both products on
+// the tcgen05 tensor cores.
+//
+// For each (batch, head) and each video query tile t ("UniServe: serving
+// FastH3 at its fastest", section "The FastH3 workload"):
+//   s[t][j] = pooled_q[t] . pooled_k[j] / sqrt(128)        over all T video tiles
+//   selection(t) = the k largest s[t][j], ties to the lower j, ascending
+//   coarse[t] = sum_j softmax_j(s[t][.]) * pooled_v[j]
+//
+// Operands. A split kernel writes the pooled Q, K and V again as bf16 rows of
+// a head plus a remainder (x ~ hi + lo, ~2^-16 relative), so that each fp32
+// product is hi.hi + hi.lo + lo.hi: three bf16 MMAs accumulating in fp32 in
+// TMEM. Rows past the request's T are zeros.
+//
+// Work unit: 64 query tiles of one (batch, head). The grid is persistent (one
+// CTA per SM at most, units taken in a fixed stride), and each CTA owns a
+// scratch row buffer in global memory (64 rows of T_pad floats, L2-resident).
+// Per unit, three phases separated by CTA barriers:
+//   A. scores, transposed so that the MMA has M = 128:
+//        S^T[128 keys x 64 queries] = Kbar_chunk . Qbar^T      (A, B K-major)
+//      for each 128-key chunk; four warps move each chunk from TMEM (lane =
+//      key, column = query), scaled by 1/sqrt(128), into the scratch rows;
+//   B. one warp per query row: the row into registers, the exact top-k (a
+//      counting threshold search; the radix select where scores tie at the
+//      cut), the row maximum m, l = sum_j exp(s_j - m), and p_j = exp(s_j - m)
+//      written back over the row's own bytes as bf16 hi then bf16 lo rows;
+//   C. the coarse product, transposed the same way:
+//        C^T[128 dims x 64 queries] = Vbar_chunk^T . P^T       (A MN-major, B K-major)
+//      accumulated over the chunks, with P loaded back by TMA; four warps
+//      divide by l and store coarse rows.
+// Score errors of ~2^-16 relative sit far inside the selection's 1e-3 tie
+// band; the selection itself is an integer decision on the fp32 scores.
+//
+// Warp roles (12 warps): warp 0 issues the TMA loads (four issuing lanes, one
+// 8 KB box each) through a ring of 32 KB stages; warps 1 and 2 issue the
+// MMAs, converged with one elected lane each, splitting every chunk's 24
+// products between two accumulators (a single issuer leaves the pipe idle
+// between N = 64 MMAs); warps 4-7 move scores and outputs out of TMEM; all 12
+// warps run phase B. Every wait is bounded.
+#include <cmath>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+#include "rank_helpers.cuh"
+
+namespace vsa {
+namespace {
+
+constexpr int kThreads = 384;                 // 12 warps: up to 168 registers a thread for a row in registers
+constexpr int kWarps = kThreads / 32;
+constexpr int kRows = 64;                     // query tiles per unit: the MMA's N
+constexpr int kChunk = 128;                   // key tiles per chunk: the MMA's M
+constexpr int kStages = 5;                    // ring stages of 32 KB
+constexpr uint32_t kStageBytes = kChunk * kHeadDim * 2;
+constexpr uint32_t kQBytes = 2 * kRows * kHeadDim * 2;  // Qbar hi and lo, 64 rows each
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpEpi0 = 4;
+constexpr uint32_t kTmemCols = 256;           // two accumulator pairs of 64 columns
+constexpr unsigned int kDetailQ = 0xE00, kDetailFull = 0xE10, kDetailEmpty = 0xE20, kDetailAcc = 0xE30,
+                       kDetailAccEmpty = 0xE40, kDetailC = 0xE50;
+
+// shared memory from a 1024-byte aligned base: Qbar hi/lo, the ring, then
+// the row sums, the selection histograms, the barriers and the TMEM slot
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffRing = kOffQ + kQBytes;
+constexpr uint32_t kOffL = kOffRing + kStages * kStageBytes;
+constexpr uint32_t kOffHist = kOffL + kRows * 4;
+constexpr uint32_t kOffBar = kOffHist + kWarps * kBins * 4;
+constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = kBarFull + kStages, kBarAccFull = kBarEmpty + kStages,
+              kBarAccEmpty = kBarAccFull + 2, kBarC = kBarAccEmpty + 2, kNumBars = kBarC + 1;
+constexpr uint32_t kOffSlot = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+
+struct CoarseParams {
+  Geometry cap;             // the plan's geometry: T_cap, k_cap and the layouts
+  DeviceLengths dl;
+  int tp_cap;               // padded rows per (b, h) of the hi/lo operands and of a scratch row
+  int n_units;              // B * H * ceil(T_cap / 64)
+  float* scratch;           // [grid][64][tp_cap] floats
+  float* coarse;            // [B, H, T_cap, 128]
+  int32_t* tile_index;      // [B, H, T_cap, k_cap]
+  unsigned int* err;
+};
+
+// The k largest of a row held in registers, lane l holding entries l + 32 i
+// (-inf past T), written ascending to dst[0 .. k): the same set, with ties
+// to the lower index, as warp_select_topk_count (a counting search for a
+// threshold with exactly k entries at or above it; the radix select where
+// entries tie at the cut or a score is not finite). h: kBins ints of shared
+// memory for the radix select.
+template <int NR>
+__device__ __forceinline__ void select_topk_regs(const float (&v)[NR], int T, int k, int* h, int32_t* dst,
+                                                 int lane) {
+  const unsigned full = 0xffffffffu;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  if (k >= T) {
+    for (int j = lane; j < T; j += 32) dst[j] = j;
+    return;
+  }
+  float vmin = INFINITY, vmax = -INFINITY, s1 = 0.f, s2 = 0.f;
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    if (32 * i + lane < T) {
+      const float x = v[i];
+      vmin = fminf(vmin, x);
+      vmax = fmaxf(vmax, x);
+      s1 += x;
+      s2 = fmaf(x, x, s2);
+      bad |= !(fabsf(x) <= 3.0e38f);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    vmin = fminf(vmin, __shfl_xor_sync(full, vmin, o));
+    vmax = fmaxf(vmax, __shfl_xor_sync(full, vmax, o));
+    s1 += __shfl_xor_sync(full, s1, o);
+    s2 += __shfl_xor_sync(full, s2, o);
+  }
+  auto count_ge = [&](float x) {
+    int c = 0;
+#pragma unroll
+    for (int i = 0; i < NR; ++i) c += v[i] >= x;  // -inf past T never counts (x > vmin >= -inf)
+    return static_cast<int>(__reduce_add_sync(full, static_cast<unsigned>(c)));
+  };
+  float theta = 0.f;
+  bool found = false;
+  if (!__any_sync(full, bad) && k >= 1) {
+    float lo = vmin, hi = nextafterf(vmax, INFINITY);
+    float flo = static_cast<float>(T - k), fhi = static_cast<float>(-k);
+    int kept = 0;
+    const float mean = s1 / static_cast<float>(T);
+    const float sd = sqrtf(fmaxf(s2 / static_cast<float>(T) - mean * mean, 0.f));
+    float x = mean + normcdfinvf(1.f - static_cast<float>(k) / static_cast<float>(T)) * sd;
+#pragma unroll 1
+    for (int it = 0; it < 48; ++it) {
+      if (it > 0) x = lo + (hi - lo) * (flo / (flo - fhi));
+      if (!(x > lo && x < hi)) x = 0.5f * (lo + hi);
+      if (!(x > lo && x < hi)) break;
+      const int c = count_ge(x);
+      if (c == k) {
+        theta = x;
+        found = true;
+        break;
+      }
+      if (c > k) {
+        lo = x;
+        flo = static_cast<float>(c - k);
+        if (kept > 0) fhi *= 0.5f;
+        kept = 1;
+      } else {
+        hi = x;
+        fhi = static_cast<float>(c - k);
+        if (kept < 0) flo *= 0.5f;
+        kept = -1;
+      }
+    }
+  }
+  if (found) {
+    int written = 0;
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+      const bool sel = 32 * i + lane < T && v[i] >= theta;
+      const unsigned selb = __ballot_sync(full, sel);
+      if (sel) dst[written + __popc(selb & lt_mask)] = 32 * i + lane;
+      written += __popc(selb);
+    }
+    return;
+  }
+  // radix select, 8 bits per pass from the top, over the order-preserving
+  // integer image of the scores (-0 and +0 alike)
+  uint32_t prefix = 0u, pmask = 0u;
+  int rem = k;
+#pragma unroll 1
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int b = lane; b < kBins; b += 32) h[b] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+      if (32 * i + lane < T) {
+        const uint32_t key = order_key(v[i]);
+        if ((key & pmask) == prefix) atomicAdd(&h[(key >> shift) & 0xFFu], 1);
+      }
+    }
+    __syncwarp();
+    int c[8], lsum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { c[i] = h[255 - 8 * lane - i]; lsum += c[i]; }
+    int incl = lsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(full, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int excl = incl - lsum;
+    const unsigned hit = __ballot_sync(full, excl < rem && incl >= rem);
+    const int src = __ffs(hit) - 1;
+    int digit = 0, above = 0;
+    if (lane == src) {
+      int run = excl;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (run + c[i] >= rem) { digit = 255 - 8 * lane - i; above = run; break; }
+        run += c[i];
+      }
+    }
+    digit = __shfl_sync(full, digit, src);
+    above = __shfl_sync(full, above, src);
+    prefix |= static_cast<uint32_t>(digit) << shift;
+    pmask |= 0xFFu << shift;
+    rem -= above;
+    __syncwarp();
+  }
+  int written = 0, eq_seen = 0;
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    const int j = 32 * i + lane;
+    const uint32_t key = j < T ? order_key(v[i]) : 0u;
+    const bool is_gt = j < T && key > prefix;
+    const bool is_eq = j < T && key == prefix;
+    const unsigned eqb = __ballot_sync(full, is_eq);
+    const bool sel = is_gt || (is_eq && eq_seen + __popc(eqb & lt_mask) < rem);
+    const unsigned selb = __ballot_sync(full, sel);
+    if (sel) dst[written + __popc(selb & lt_mask)] = j;
+    written += __popc(selb);
+    eq_seen += __popc(eqb);
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+template <int NR>
+__global__ void __launch_bounds__(kThreads, 1)
+coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
+                 const __grid_constant__ CUtensorMap map_kh, const __grid_constant__ CUtensorMap map_kl,
+                 const __grid_constant__ CUtensorMap map_vh, const __grid_constant__ CUtensorMap map_vl,
+                 const __grid_constant__ CUtensorMap map_p, const CoarseParams p) {
+  const DynGeom dg = dyn_geom(p.cap, p.dl);
+  if (!dg.valid) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.dl.invalid = 1u;
+    return;
+  }
+  const int T = dg.T, k = dg.k, T_cap = p.cap.T, k_cap = p.cap.k;
+  const int n_chunks = (T + kChunk - 1) / kChunk;
+  const int groups_cap = (T_cap + kRows - 1) / kRows;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  float* l_row = reinterpret_cast<float*>(smem + kOffL);
+  int* hist = reinterpret_cast<int*>(smem + kOffHist);
+  auto bar = [&](int i) { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
+
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  unsigned int* err = p.err;
+  if (tid == 0) {
+    mbar_init(bar(kBarQ), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kBarFull + s), 1);
+      mbar_init(bar(kBarEmpty + s), 2);  // both issuers read every stage
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar(kBarAccFull + a), 2);  // one commit per issuer
+      mbar_init(bar(kBarAccEmpty + a), 4);  // the four epilogue warps
+    }
+    mbar_init(bar(kBarC), 2);
+    fence_barrier_init();
+  }
+  if (warp == kWarpMma) tmem_alloc(smem_u32(tslot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  float* rows = p.scratch + static_cast<size_t>(blockIdx.x) * kRows * p.tp_cap;  // this CTA's scratch rows
+  const float scale = 0.08838834764831845f;  // 1/sqrt(128)
+  bool failed = false;
+
+  // Ring positions and accumulator-pair uses, counted alike by every warp
+  // over all units: phase A takes 2 stages (K hi, K lo) and one accumulator
+  // pair per chunk, phase C 3 stages (V hi, V lo, P hi + lo) per chunk.
+  uint32_t ring0 = 0, acc0 = 0, units_done = 0;
+  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+    const int bh = u / groups_cap;
+    const int q0 = (u - bh * groups_cap) * kRows;
+    if (q0 >= T) continue;  // uniform: a query group past the request's tiles
+    const int n_rows = min(kRows, T - q0);
+
+    // ------------------------------------------------------------ phase A: scores
+    if (warp == kWarpTma) {
+      bool lane_failed = false;
+      if (lane < 4) {
+        const int half = lane >> 1, rg = lane & 1;
+        if (lane == 0) mbar_arrive_expect_tx(bar(kBarQ), kQBytes);
+        // Qbar: lane l loads channel half l & 1 of the hi (l < 2) or lo rows
+        tma_load_4d(sbase + kOffQ + (lane >> 1) * (kQBytes / 2) + (lane & 1) * 8192, (lane >> 1) ? &map_ql : &map_qh,
+                    64 * (lane & 1), q0, bh, 0, bar(kBarQ));
+        for (int i = 0; i < 2 * n_chunks && !lane_failed; ++i) {
+          const uint32_t r = ring0 + i;
+          const int st = r % kStages;
+          if (r >= kStages && !mbar_wait(bar(kBarEmpty + st), ((r / kStages) - 1) & 1, err, kDetailEmpty)) {
+            lane_failed = true;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(bar(kBarFull + st), kStageBytes);
+          tma_load_4d(sbase + kOffRing + st * kStageBytes + half * 16384 + rg * 8192, (i & 1) ? &map_kl : &map_kh,
+                      64 * half, kChunk * (i / 2) + 64 * rg, bh, 0, bar(kBarFull + st));
+        }
+      }
+      failed = __any_sync(0xffffffffu, lane_failed);
+    } else if (warp == kWarpMma || warp == kWarpMma + 1) {
+      // issuer 0: hi.hi over k-steps 0-7, then lo.hi over 0-3; issuer 1:
+      // hi.lo over 0-7, then lo.hi over 4-7
+      const int w = warp - kWarpMma;
+      const uint32_t idesc = idesc_bf16_f32(128, kRows, 0, 0);
+      const uint64_t dq_hi = smem_desc_sw128(sbase + kOffQ, 16, 1024);
+      const uint64_t dq_lo = smem_desc_sw128(sbase + kOffQ + kQBytes / 2, 16, 1024);
+      const uint64_t dq_b = w == 0 ? dq_hi : dq_lo;
+      failed = !mbar_wait_warp(bar(kBarQ), units_done & 1, err, kDetailQ);
+      for (int c = 0; c < n_chunks && !failed; ++c) {
+        const uint32_t au = acc0 + c;
+        const int a = au & 1;
+        if (au >= 2 && !mbar_wait_warp(bar(kBarAccEmpty + a), ((au / 2) - 1) & 1, err, kDetailAccEmpty)) {
+          failed = true;
+          break;
+        }
+        const uint32_t d = tbase + static_cast<uint32_t>((2 * a + w) * kRows);
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t r = ring0 + 2 * c + part;
+          const int st = r % kStages;
+          if (!mbar_wait_warp(bar(kBarFull + st), (r / kStages) & 1, err, kDetailFull)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t dk = smem_desc_sw128(sbase + kOffRing + st * kStageBytes, 16, 1024);
+          if (part == 0) {
+#pragma unroll
+            for (int s = 0; s < kHeadDim / 16; ++s) {
+              const uint32_t koff = ((s >> 2) * 16384 + (s & 3) * 32) >> 4;
+              const uint32_t qoff = ((s >> 2) * 8192 + (s & 3) * 32) >> 4;
+              umma_bf16_elect(d, dk + koff, dq_b + qoff, idesc, s > 0 ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < kHeadDim / 32; ++j) {
+              const int s = 4 * w + j;
+              const uint32_t koff = ((s >> 2) * 16384 + (s & 3) * 32) >> 4;
+              const uint32_t qoff = ((s >> 2) * 8192 + (s & 3) * 32) >> 4;
+              umma_bf16_elect(d, dk + koff, dq_hi + qoff, idesc, 1u);
+            }
+          }
+          umma_commit_elect(bar(kBarEmpty + st));
+        }
+        if (!failed) umma_commit_elect(bar(kBarAccFull + a));
+      }
+    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
+      // one lane quarter per warp: TMEM lane = key 128 c + 32 q + lane
+      const int q = warp % 4;
+      const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+      for (int c = 0; c < n_chunks && !failed; ++c) {
+        const uint32_t au = acc0 + c;
+        const int a = au & 1;
+        if (!mbar_wait_warp(bar(kBarAccFull + a), (au / 2) & 1, err, kDetailAcc)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const int key = kChunk * c + 32 * q + lane;
+#pragma unroll
+        for (int part = 0; part < kRows / 16; ++part) {
+          uint32_t x0[16], x1[16];
+          tmem_ld16(tbase + lane_off + static_cast<uint32_t>(2 * a * kRows + 16 * part), x0);
+          tmem_ld16(tbase + lane_off + static_cast<uint32_t>((2 * a + 1) * kRows + 16 * part), x1);
+          tmem_wait_ld();
+          if (key < T) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int r = 16 * part + j;
+              if (r < n_rows)
+                rows[static_cast<size_t>(r) * p.tp_cap + key] =
+                    (__uint_as_float(x0[j]) + __uint_as_float(x1[j])) * scale;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarAccEmpty + a));
+      }
+    }
+    ring0 += 2 * n_chunks;
+    acc0 += n_chunks;
+    failed = __syncthreads_or(failed);
+    if (failed) break;
+
+    // ------------------------------------------------------------ phase B: selection, softmax, P
+    for (int r = warp; r < n_rows; r += kWarps) {
+      float* row = rows + static_cast<size_t>(r) * p.tp_cap;
+      float v[NR];
+#pragma unroll
+      for (int i = 0; i < NR; ++i) {
+        const int j = 32 * i + lane;
+        v[i] = j < T ? row[j] : -INFINITY;
+      }
+      select_topk_regs<NR>(v, T, k, hist + warp * kBins,
+                           p.tile_index + (static_cast<size_t>(bh) * T_cap + q0 + r) * k_cap, lane);
+      float m = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < NR; ++i) m = fmaxf(m, v[i]);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float l = 0.f;
+      __nv_bfloat16* ph = reinterpret_cast<__nv_bfloat16*>(row);   // the row's first half: p hi
+      __nv_bfloat16* pl = ph + p.tp_cap;                          // second half: p lo
+      __syncwarp();  // every lane has read the row before it is overwritten
+#pragma unroll
+      for (int i = 0; i < NR; ++i) {
+        const int j = 32 * i + lane;
+        if (j < kChunk * n_chunks) {
+          const float e = j < T ? expf(v[i] - m) : 0.f;
+          l += e;
+          const __nv_bfloat16 h = __float2bfloat16_rn(e);
+          ph[j] = h;
+          pl[j] = __float2bfloat16_rn(e - __bfloat162float(h));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+      if (lane == 0) l_row[r] = l;
+    }
+    // P is read back by TMA (the async proxy): order these generic writes before it
+    fence_proxy_async_global();
+    failed = __syncthreads_or(failed);
+    if (failed) break;
+
+    // ------------------------------------------------------------ phase C: coarse product
+    if (warp == kWarpTma) {
+      bool lane_failed = false;
+      if (lane < 4) {
+        const int half = lane >> 1, kh = lane & 1;
+        for (int i = 0; i < 3 * n_chunks && !lane_failed; ++i) {
+          const uint32_t r = ring0 + i;
+          const int st = r % kStages, c = i / 3, part = i % 3;
+          if (r >= kStages && !mbar_wait(bar(kBarEmpty + st), ((r / kStages) - 1) & 1, err, kDetailEmpty)) {
+            lane_failed = true;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(bar(kBarFull + st), kStageBytes);
+          const uint32_t dst = sbase + kOffRing + st * kStageBytes + half * 16384 + kh * 8192;
+          if (part < 2) {
+            // Vbar rows: dims half `half`, keys 64 kh .. + 63 of the chunk
+            tma_load_4d(dst, part ? &map_vl : &map_vh, 64 * half, kChunk * c + 64 * kh, bh, 0, bar(kBarFull + st));
+          } else {
+            // P: plane `half` (hi, lo), keys 64 kh .. + 63 of the chunk, all 64 rows
+            tma_load_4d(dst, &map_p, kChunk * c + 64 * kh, half, 0, static_cast<int>(blockIdx.x), bar(kBarFull + st));
+          }
+        }
+      }
+      failed = __any_sync(0xffffffffu, lane_failed);
+    } else if (warp == kWarpMma || warp == kWarpMma + 1) {
+      // issuer 0: Vhi.Phi over k-steps 0-7, then Vlo.Phi over 0-3; issuer 1:
+      // Vhi.Plo over 0-7, then Vlo.Phi over 4-7; each into its own
+      // accumulator of 64 columns, summed in the epilogue
+      const int w = warp - kWarpMma;
+      const uint32_t idesc = idesc_bf16_f32(128, kRows, 1, 0);
+      const uint32_t d = tbase + static_cast<uint32_t>(w * kRows);
+      for (int c = 0; c < n_chunks && !failed; ++c) {
+        const uint32_t r = ring0 + 3 * c;
+        const int sv_hi = r % kStages, sv_lo = (r + 1) % kStages, sp = (r + 2) % kStages;
+        if (!mbar_wait_warp(bar(kBarFull + sv_hi), (r / kStages) & 1, err, kDetailFull) ||
+            !mbar_wait_warp(bar(kBarFull + sv_lo), ((r + 1) / kStages) & 1, err, kDetailFull) ||
+            !mbar_wait_warp(bar(kBarFull + sp), ((r + 2) / kStages) & 1, err, kDetailFull)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t pbase = sbase + kOffRing + sp * kStageBytes;
+        const uint64_t dp_hi = smem_desc_sw128(pbase, 16, 1024);
+        const uint64_t dp_lo = smem_desc_sw128(pbase + 16384, 16, 1024);
+        const uint64_t dv_hi = smem_desc_sw128(sbase + kOffRing + sv_hi * kStageBytes, 16384, 1024);
+        const uint64_t dv_lo = smem_desc_sw128(sbase + kOffRing + sv_lo * kStageBytes, 16384, 1024);
+        const uint64_t dp_b = w == 0 ? dp_hi : dp_lo;
+#pragma unroll
+        for (int s = 0; s < kChunk / 16; ++s) {
+          const uint32_t voff = (s * 2048) >> 4;
+          const uint32_t poff = ((s >> 2) * 8192 + (s & 3) * 32) >> 4;
+          umma_bf16_elect(d, dv_hi + voff, dp_b + poff, idesc, (c > 0 || s > 0) ? 1u : 0u);
+        }
+        umma_commit_elect(bar(kBarEmpty + sv_hi));
+#pragma unroll
+        for (int j = 0; j < kChunk / 32; ++j) {
+          const int s = 4 * w + j;
+          const uint32_t voff = (s * 2048) >> 4;
+          const uint32_t poff = ((s >> 2) * 8192 + (s & 3) * 32) >> 4;
+          umma_bf16_elect(d, dv_lo + voff, dp_hi + poff, idesc, 1u);
+        }
+        umma_commit_elect(bar(kBarEmpty + sv_lo));
+        umma_commit_elect(bar(kBarEmpty + sp));
+      }
+      if (!failed) umma_commit_elect(bar(kBarC));
+    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
+      const int q = warp % 4;
+      const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+      const int dim = 32 * q + lane;
+      if (!mbar_wait_warp(bar(kBarC), units_done & 1, err, kDetailC)) {
+        failed = true;
+      } else {
+        tc_fence_after();
+#pragma unroll
+        for (int part = 0; part < kRows / 16; ++part) {
+          uint32_t x0[16], x1[16];
+          tmem_ld16(tbase + lane_off + static_cast<uint32_t>(16 * part), x0);
+          tmem_ld16(tbase + lane_off + static_cast<uint32_t>(kRows + 16 * part), x1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int r = 16 * part + j;
+            if (r < n_rows)
+              p.coarse[(static_cast<size_t>(bh) * T_cap + q0 + r) * kHeadDim + dim] =
+                  (__uint_as_float(x0[j]) + __uint_as_float(x1[j])) / l_row[r];
+          }
+        }
+        tc_fence_before();
+      }
+    }
+    ring0 += 3 * n_chunks;
+    ++units_done;
+    failed = __syncthreads_or(failed);
+    if (failed) break;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) tmem_dealloc(tbase, kTmemCols);
+}
+
+// The pooled q, k, v (fp32 [B, H, T_cap, 128]) as bf16 hi and lo rows
+// ([B H][tp_cap][128] each, x ~ hi + lo), rows past the request's T zero.
+// One thread per 8 channels of one row of one tensor.
+__global__ void __launch_bounds__(256)
+split_kernel(const float* __restrict__ pq, const float* __restrict__ pk, const float* __restrict__ pv,
+             uint4* __restrict__ out, Geometry cap, DeviceLengths dl, int tp_cap) {
+  const DynGeom dg = dyn_geom(cap, dl);
+  if (!dg.valid) return;  // reported by the coarse kernel
+  const size_t per_tensor = static_cast<size_t>(cap.B) * cap.H * tp_cap * (kHeadDim / 8);
+  size_t idx = static_cast<size_t>(blockIdx.x) * 256 + threadIdx.x;
+  if (idx >= 3 * per_tensor) return;
+  const int tensor = static_cast<int>(idx / per_tensor);
+  idx -= tensor * per_tensor;
+  const int c8 = static_cast<int>(idx % (kHeadDim / 8));
+  const size_t row = idx / (kHeadDim / 8);
+  const int t = static_cast<int>(row % tp_cap);
+  const size_t bh = row / tp_cap;
+  float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (t < dg.T) {
+    const float* src = (tensor == 0 ? pq : tensor == 1 ? pk : pv) + (bh * cap.T + t) * kHeadDim + 8 * c8;
+    const float4 a = __ldg(reinterpret_cast<const float4*>(src));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(src) + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
+  uint32_t hi[4], lo[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) split_bf16_pair(x[2 * i], x[2 * i + 1], hi[i], lo[i]);
+  // tensor-major: [tensor][hi, lo][B H][tp_cap][128]
+  out[(2 * tensor) * per_tensor + idx] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  out[(2 * tensor + 1) * per_tensor + idx] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+template <int NR>
+cudaError_t launch_nr(const CUtensorMap (&maps)[7], const CoarseParams& p, int grid, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(coarse_tc_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  coarse_tc_kernel<NR><<<grid, kThreads, kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
+                                                              maps[5], maps[6], p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int coarse_tc_padded(const Geometry& g) { return (g.T + kChunk - 1) / kChunk * kChunk; }
+
+bool coarse_tc_supported(const Geometry& g) { return g.T <= kCoarseTcMaxT; }
+
+int coarse_tc_units(const Geometry& g) { return g.B * g.H * ((g.T + kRows - 1) / kRows); }
+
+size_t coarse_tc_operand_bytes(const Geometry& g) {
+  return 6 * static_cast<size_t>(g.B) * g.H * coarse_tc_padded(g) * kHeadDim * 2;
+}
+
+size_t coarse_tc_scratch_bytes(const Geometry& g) {
+  const int slots = coarse_tc_units(g) < kCoarseTcMaxSlots ? coarse_tc_units(g) : kCoarseTcMaxSlots;
+  return static_cast<size_t>(slots) * kRows * coarse_tc_padded(g) * sizeof(float);
+}
+
+cudaError_t launch_split(const Geometry& g, const float* pq, const float* pk, const float* pv, void* operands,
+                         const DeviceLengths& dl, cudaStream_t stream) {
+  const int tp = coarse_tc_padded(g);
+  const size_t n = 3 * static_cast<size_t>(g.B) * g.H * tp * (kHeadDim / 8);
+  split_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(pq, pk, pv, static_cast<uint4*>(operands),
+                                                                           g, dl, tp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_coarse_tc(const Geometry& g, const CUtensorMap (&maps)[7], float* scratch, float* coarse,
+                             int32_t* tile_index, unsigned int* err, const DeviceLengths& dl, int num_sms,
+                             cudaStream_t stream) {
+  CoarseParams p;
+  p.cap = g;
+  p.dl = dl;
+  p.tp_cap = coarse_tc_padded(g);
+  p.n_units = coarse_tc_units(g);
+  p.scratch = scratch;
+  p.coarse = coarse;
+  p.tile_index = tile_index;
+  p.err = err;
+  int grid = p.n_units < num_sms ? p.n_units : num_sms;
+  if (grid > kCoarseTcMaxSlots) grid = kCoarseTcMaxSlots;
+  // a query row's scores in NR registers per lane (the same results for any
+  // NR that holds the row: entries past T take no part)
+  static_assert(kCoarseTcMaxT <= 32 * 72, "rows held in at most 72 registers per lane");
+  if (g.T <= 32 * 20) return launch_nr<20>(maps, p, grid, stream);
+  if (g.T <= 32 * 40) return launch_nr<40>(maps, p, grid, stream);
+  return launch_nr<72>(maps, p, grid, stream);
+}
+
+}  // namespace vsa

@@ -110,6 +110,28 @@ cudaError_t launch_coarse_topk(const Geometry& g, const float* pooled_q, const f
                                const float* pooled_v, float* coarse, int32_t* tile_index, void* vfrag,
                                const DeviceLengths& dl, cudaStream_t stream);
 
+// Coarse attention + top-k with both products on the tcgen05 tensor cores,
+// for up to kCoarseTcMaxT video tiles (longer videos take the kernel above).
+// launch_split writes the pooled q, k, v as bf16 hi/lo rows (`operands`:
+// [q, k, v][hi, lo][B H][coarse_tc_padded(g)][128], coarse_tc_operand_bytes);
+// launch_coarse_tc reads them through `maps` (q hi, q lo, k hi, k lo, v hi,
+// v lo: {128 channels, padded rows, B H, 1}, boxes of 64 x 64, 128-byte
+// swizzled; then the scratch rows as bf16 {padded keys, 2 planes, 64 rows,
+// slots}, boxes of 64 keys x 1 x 64 rows) and keeps its score rows in
+// `scratch` (coarse_tc_scratch_bytes: one 64-row buffer per CTA).
+constexpr int kCoarseTcMaxT = 2304;  // a query row of scores fits 72 registers per lane
+constexpr int kCoarseTcMaxSlots = 160;  // CTAs of the persistent grid, at most
+int coarse_tc_padded(const Geometry& g);
+bool coarse_tc_supported(const Geometry& g);
+int coarse_tc_units(const Geometry& g);
+size_t coarse_tc_operand_bytes(const Geometry& g);
+size_t coarse_tc_scratch_bytes(const Geometry& g);
+cudaError_t launch_split(const Geometry& g, const float* pooled_q, const float* pooled_k, const float* pooled_v,
+                         void* operands, const DeviceLengths& dl, cudaStream_t stream);
+cudaError_t launch_coarse_tc(const Geometry& g, const CUtensorMap (&maps)[7], float* scratch, float* coarse,
+                             int32_t* tile_index, unsigned int* err, const DeviceLengths& dl, int num_sms,
+                             cudaStream_t stream);
+
 // SubBlock routing: 16-token sub-block means of q and k (fp32 [B, H, 4T, 128],
 // empty sub-blocks of a ragged last tile as 0, plus the same values split into
 // bf16 hi + lo rows: frag_* holds hi [B, H, spad, 128] then lo [B, H, spad,

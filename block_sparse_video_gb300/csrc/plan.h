@@ -24,6 +24,7 @@ struct vsa_plan {
   vsa_shape_t shape;
   int device;
   int subblock;         // 0: VSA (coarse branch + top-k); 1: SubBlock routing, no coarse term
+  int coarse_tc;        // VSA: 1 when the coarse branch runs on the tcgen05 kernel
   double sparsity;      // SubBlock plans: fraction of video key tiles that may be dropped
   vsa::Geometry g;
   size_t off_err, off_pq, off_pk, off_pv, off_coarse, off_idx, off_redo, off_fq, off_fk, off_vf, ws_bytes;

@@ -57,6 +57,23 @@ bool encode_bnhd(CUtensorMap* map, const void* ptr, const vsa::Geometry& g) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map over the tcgen05 coarse kernel's score rows read back as bf16
+// probabilities: per CTA slot, 64 rows of `tp` floats, each row's bytes
+// holding tp bf16 hi values then tp bf16 lo values ({tp keys, 2 planes, 64
+// rows, slots}); one box = 64 keys x 1 plane x 64 rows, 128-byte swizzled.
+bool encode_prob_rows(CUtensorMap* map, const void* ptr, int tp, int slots) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(tp), 2, 64, static_cast<cuuint64_t>(slots)};
+  const cuuint64_t plane = static_cast<cuuint64_t>(tp) * 2;
+  const cuuint64_t strides[3] = {plane, 2 * plane, 128 * plane};
+  const cuuint32_t box[4] = {64, 1, 64, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Tensor map over `rows` bf16 rows of 128 channels per (batch, head), for B H
 // of them ({128, rows, B H, 1}); one box = 64 channels x 64 rows, 128-byte
 // swizzled. Rows past `rows` read as zeros.
@@ -173,7 +190,9 @@ vsa_status_t create_plan(const vsa_shape_t* shape, int device, bool subblock, do
   if (static_cast<int64_t>(g.B) * g.H > 65535) return VSA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(g.B) * g.H * (g.TP + g.T) >= (int64_t(1) << 31)) return VSA_ERR_UNSUPPORTED;
   int rows = 0;
-  if (subblock ? vsa::subblock_router_smem_bytes(g, &rows) == 0 : vsa::coarse_smem_bytes(g, &rows) == 0)
+  const bool coarse_tc = !subblock && vsa::coarse_tc_supported(g);
+  if (subblock ? vsa::subblock_router_smem_bytes(g, &rows) == 0
+               : !coarse_tc && vsa::coarse_smem_bytes(g, &rows) == 0)
     return VSA_ERR_UNSUPPORTED;  // T too large for the selection kernel's shared memory
 
   vsa_plan* p = new (std::nothrow) vsa_plan;
@@ -182,6 +201,7 @@ vsa_status_t create_plan(const vsa_shape_t* shape, int device, bool subblock, do
   p->shape = s;
   p->device = device;
   p->subblock = subblock ? 1 : 0;
+  p->coarse_tc = coarse_tc ? 1 : 0;
   p->sparsity = subblock ? sparsity : 0.0;
   p->g = g;
   // VSA: pooled q, k, v and the coarse output, fp32 [B, H, T, 128] each.
@@ -200,8 +220,12 @@ vsa_status_t create_plan(const vsa_shape_t* shape, int device, bool subblock, do
   const size_t frag = subblock ? static_cast<size_t>(g.B) * g.H * vsa::subblock_rows_padded(g) * 512 : 0;
   p->off_fq = off;   off += align_up(frag);
   p->off_fk = off;   off += align_up(frag);
-  // VSA: the pooled V again, as bf16 hi/lo mma fragments for the coarse product
-  p->off_vf = off;   off += subblock ? 0 : align_up(vsa::coarse_vfrag_bytes(g));
+  // VSA: the pooled Q, K, V again as bf16 hi/lo rows plus the score rows of the
+  // tcgen05 coarse kernel, or the pooled K and V as mma fragments for the other one
+  p->off_vf = off;
+  off += subblock ? 0
+                  : align_up(coarse_tc ? vsa::coarse_tc_operand_bytes(g) + vsa::coarse_tc_scratch_bytes(g)
+                                       : vsa::coarse_vfrag_bytes(g));
   p->ws_bytes = off;
   p->tensor_bytes = static_cast<size_t>(g.B) * g.N * g.H * vsa::kHeadDim * 2;
   *out = p;
@@ -438,8 +462,23 @@ vsa_status_t forward_impl(vsa_plan_t plan, const void* q, const void* k, const v
         vsa::launch_pool(g, qb, kb, static_cast<const __nv_bfloat16*>(v), pq, pk, pv, dl, st) != cudaSuccess)
       return VSA_ERR_CUDA;
     if ((rs = record(plan, 1, st)) != VSA_OK) return rs;
-    if (vsa::launch_coarse_topk(g, pq, pk, pv, coarse, idx, ws + plan->off_vf, dl, st) != cudaSuccess)
+    if (plan->coarse_tc) {
+      uint8_t* ops = ws + plan->off_vf;
+      const int tp = vsa::coarse_tc_padded(g);
+      const size_t plane = static_cast<size_t>(g.B) * g.H * tp * vsa::kHeadDim * 2;
+      const int slots = vsa::coarse_tc_units(g) < vsa::kCoarseTcMaxSlots ? vsa::coarse_tc_units(g)
+                                                                         : vsa::kCoarseTcMaxSlots;
+      float* scratch = reinterpret_cast<float*>(ops + vsa::coarse_tc_operand_bytes(g));
+      CUtensorMap maps[7];
+      for (int i = 0; i < 6; ++i)
+        if (!encode_rows(&maps[i], ops + i * plane, tp, g.B * g.H)) return VSA_ERR_CUDA;
+      if (!encode_prob_rows(&maps[6], scratch, tp, slots)) return VSA_ERR_CUDA;
+      if (vsa::launch_split(g, pq, pk, pv, ops, dl, st) != cudaSuccess ||
+          vsa::launch_coarse_tc(g, maps, scratch, coarse, idx, err, dl, plan->num_sms, st) != cudaSuccess)
+        return VSA_ERR_CUDA;
+    } else if (vsa::launch_coarse_topk(g, pq, pk, pv, coarse, idx, ws + plan->off_vf, dl, st) != cudaSuccess) {
       return VSA_ERR_CUDA;
+    }
   }
   if ((rs = record(plan, 2, st)) != VSA_OK) return rs;
   vsa::FineArgs a;

@@ -398,9 +398,9 @@ vsa_status_t vsa_plan_set_stage_events(vsa_plan_t plan, void* const* events);
 vsa_status_t vsa_diag_wait_timeout(vsa_plan_t plan, void* workspace, int n_ctas, void* stream);
 
 /* Size of the library-owned workspace used by vsa_forward_static_workspace:
- * 32 MiB, enough for one GPU's head share of a 5 s request (14 heads, 36,288
- * video tokens) or anything whose workspace_bytes (vsa_plan_info) fits. */
-#define VSA_STATIC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+ * 64 MiB, enough for one GPU's head share of a 5 s request (14 heads, 36,288
+ * video tokens: 54 MB) or anything whose workspace_bytes (vsa_plan_info) fits. */
+#define VSA_STATIC_WORKSPACE_BYTES (64u * 1024u * 1024u)
 
 /* The forward for callers that cannot allocate device memory (a serving engine
  * that budgets all device memory at start-up, a plugin interface without an
@@ -414,8 +414,10 @@ vsa_status_t vsa_diag_wait_timeout(vsa_plan_t plan, void* workspace, int n_ctas,
  * Returns VSA_ERR_UNSUPPORTED, without launching, if the plan's workspace_bytes
  * exceed VSA_STATIC_WORKSPACE_BYTES.
  * The first call for a plan on a given device resolves the array's device
- * address (cudaGetSymbolAddress, once per device); make that first call before
- * any stream capture.
+ * address (cudaGetSymbolAddress, once per device), which may also load the
+ * library's device code and back the array on that device; make that first
+ * call before any stream capture. The address is kept for the life of the
+ * process: do not use this entry point on a device after cudaDeviceReset.
  * All calls share the one array, which keeps the previous call's contents (the
  * forward clears what must start at zero and overwrites the rest): calls whose
  * work overlaps on the GPU (different streams, or host threads, without

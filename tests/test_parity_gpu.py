@@ -97,16 +97,18 @@ def test_ragged_sweep_sampled_parity(cuda_ok):
 
 
 def test_long_video_smaller_coarse_tiles(cuda_ok):
-    """T = 1,500 video tiles: the coarse kernel switches to 16 query tiles per CTA."""
+    """T = 1,500 video tiles: the tcgen05 coarse kernel holds each score row in
+    72 registers a lane (its widest row form)."""
     q, k, v, g = make_inputs(1, 2, 40, 24, 96000, 21, device="cuda")
     stats = _sampled(q, k, v, g, 40, 24, 96000, 0.2, [(0, 0), (0, 1)], 24, {(0, 1)}, 21)
     assert_errors(stats, "long video")
 
 
 def test_very_long_video_sixteen_coarse_tiles(cuda_ok):
-    """T = 2,600 video tiles (the last one ragged): the coarse kernel keeps 16
-    query tiles per CTA (its score rows would not fit 32). Every pooled
-    statistic, selection and coarse row of both heads is checked."""
+    """T = 2,600 video tiles (the last one ragged), past the tcgen05 coarse
+    kernel's 2,304: the mma.sync coarse kernel keeps 16 query tiles per CTA
+    (its score rows would not fit 32). Every pooled statistic, selection and
+    coarse row of both heads is checked."""
     lv = 64 * 2600 - 30
     q, k, v, g = make_inputs(1, 2, 40, 24, lv, 23, device="cuda")
     stats = _sampled(q, k, v, g, 40, 24, lv, 0.2, [(0, 0), (0, 1)], 16, {(0, 0)}, 23)
@@ -114,8 +116,8 @@ def test_very_long_video_sixteen_coarse_tiles(cuda_ok):
 
 
 def test_longest_video_eight_coarse_tiles(cuda_ok):
-    """T = 4,000 video tiles: the coarse kernel keeps 8 query tiles per CTA and
-    runs its tensor-core tiles with half the rows empty."""
+    """T = 4,000 video tiles: the mma.sync coarse kernel keeps 8 query tiles per
+    CTA and runs its tensor-core tiles with half the rows empty."""
     lv = 64 * 4000 - 17
     q, k, v, g = make_inputs(1, 1, 64, 0, lv, 24, device="cuda")
     stats = _sampled(q, k, v, g, 64, 0, lv, 0.2, [(0, 0)], 12, {(0, 0)}, 24)

@@ -25,6 +25,7 @@ MEAN_ABS = 2e-3
 
 @pytest.mark.parametrize("shape", [
     (1, 14, 1024, 512, 8192, 0.2, 1),   # medium workload
+    (1, 14, 1024, 1024, 36288, 0.2, 2), # one GPU's head share of a 5 s request
     (2, 3, 37, 50, 1000, 0.3, 5),       # ragged prefix and last tile, batch 2
 ])
 def test_static_workspace_forward_matches_regular_forward(cuda_ok, shape):
@@ -45,7 +46,7 @@ def test_static_workspace_forward_matches_regular_forward(cuda_ok, shape):
 
 
 def test_static_workspace_rejects_plans_that_do_not_fit(cuda_ok):
-    plan = bsv.vsa_plan_create(1, 56, 1024, 1024, 72576, 0.2)  # the 10 s shape needs ~190 MB
+    plan = bsv.vsa_plan_create(1, 56, 1024, 1024, 72576, 0.2)  # the 10 s shape needs ~334 MB
     try:
         assert bsv.vsa_plan_info(plan)[2] > bsv.STATIC_WORKSPACE_BYTES
         x = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
