@@ -82,34 +82,50 @@ struct CoarseParams {
   unsigned int* err;
 };
 
-// The k largest of a row held in registers, lane l holding entries l + 32 i
-// (-inf past T), written ascending to dst[0 .. k): the same set, with ties
-// to the lower index, as warp_select_topk_count (a counting search for a
-// threshold with exactly k entries at or above it; the radix select where
-// entries tie at the cut or a score is not finite). h: kBins ints of shared
-// memory for the radix select.
-template <int NR>
-__device__ __forceinline__ void select_topk_regs(const float (&v)[NR], int T, int k, int* h, int32_t* dst,
+// A query row held in registers: lane l holds keys 128 m + 4 l .. + 3 in
+// v[m].x .. .w, m < NM (-inf past T), so each m is one coalesced float4 load.
+
+// Exclusive prefix sum of a small per-lane count over the warp, and the total.
+__device__ __forceinline__ int warp_exclusive_scan(int x, int lane, int& total) {
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  total = __shfl_sync(0xffffffffu, incl, 31);
+  return incl - x;
+}
+
+// The k largest entries of the row, written ascending to dst[0 .. k): the
+// same set, with ties to the lower index, as warp_select_topk_count (a
+// counting search for a threshold with exactly k entries at or above it; the
+// radix select where entries tie at the cut or a score is not finite). h: kBins
+// ints of shared memory for the radix select.
+template <int NM>
+__device__ __forceinline__ void select_topk_regs(const float4 (&v)[NM], int T, int k, int* h, int32_t* dst,
                                                  int lane) {
   const unsigned full = 0xffffffffu;
-  const unsigned lt_mask = (1u << lane) - 1u;
   if (k >= T) {
     for (int j = lane; j < T; j += 32) dst[j] = j;
     return;
   }
+  auto at = [&](int m, int e) { return e == 0 ? v[m].x : e == 1 ? v[m].y : e == 2 ? v[m].z : v[m].w; };
   float vmin = INFINITY, vmax = -INFINITY, s1 = 0.f, s2 = 0.f;
   bool bad = false;
 #pragma unroll
-  for (int i = 0; i < NR; ++i) {
-    if (32 * i + lane < T) {
-      const float x = v[i];
-      vmin = fminf(vmin, x);
-      vmax = fmaxf(vmax, x);
-      s1 += x;
-      s2 = fmaf(x, x, s2);
-      bad |= !(fabsf(x) <= 3.0e38f);
+  for (int m = 0; m < NM; ++m)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x = at(m, e);
+      if (128 * m + 4 * lane + e < T) {
+        vmin = fminf(vmin, x);
+        vmax = fmaxf(vmax, x);
+        s1 += x;
+        s2 = fmaf(x, x, s2);
+        bad |= !(fabsf(x) <= 3.0e38f);
+      }
     }
-  }
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
     vmin = fminf(vmin, __shfl_xor_sync(full, vmin, o));
@@ -117,10 +133,10 @@ __device__ __forceinline__ void select_topk_regs(const float (&v)[NR], int T, in
     s1 += __shfl_xor_sync(full, s1, o);
     s2 += __shfl_xor_sync(full, s2, o);
   }
-  auto count_ge = [&](float x) {
+  auto count_ge = [&](float x) {  // -inf past T never counts (x > vmin >= -inf)
     int c = 0;
 #pragma unroll
-    for (int i = 0; i < NR; ++i) c += v[i] >= x;  // -inf past T never counts (x > vmin >= -inf)
+    for (int m = 0; m < NM; ++m) c += (v[m].x >= x) + (v[m].y >= x) + (v[m].z >= x) + (v[m].w >= x);
     return static_cast<int>(__reduce_add_sync(full, static_cast<unsigned>(c)));
   };
   float theta = 0.f;
@@ -159,11 +175,20 @@ __device__ __forceinline__ void select_topk_regs(const float (&v)[NR], int T, in
   if (found) {
     int written = 0;
 #pragma unroll
-    for (int i = 0; i < NR; ++i) {
-      const bool sel = 32 * i + lane < T && v[i] >= theta;
-      const unsigned selb = __ballot_sync(full, sel);
-      if (sel) dst[written + __popc(selb & lt_mask)] = 32 * i + lane;
-      written += __popc(selb);
+    for (int m = 0; m < NM; ++m) {
+      bool sel[4];
+      int cnt = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        sel[e] = at(m, e) >= theta;  // -inf past T never reaches theta
+        cnt += sel[e];
+      }
+      int total;
+      int pos = written + warp_exclusive_scan(cnt, lane, total);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (sel[e]) dst[pos++] = 128 * m + 4 * lane + e;
+      written += total;
     }
     return;
   }
@@ -176,12 +201,13 @@ __device__ __forceinline__ void select_topk_regs(const float (&v)[NR], int T, in
     for (int b = lane; b < kBins; b += 32) h[b] = 0;
     __syncwarp();
 #pragma unroll
-    for (int i = 0; i < NR; ++i) {
-      if (32 * i + lane < T) {
-        const uint32_t key = order_key(v[i]);
-        if ((key & pmask) == prefix) atomicAdd(&h[(key >> shift) & 0xFFu], 1);
-      }
-    }
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (128 * m + 4 * lane + e < T) {
+          const uint32_t key = order_key(at(m, e));
+          if ((key & pmask) == prefix) atomicAdd(&h[(key >> shift) & 0xFFu], 1);
+        }
     __syncwarp();
     int c[8], lsum = 0;
 #pragma unroll
@@ -211,19 +237,37 @@ __device__ __forceinline__ void select_topk_regs(const float (&v)[NR], int T, in
     rem -= above;
     __syncwarp();
   }
+  // every key above the k-th largest, and the lowest `rem` keys equal to it
   int written = 0, eq_seen = 0;
 #pragma unroll
-  for (int i = 0; i < NR; ++i) {
-    const int j = 32 * i + lane;
-    const uint32_t key = j < T ? order_key(v[i]) : 0u;
-    const bool is_gt = j < T && key > prefix;
-    const bool is_eq = j < T && key == prefix;
-    const unsigned eqb = __ballot_sync(full, is_eq);
-    const bool sel = is_gt || (is_eq && eq_seen + __popc(eqb & lt_mask) < rem);
-    const unsigned selb = __ballot_sync(full, sel);
-    if (sel) dst[written + __popc(selb & lt_mask)] = j;
-    written += __popc(selb);
-    eq_seen += __popc(eqb);
+  for (int m = 0; m < NM; ++m) {
+    bool gt[4], eq[4];
+    int n_eq = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const bool in = 128 * m + 4 * lane + e < T;
+      const uint32_t key = in ? order_key(at(m, e)) : 0u;
+      gt[e] = in && key > prefix;
+      eq[e] = in && key == prefix;
+      n_eq += eq[e];
+    }
+    int eq_total;
+    int eq_before = eq_seen + warp_exclusive_scan(n_eq, lane, eq_total);
+    bool sel[4];
+    int cnt = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      sel[e] = gt[e] || (eq[e] && eq_before < rem);
+      eq_before += eq[e];
+      cnt += sel[e];
+    }
+    int total;
+    int pos = written + warp_exclusive_scan(cnt, lane, total);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (sel[e]) dst[pos++] = 128 * m + 4 * lane + e;
+    written += total;
+    eq_seen += eq_total;
   }
 }
 
@@ -231,7 +275,7 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-template <int NR>
+template <int NM>
 __global__ void __launch_bounds__(kThreads, 1)
 coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
                  const __grid_constant__ CUtensorMap map_kh, const __grid_constant__ CUtensorMap map_kl,
@@ -399,32 +443,43 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
     // ------------------------------------------------------------ phase B: selection, softmax, P
     for (int r = warp; r < n_rows; r += kWarps) {
       float* row = rows + static_cast<size_t>(r) * p.tp_cap;
-      float v[NR];
+      float4 v[NM];
 #pragma unroll
-      for (int i = 0; i < NR; ++i) {
-        const int j = 32 * i + lane;
-        v[i] = j < T ? row[j] : -INFINITY;
+      for (int m = 0; m < NM; ++m) {
+        const int j = 128 * m + 4 * lane;  // T_pad is a multiple of 128, so j + 3 < T_pad
+        v[m] = j < T ? reinterpret_cast<const float4*>(row)[32 * m + lane] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (j + 3 >= T) {  // the row's ragged end: entries past T are -inf
+          if (j + 1 >= T) v[m].y = -INFINITY;
+          if (j + 2 >= T) v[m].z = -INFINITY;
+          if (j + 3 >= T) v[m].w = -INFINITY;
+        }
       }
-      select_topk_regs<NR>(v, T, k, hist + warp * kBins,
+      select_topk_regs<NM>(v, T, k, hist + warp * kBins,
                            p.tile_index + (static_cast<size_t>(bh) * T_cap + q0 + r) * k_cap, lane);
-      float m = -INFINITY;
+      float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < NR; ++i) m = fmaxf(m, v[i]);
+      for (int m = 0; m < NM; ++m) mx = fmaxf(mx, fmaxf(fmaxf(v[m].x, v[m].y), fmaxf(v[m].z, v[m].w)));
 #pragma unroll
-      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      // p = exp(s - max) = 2^((s - max) log2 e); entries past T give 2^-inf = 0
+      const float nmx = -mx * 1.4426950408889634f;
       float l = 0.f;
-      __nv_bfloat16* ph = reinterpret_cast<__nv_bfloat16*>(row);   // the row's first half: p hi
-      __nv_bfloat16* pl = ph + p.tp_cap;                          // second half: p lo
       __syncwarp();  // every lane has read the row before it is overwritten
+      uint2* ph = reinterpret_cast<uint2*>(row);                 // the row's first half: p hi, 4 keys per uint2
+      uint2* pl = reinterpret_cast<uint2*>(row + p.tp_cap / 2);  // second half: p lo
 #pragma unroll
-      for (int i = 0; i < NR; ++i) {
-        const int j = 32 * i + lane;
-        if (j < kChunk * n_chunks) {
-          const float e = j < T ? expf(v[i] - m) : 0.f;
-          l += e;
-          const __nv_bfloat16 h = __float2bfloat16_rn(e);
-          ph[j] = h;
-          pl[j] = __float2bfloat16_rn(e - __bfloat162float(h));
+      for (int m = 0; m < NM; ++m) {
+        if (128 * m < kChunk * n_chunks) {
+          const float e0 = ex2_approx(fmaf(v[m].x, 1.4426950408889634f, nmx));
+          const float e1 = ex2_approx(fmaf(v[m].y, 1.4426950408889634f, nmx));
+          const float e2 = ex2_approx(fmaf(v[m].z, 1.4426950408889634f, nmx));
+          const float e3 = ex2_approx(fmaf(v[m].w, 1.4426950408889634f, nmx));
+          l += (e0 + e1) + (e2 + e3);
+          uint32_t h01, l01, h23, l23;
+          split_bf16_pair(e0, e1, h01, l01);
+          split_bf16_pair(e2, e3, h23, l23);
+          ph[32 * m + lane] = make_uint2(h01, h23);
+          pl[32 * m + lane] = make_uint2(l01, l23);
         }
       }
 #pragma unroll
@@ -569,12 +624,12 @@ split_kernel(const float* __restrict__ pq, const float* __restrict__ pk, const f
   out[(2 * tensor + 1) * per_tensor + idx] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
 }
 
-template <int NR>
-cudaError_t launch_nr(const CUtensorMap (&maps)[7], const CoarseParams& p, int grid, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(coarse_tc_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <int NM>
+cudaError_t launch_nm(const CUtensorMap (&maps)[7], const CoarseParams& p, int grid, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(coarse_tc_kernel<NM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  coarse_tc_kernel<NR><<<grid, kThreads, kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
+  coarse_tc_kernel<NM><<<grid, kThreads, kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
                                                               maps[5], maps[6], p);
   return cudaGetLastError();
 }
@@ -619,12 +674,12 @@ cudaError_t launch_coarse_tc(const Geometry& g, const CUtensorMap (&maps)[7], fl
   p.err = err;
   int grid = p.n_units < num_sms ? p.n_units : num_sms;
   if (grid > kCoarseTcMaxSlots) grid = kCoarseTcMaxSlots;
-  // a query row's scores in NR registers per lane (the same results for any
-  // NR that holds the row: entries past T take no part)
-  static_assert(kCoarseTcMaxT <= 32 * 72, "rows held in at most 72 registers per lane");
-  if (g.T <= 32 * 20) return launch_nr<20>(maps, p, grid, stream);
-  if (g.T <= 32 * 40) return launch_nr<40>(maps, p, grid, stream);
-  return launch_nr<72>(maps, p, grid, stream);
+  // a query row's scores in NM float4 registers per lane (the same results
+  // for any NM that holds the row: entries past T take no part)
+  static_assert(kCoarseTcMaxT <= 128 * 18, "rows held in at most 18 float4 registers per lane");
+  if (g.T <= 128 * 5) return launch_nm<5>(maps, p, grid, stream);
+  if (g.T <= 128 * 10) return launch_nm<10>(maps, p, grid, stream);
+  return launch_nm<18>(maps, p, grid, stream);
 }
 
 }  // namespace vsa
