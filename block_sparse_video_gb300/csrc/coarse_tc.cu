@@ -35,7 +35,8 @@
 // 8 KB box each) through a ring of 32 KB stages; warps 1 and 2 issue the
 // MMAs, converged with one elected lane each, splitting every chunk's 24
 // products between two accumulators (a single issuer leaves the pipe idle
-// between N = 64 MMAs); warps 4-7 move scores and outputs out of TMEM; all 12
+// between N = 64 MMAs); warps 4-11 move scores and outputs out of TMEM (two
+// per lane quarter, 32 columns each); all 12
 // warps run phase B. Every wait is bounded.
 #include <cmath>
 
@@ -54,6 +55,7 @@ constexpr int kStages = 5;                    // ring stages of 32 KB
 constexpr uint32_t kStageBytes = kChunk * kHeadDim * 2;
 constexpr uint32_t kQBytes = 2 * kRows * kHeadDim * 2;  // Qbar hi and lo, 64 rows each
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpEpi0 = 4;
+constexpr int kEpiWarps = 8;                  // warps 4-11: lane quarter warp % 4, column half (warp - 4) / 4
 constexpr uint32_t kTmemCols = 256;           // two accumulator pairs of 64 columns
 constexpr unsigned int kDetailQ = 0xE00, kDetailFull = 0xE10, kDetailEmpty = 0xE20, kDetailAcc = 0xE30,
                        kDetailAccEmpty = 0xE40, kDetailC = 0xE50;
@@ -150,7 +152,7 @@ __device__ __forceinline__ void select_topk_regs(const float4 (&v)[NM], int T, i
     float x = mean + normcdfinvf(1.f - static_cast<float>(k) / static_cast<float>(T)) * sd;
 #pragma unroll 1
     for (int it = 0; it < 48; ++it) {
-      if (it > 0) x = lo + (hi - lo) * (flo / (flo - fhi));
+      if (it > 0) x = lo + (hi - lo) * __fdividef(flo, flo - fhi);  // a trial point: any x in (lo, hi) is valid
       if (!(x > lo && x < hi)) x = 0.5f * (lo + hi);
       if (!(x > lo && x < hi)) break;
       const int c = count_ge(x);
@@ -173,22 +175,22 @@ __device__ __forceinline__ void select_topk_regs(const float4 (&v)[NM], int T, i
     }
   }
   if (found) {
+    // in key order: lane-major, then the lane's four keys; one ballot per key
+    // slot gives every lane the count of selected keys in the lanes before it
+    const unsigned lt_mask = (1u << lane) - 1u;
     int written = 0;
 #pragma unroll
     for (int m = 0; m < NM; ++m) {
-      bool sel[4];
-      int cnt = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        sel[e] = at(m, e) >= theta;  // -inf past T never reaches theta
-        cnt += sel[e];
-      }
-      int total;
-      int pos = written + warp_exclusive_scan(cnt, lane, total);
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (sel[e]) dst[pos++] = 128 * m + 4 * lane + e;
-      written += total;
+      const bool s0 = v[m].x >= theta, s1b = v[m].y >= theta, s2b = v[m].z >= theta, s3 = v[m].w >= theta;
+      const unsigned b0 = __ballot_sync(full, s0), b1 = __ballot_sync(full, s1b), b2 = __ballot_sync(full, s2b),
+                     b3 = __ballot_sync(full, s3);  // -inf past T never reaches theta
+      int pos = written + __popc(b0 & lt_mask) + __popc(b1 & lt_mask) + __popc(b2 & lt_mask) + __popc(b3 & lt_mask);
+      const int key = 128 * m + 4 * lane;
+      if (s0) dst[pos++] = key;
+      if (s1b) dst[pos++] = key + 1;
+      if (s2b) dst[pos++] = key + 2;
+      if (s3) dst[pos] = key + 3;
+      written += __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
     }
     return;
   }
@@ -309,7 +311,7 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar(kBarAccFull + a), 2);  // one commit per issuer
-      mbar_init(bar(kBarAccEmpty + a), 4);  // the four epilogue warps
+      mbar_init(bar(kBarAccEmpty + a), kEpiWarps);
     }
     mbar_init(bar(kBarC), 2);
     fence_barrier_init();
@@ -401,9 +403,9 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
         }
         if (!failed) umma_commit_elect(bar(kBarAccFull + a));
       }
-    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
-      // one lane quarter per warp: TMEM lane = key 128 c + 32 q + lane
-      const int q = warp % 4;
+    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
+      // lane quarter q (TMEM lane = key 128 c + 32 q + lane), columns 32 ch .. + 31
+      const int q = warp % 4, ch = (warp - kWarpEpi0) / 4;
       const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
       for (int c = 0; c < n_chunks && !failed; ++c) {
         const uint32_t au = acc0 + c;
@@ -415,15 +417,16 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
         tc_fence_after();
         const int key = kChunk * c + 32 * q + lane;
 #pragma unroll
-        for (int part = 0; part < kRows / 16; ++part) {
+        for (int part = 0; part < kRows / 32; ++part) {
+          const int col = 32 * ch + 16 * part;
           uint32_t x0[16], x1[16];
-          tmem_ld16(tbase + lane_off + static_cast<uint32_t>(2 * a * kRows + 16 * part), x0);
-          tmem_ld16(tbase + lane_off + static_cast<uint32_t>((2 * a + 1) * kRows + 16 * part), x1);
+          tmem_ld16(tbase + lane_off + static_cast<uint32_t>(2 * a * kRows + col), x0);
+          tmem_ld16(tbase + lane_off + static_cast<uint32_t>((2 * a + 1) * kRows + col), x1);
           tmem_wait_ld();
           if (key < T) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const int r = 16 * part + j;
+              const int r = col + j;
               if (r < n_rows)
                 rows[static_cast<size_t>(r) * p.tp_cap + key] =
                     (__uint_as_float(x0[j]) + __uint_as_float(x1[j])) * scale;
@@ -556,8 +559,9 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
         umma_commit_elect(bar(kBarEmpty + sp));
       }
       if (!failed) umma_commit_elect(bar(kBarC));
-    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
-      const int q = warp % 4;
+    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
+      // lane quarter q (TMEM lane = head dim 32 q + lane), columns 32 ch .. + 31
+      const int q = warp % 4, ch = (warp - kWarpEpi0) / 4;
       const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
       const int dim = 32 * q + lane;
       if (!mbar_wait_warp(bar(kBarC), units_done & 1, err, kDetailC)) {
@@ -565,14 +569,15 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
       } else {
         tc_fence_after();
 #pragma unroll
-        for (int part = 0; part < kRows / 16; ++part) {
+        for (int part = 0; part < kRows / 32; ++part) {
+          const int col = 32 * ch + 16 * part;
           uint32_t x0[16], x1[16];
-          tmem_ld16(tbase + lane_off + static_cast<uint32_t>(16 * part), x0);
-          tmem_ld16(tbase + lane_off + static_cast<uint32_t>(kRows + 16 * part), x1);
+          tmem_ld16(tbase + lane_off + static_cast<uint32_t>(col), x0);
+          tmem_ld16(tbase + lane_off + static_cast<uint32_t>(kRows + col), x1);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int r = 16 * part + j;
+            const int r = col + j;
             if (r < n_rows)
               p.coarse[(static_cast<size_t>(bh) * T_cap + q0 + r) * kHeadDim + dim] =
                   (__uint_as_float(x0[j]) + __uint_as_float(x1[j])) / l_row[r];
