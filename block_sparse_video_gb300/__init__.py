@@ -126,6 +126,8 @@ def load_library(path: str = LIB_PATH):
         "vsa_check": (i32, [vp, vp, vp]),
         "vsa_plan_set_stage_events": (i32, [vp, ctypes.POINTER(vp)]),
         "vsa_forward_static_workspace": (i32, [vp, vp, vp, vp, vp, vp, vp]),
+        "vsa_check_static_workspace": (i32, [vp, vp]),
+        "vsa_diag_wait_timeout_static": (i32, [vp, ctypes.c_int, vp]),
         "vsa_diag_wait_timeout": (i32, [vp, vp, ctypes.c_int, vp]),
         "vsa_plan_destroy": (None, [vp]),
         "vsa_status_string": (ctypes.c_char_p, [i32]),
@@ -311,6 +313,17 @@ def vsa_forward_static_workspace(plan, q, k, v, gate, out, stream=None):
         raise VsaError(status, "vsa_forward_static_workspace: the plan's workspace exceeds "
                                f"{STATIC_WORKSPACE_BYTES} bytes")
     _check(status, "vsa_forward_static_workspace")
+
+
+def vsa_check_static_workspace(plan, stream=None):
+    """vsa_check for the library-owned array of vsa_forward_static_workspace."""
+    _check(load_library().vsa_check_static_workspace(plan, _stream_handle(stream)), "vsa_check_static_workspace")
+
+
+def vsa_diag_wait_timeout_static(plan, n_ctas=1, stream=None):
+    """The diagnostic bounded-wait kernel on the library-owned array (see vsa.h)."""
+    _check(load_library().vsa_diag_wait_timeout_static(plan, int(n_ctas), _stream_handle(stream)),
+           "vsa_diag_wait_timeout_static")
 
 
 def vsa_diag_wait_timeout(plan, workspace, n_ctas=1, stream=None):

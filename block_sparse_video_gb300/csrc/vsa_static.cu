@@ -44,6 +44,21 @@ void* static_workspace(int device) {
   return g_workspace_ptr[device];
 }
 
+// Runs fn(ws) with the plan's device current and ws the device address of the
+// array on it; restores the caller's device afterwards.
+template <typename Fn>
+vsa_status_t with_static_workspace(vsa_plan_t plan, Fn&& fn) {
+  const int device = plan->device;
+  if (device < 0 || device >= kMaxDevices) return VSA_ERR_UNSUPPORTED;
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess) return VSA_ERR_CUDA;
+  if (prev != device && cudaSetDevice(device) != cudaSuccess) return VSA_ERR_CUDA;
+  void* ws = static_workspace(device);
+  const vsa_status_t s = ws != nullptr ? fn(ws) : VSA_ERR_CUDA;
+  if (prev != device) cudaSetDevice(prev);
+  return s;
+}
+
 }  // namespace
 
 extern "C" vsa_status_t vsa_forward_static_workspace(vsa_plan_t plan, const void* q, const void* k,
@@ -51,15 +66,17 @@ extern "C" vsa_status_t vsa_forward_static_workspace(vsa_plan_t plan, const void
                                                      void* stream) {
   if (!plan) return VSA_ERR_INVALID_ARG;
   if (plan->ws_bytes > VSA_STATIC_WORKSPACE_BYTES) return VSA_ERR_UNSUPPORTED;
-  const int device = plan->device;
-  if (device < 0 || device >= kMaxDevices) return VSA_ERR_UNSUPPORTED;
-  int prev = -1;
-  if (cudaGetDevice(&prev) != cudaSuccess) return VSA_ERR_CUDA;
-  if (prev != device && cudaSetDevice(device) != cudaSuccess) return VSA_ERR_CUDA;
-  void* ws = static_workspace(device);
-  vsa_status_t s = VSA_ERR_CUDA;
-  if (ws != nullptr)
-    s = vsa_forward(plan, q, k, v, gate, out, ws, VSA_STATIC_WORKSPACE_BYTES, stream);
-  if (prev != device) cudaSetDevice(prev);
-  return s;
+  return with_static_workspace(plan, [&](void* ws) {
+    return vsa_forward(plan, q, k, v, gate, out, ws, VSA_STATIC_WORKSPACE_BYTES, stream);
+  });
+}
+
+extern "C" vsa_status_t vsa_check_static_workspace(vsa_plan_t plan, void* stream) {
+  if (!plan) return VSA_ERR_INVALID_ARG;
+  return with_static_workspace(plan, [&](void* ws) { return vsa_check(plan, ws, stream); });
+}
+
+extern "C" vsa_status_t vsa_diag_wait_timeout_static(vsa_plan_t plan, int n_ctas, void* stream) {
+  if (!plan) return VSA_ERR_INVALID_ARG;
+  return with_static_workspace(plan, [&](void* ws) { return vsa_diag_wait_timeout(plan, ws, n_ctas, stream); });
 }

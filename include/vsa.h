@@ -422,10 +422,20 @@ vsa_status_t vsa_diag_wait_timeout(vsa_plan_t plan, void* workspace, int n_ctas,
  * forward clears what must start at zero and overwrites the rest): calls whose
  * work overlaps on the GPU (different streams, or host threads, without
  * ordering between them) race on it. Device-side wait timeouts land in the
- * array's error words and are not reported by this entry point. */
+ * array's error words: vsa_check_static_workspace reports them. */
 vsa_status_t vsa_forward_static_workspace(vsa_plan_t plan, const void* q, const void* k,
                                           const void* v, const void* gate, void* out,
                                           void* stream);
+
+/* vsa_check for the library-owned array of vsa_forward_static_workspace:
+ * synchronises `stream` and reports the error words the last forward on this
+ * plan's device left in that array (VSA_OK, VSA_ERR_DEVICE_TIMEOUT, ...). Like
+ * the forward, it allocates nothing; the paper has no counterpart. */
+vsa_status_t vsa_check_static_workspace(vsa_plan_t plan, void* stream);
+
+/* vsa_diag_wait_timeout on the library-owned array: lets a test of the
+ * static-workspace path exercise its error report without a GPU fault. */
+vsa_status_t vsa_diag_wait_timeout_static(vsa_plan_t plan, int n_ctas, void* stream);
 
 void vsa_plan_destroy(vsa_plan_t plan);
 

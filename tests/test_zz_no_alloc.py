@@ -57,3 +57,26 @@ def test_static_workspace_rejects_plans_that_do_not_fit(cuda_ok):
             bsv.vsa_forward_static_workspace(plan, x, x, x, x, x)
     finally:
         bsv.vsa_plan_destroy(plan)
+
+
+def test_static_workspace_reports_device_errors(cuda_ok):
+    """The library-owned array keeps the forward's error words; the check that
+    goes with the entry point reads them (a bounded wait that ran out is planted
+    by the diagnostic kernel, no GPU fault), and the next forward starts clean."""
+    b, h, lt, la, lv, keep = 1, 2, 64, 64, 1024, 0.2
+    q, k, v, g = make_inputs(b, h, lt, la, lv, 0, device="cuda")
+    op = bsv.VSA(b, h, lt, la, lv, keep)
+    ref = op(q, k, v, g).clone()
+    op.check()
+    out = torch.empty_like(q)
+    bsv.vsa_forward_static_workspace(op.plan, q, k, v, g, out)
+    bsv.vsa_check_static_workspace(op.plan)
+    bsv.vsa_diag_wait_timeout_static(op.plan, n_ctas=4)
+    with pytest.raises(bsv.VsaError) as exc:
+        bsv.vsa_check_static_workspace(op.plan)
+    assert exc.value.status == bsv.VSA_ERR_DEVICE_TIMEOUT
+    out = torch.full_like(q, float("nan"))
+    bsv.vsa_forward_static_workspace(op.plan, q, k, v, g, out)
+    bsv.vsa_check_static_workspace(op.plan)
+    err = (out.float() - ref.float()).abs()
+    assert err.max().item() <= MAX_ABS and err.mean().item() <= MEAN_ABS
