@@ -20,7 +20,9 @@
 //        S^T[128 keys x 64 queries] = Kbar_chunk . Qbar^T      (A, B K-major)
 //      for each 128-key chunk; four warps move each chunk from TMEM (lane =
 //      key, column = query), scaled by 1/sqrt(128), into the scratch rows;
-//   B. one warp per query row: the row into registers, the exact top-k (a
+//   B. one warp per query row: the row into registers (through shared memory,
+//      the next row copied in while this one is worked on, for rows of up to
+//      1,280 keys), the exact top-k (a
 //      counting threshold search; the radix select where scores tie at the
 //      cut), the row maximum m, l = sum_j exp(s_j - m), and p_j = exp(s_j - m)
 //      written back over the row's own bytes as bf16 hi then bf16 lo rows;
@@ -58,7 +60,7 @@ constexpr int kWarpTma = 0, kWarpMma = 1, kWarpEpi0 = 4;
 constexpr int kEpiWarps = 8;                  // warps 4-11: lane quarter warp % 4, column half (warp - 4) / 4
 constexpr uint32_t kTmemCols = 256;           // two accumulator pairs of 64 columns
 constexpr unsigned int kDetailQ = 0xE00, kDetailFull = 0xE10, kDetailEmpty = 0xE20, kDetailAcc = 0xE30,
-                       kDetailAccEmpty = 0xE40, kDetailC = 0xE50;
+                       kDetailAccEmpty = 0xE40, kDetailC = 0xE50, kDetailRow = 0xE60;
 
 // shared memory from a 1024-byte aligned base: Qbar hi/lo, the ring, then
 // the row sums, the selection histograms, the barriers and the TMEM slot
@@ -68,7 +70,8 @@ constexpr uint32_t kOffL = kOffRing + kStages * kStageBytes;
 constexpr uint32_t kOffHist = kOffL + kRows * 4;
 constexpr uint32_t kOffBar = kOffHist + kWarps * kBins * 4;
 constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = kBarFull + kStages, kBarAccFull = kBarEmpty + kStages,
-              kBarAccEmpty = kBarAccFull + 2, kBarC = kBarAccEmpty + 2, kNumBars = kBarC + 1;
+              kBarAccEmpty = kBarAccFull + 2, kBarC = kBarAccEmpty + 2, kBarRow = kBarC + 1,
+              kNumBars = kBarRow + 2 * kWarps;  // kBarRow: two staged score rows a warp in phase B
 constexpr uint32_t kOffSlot = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -113,21 +116,43 @@ __device__ __forceinline__ void select_topk_regs(const float4 (&v)[NM], int T, i
     return;
   }
   auto at = [&](int m, int e) { return e == 0 ? v[m].x : e == 1 ? v[m].y : e == 2 ? v[m].z : v[m].w; };
-  float vmin = INFINITY, vmax = -INFINITY, s1 = 0.f, s2 = 0.f;
-  bool bad = false;
+  // Row moments. Slices m holding only keys < T take no per-entry test; the
+  // slice with the row's end skips the -inf entries past T. Four partial sums
+  // a lane keep the dependent chains short. A score that is not finite (or
+  // sums that overflow) sends the row to the radix select.
+  float mn[2] = {INFINITY, INFINITY}, mxv[2] = {-INFINITY, -INFINITY};
+  float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int m = 0; m < NM; ++m)
+  for (int m = 0; m < NM; ++m) {
+    if (128 * m + 128 <= T) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float x = at(m, e);
-      if (128 * m + 4 * lane + e < T) {
-        vmin = fminf(vmin, x);
-        vmax = fmaxf(vmax, x);
-        s1 += x;
-        s2 = fmaf(x, x, s2);
-        bad |= !(fabsf(x) <= 3.0e38f);
+      for (int e = 0; e < 4; ++e) {
+        const float x = at(m, e);
+        mn[e & 1] = fminf(mn[e & 1], x);
+        mxv[e & 1] = fmaxf(mxv[e & 1], x);
+        a1[e] += x;
+        a2[e] = fmaf(x, x, a2[e]);
+      }
+    } else if (128 * m < T) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x = at(m, e);
+        if (128 * m + 4 * lane + e < T) {
+          mn[e & 1] = fminf(mn[e & 1], x);
+          mxv[e & 1] = fmaxf(mxv[e & 1], x);
+          a1[e] += x;
+          a2[e] = fmaf(x, x, a2[e]);
+        }
       }
     }
+  }
+  float vmin = fminf(mn[0], mn[1]), vmax = fmaxf(mxv[0], mxv[1]);
+  float s1 = (a1[0] + a1[1]) + (a1[2] + a1[3]), s2 = (a2[0] + a2[1]) + (a2[2] + a2[3]);
+  // a lane with no key has vmin > vmax and zero sums: nothing to flag (a NaN
+  // key leaves the extremes alone but not the sum)
+  const bool has_key = vmin <= vmax || s1 != s1;
+  const bool bad =
+      has_key && !(fabsf(vmin) <= 3.0e38f && fabsf(vmax) <= 3.0e38f && fabsf(s1) <= 3.0e38f && s2 <= 3.0e38f);
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
     vmin = fminf(vmin, __shfl_xor_sync(full, vmin, o));
@@ -273,6 +298,15 @@ __device__ __forceinline__ void select_topk_regs(const float4 (&v)[NM], int T, i
   }
 }
 
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -314,6 +348,7 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
       mbar_init(bar(kBarAccEmpty + a), kEpiWarps);
     }
     mbar_init(bar(kBarC), 2);
+    for (int i = 0; i < 2 * kWarps; ++i) mbar_init(bar(kBarRow + i), 1);
     fence_barrier_init();
   }
   if (warp == kWarpMma) tmem_alloc(smem_u32(tslot), kTmemCols);
@@ -329,6 +364,7 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
   // over all units: phase A takes 2 stages (K hi, K lo) and one accumulator
   // pair per chunk, phase C 3 stages (V hi, V lo, P hi + lo) per chunk.
   uint32_t ring0 = 0, acc0 = 0, units_done = 0;
+  uint32_t rows_staged = 0;  // score rows this warp has taken in phase B, over all units
   for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
     const int bh = u / groups_cap;
     const int q0 = (u - bh * groups_cap) * kRows;
@@ -437,6 +473,8 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarAccEmpty + a));
       }
+      // phase B copies the score rows into shared memory through the async proxy
+      fence_proxy_async_global();
     }
     ring0 += 2 * n_chunks;
     acc0 += n_chunks;
@@ -444,13 +482,41 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
     if (failed) break;
 
     // ------------------------------------------------------------ phase B: selection, softmax, P
-    for (int r = warp; r < n_rows; r += kWarps) {
+    // With rows of up to 1,280 keys, each warp's next row is copied into shared
+    // memory (the ring is idle in this phase; two buffers a warp) while the
+    // current one is worked on, so its loads come from shared memory.
+    constexpr bool kStaged = NM <= 10;
+    static_assert(!kStaged || 2 * kWarps * 128 * 10 * 4 <= kStages * kStageBytes, "staged rows fit the ring");
+    const uint32_t row_bytes = (static_cast<uint32_t>(T) * 4u + 15u) & ~15u;
+    auto stage_buf = [&](uint32_t n) {
+      return sbase + kOffRing + static_cast<uint32_t>(warp * 2 + static_cast<int>(n & 1u)) * p.tp_cap * 4u;
+    };
+    auto stage_issue = [&](uint32_t n, int r) {
+      if (lane == 0) {
+        const uint32_t b = bar(kBarRow + warp * 2 + static_cast<int>(n & 1u));
+        fence_proxy_async_smem();  // this buffer's earlier reads come before the copy overwrites it
+        mbar_arrive_expect_tx(b, row_bytes);
+        bulk_load(stage_buf(n), rows + static_cast<size_t>(r) * p.tp_cap, row_bytes, b);
+      }
+    };
+    if (kStaged && warp < n_rows) stage_issue(rows_staged, warp);
+    for (int r = warp; r < n_rows && !failed; r += kWarps, ++rows_staged) {
       float* row = rows + static_cast<size_t>(r) * p.tp_cap;
+      if (kStaged && r + kWarps < n_rows) stage_issue(rows_staged + 1, r + kWarps);
+      if (kStaged &&
+          !__all_sync(0xffffffffu, mbar_wait(bar(kBarRow + warp * 2 + static_cast<int>(rows_staged & 1u)),
+                                             (rows_staged >> 1) & 1u, err, kDetailRow))) {
+        failed = true;
+        break;
+      }
       float4 v[NM];
 #pragma unroll
       for (int m = 0; m < NM; ++m) {
         const int j = 128 * m + 4 * lane;  // T_pad is a multiple of 128, so j + 3 < T_pad
-        v[m] = j < T ? reinterpret_cast<const float4*>(row)[32 * m + lane] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (j < T) x = kStaged ? ld_shared_f4(stage_buf(rows_staged) + 16u * static_cast<uint32_t>(32 * m + lane))
+                               : reinterpret_cast<const float4*>(row)[32 * m + lane];
+        v[m] = x;
         if (j + 3 >= T) {  // the row's ragged end: entries past T are -inf
           if (j + 1 >= T) v[m].y = -INFINITY;
           if (j + 2 >= T) v[m].z = -INFINITY;
@@ -489,8 +555,10 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
       for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
       if (lane == 0) l_row[r] = l;
     }
-    // P is read back by TMA (the async proxy): order these generic writes before it
+    // P is read back by TMA (the async proxy): order these generic writes before it,
+    // and the reads of the staged rows before the TMA writes of phase C
     fence_proxy_async_global();
+    fence_proxy_async_smem();
     failed = __syncthreads_or(failed);
     if (failed) break;
 
