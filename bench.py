@@ -617,6 +617,44 @@ def run_ours(args):
         except Exception:
             traffic = None
 
+    # ---- end to end through the host-buffer entry point
+    e2e = None
+    if args.e2e_steps > 0:
+        # this rank's heads as they arrive on the host (contiguous, pinned), and the device
+        # forward's output of the same heads to check the host path against
+        dev_out = out_slice.contiguous().cpu()
+        hq, hk, hv, hg = [x.contiguous().cpu().pin_memory() for x in ins]
+        hout = torch.empty_like(hq).pin_memory()
+        dbuf = torch.empty(bsv.vsa_plan_host_path_bytes(op.plan), dtype=torch.uint8, device=dev)
+        for _ in range(2):
+            bsv.vsa_forward_host(op.plan, hq, hk, hv, hg, hout, dbuf)
+        barrier(world)
+        times = []
+        for _ in range(args.e2e_steps):
+            hout.fill_(float("nan"))  # outside the timed call: every step must write the whole output
+            barrier(world)
+            t0 = time.perf_counter()
+            bsv.vsa_forward_host(op.plan, hq, hk, hv, hg, hout, dbuf)
+            times.append(time.perf_counter() - t0)
+        # the last step's output, bit for bit against the device forward (outside the timed region)
+        same = bool(torch.equal(hout.view(torch.int16), dev_out.view(torch.int16)))
+        same = reduce_max(0.0 if same else 1.0, world, dev) == 0.0
+        # host wall clock, the mean over the steps (max over ranks); the median, min and max are
+        # reported beside it
+        e2e_s = reduce_max(statistics.mean(times), world, dev)
+        tb = hq.numel() * hq.element_size()
+        e2e = {"value": total_flops / e2e_s / 1e12 if same else None, "unit": UNIT, "ms_per_step": e2e_s * 1e3,
+               "statistic": f"mean of {len(times)} steps",
+               "median_ms": statistics.median(times) * 1e3, "min_ms": min(times) * 1e3,
+               "max_ms": max(times) * 1e3, "steps_ms": [round(t * 1e3, 2) for t in times],
+               "steps_over_twice_median": sum(t > 2 * statistics.median(times) for t in times),
+               "bitwise_equal_to_device_forward": same,
+               "h2d_bytes_per_step": int(reduce_sum(4 * tb, world, dev)),
+               "d2h_bytes_per_step": int(reduce_sum(tb, world, dev)),
+               "api": "vsa_forward_host (C ABI), pinned host buffers of this rank's heads, synchronous; "
+                      "head groups pipelined: copy-in, forward and copy-out overlap"}
+        del dev_out, hq, hk, hv, hg, hout, dbuf
+
     # the lines measured beside the step belong to the single-GPU benchmark workload only
     side = cfg.name == "10s" and args.keep is None and world == 1
 
@@ -641,45 +679,6 @@ def run_ours(args):
     if not args.no_send_layout and side:
         send_layout = measure_send_layout(op, q, k, v, g, cfg, dev, stream, flush, steps, args.warmup, world,
                                           cfg.seed + 300)
-
-    # ---- end to end through the host-buffer entry point
-    e2e = None
-    if args.e2e_steps > 0:
-        # this rank's heads as they arrive on the host (contiguous, pinned), and the device
-        # forward's output of the same heads to check the host path against
-        dev_out = out_slice.contiguous().cpu()
-        hq, hk, hv, hg = [x.contiguous().cpu().pin_memory() for x in ins]
-        hout = torch.empty_like(hq).pin_memory()
-        del out, out_slice, ins, q, k, v, g
-        torch.cuda.empty_cache()
-        dbuf = torch.empty(bsv.vsa_plan_host_path_bytes(op.plan), dtype=torch.uint8, device=dev)
-        for _ in range(2):
-            bsv.vsa_forward_host(op.plan, hq, hk, hv, hg, hout, dbuf)
-        barrier(world)
-        times = []
-        for _ in range(args.e2e_steps):
-            hout.fill_(float("nan"))  # outside the timed call: every step must write the whole output
-            barrier(world)
-            t0 = time.perf_counter()
-            bsv.vsa_forward_host(op.plan, hq, hk, hv, hg, hout, dbuf)
-            times.append(time.perf_counter() - t0)
-        # the last step's output, bit for bit against the device forward (outside the timed region)
-        same = bool(torch.equal(hout.view(torch.int16), dev_out.view(torch.int16)))
-        same = reduce_max(0.0 if same else 1.0, world, dev) == 0.0
-        # host wall clock, the mean over the steps (max over ranks); the median, min and max are
-        # reported beside it
-        e2e_s = reduce_max(statistics.mean(times), world, dev)
-        tb = hq.numel() * hq.element_size()
-        e2e = {"value": total_flops / e2e_s / 1e12 if same else None, "unit": UNIT, "ms_per_step": e2e_s * 1e3,
-               "statistic": f"mean of {len(times)} steps",
-               "median_ms": statistics.median(times) * 1e3, "min_ms": min(times) * 1e3,
-               "max_ms": max(times) * 1e3, "steps_ms": [round(t * 1e3, 2) for t in times],
-               "bitwise_equal_to_device_forward": same,
-               "h2d_bytes_per_step": int(reduce_sum(4 * tb, world, dev)),
-               "d2h_bytes_per_step": int(reduce_sum(tb, world, dev)),
-               "api": "vsa_forward_host (C ABI), pinned host buffers of this rank's heads, synchronous; "
-                      "head groups pipelined: copy-in, forward and copy-out overlap"}
-        del dev_out, hq, hk, hv, hg, hout, dbuf
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
