@@ -20,9 +20,9 @@
 //        S^T[128 keys x 64 queries] = Kbar_chunk . Qbar^T      (A, B K-major)
 //      for each 128-key chunk; four warps move each chunk from TMEM (lane =
 //      key, column = query), scaled by 1/sqrt(128), into the scratch rows;
-//   B. one warp per query row: the row into registers (through shared memory,
-//      the next row copied in while this one is worked on, for rows of up to
-//      1,280 keys), the exact top-k (a
+//   B. one warp per query row: the row copied into shared memory and read
+//      from there (rows of up to 1,280 keys) or held in registers, the exact
+//      top-k (a
 //      counting threshold search; the radix select where scores tie at the
 //      cut), the row maximum m, l = sum_j exp(s_j - m), and p_j = exp(s_j - m)
 //      written back over the row's own bytes as bf16 hi then bf16 lo rows;
@@ -33,13 +33,15 @@
 // Score errors of ~2^-16 relative sit far inside the selection's 1e-3 tie
 // band; the selection itself is an integer decision on the fp32 scores.
 //
-// Warp roles (12 warps): warp 0 issues the TMA loads (four issuing lanes, one
-// 8 KB box each) through a ring of 32 KB stages; warps 1 and 2 issue the
-// MMAs, converged with one elected lane each, splitting every chunk's 24
-// products between two accumulators (a single issuer leaves the pipe idle
-// between N = 64 MMAs); warps 4-11 move scores and outputs out of TMEM (two
-// per lane quarter, 32 columns each); all 12
-// warps run phase B. Every wait is bounded.
+// Warp roles: warp 0 issues the TMA loads (four issuing lanes, one 8 KB box
+// each) through a ring of 32 KB stages; warps 1 and 2 issue the MMAs,
+// converged with one elected lane each, splitting every chunk's 24 products
+// between two accumulators (a single issuer leaves the pipe idle between
+// N = 64 MMAs); warps from 4 move scores and outputs out of TMEM (per lane
+// quarter, a share of the 64 columns each); every warp runs phase B. Rows of up
+// to 1,280 keys: 24 warps (16 movers), the row read from shared memory in
+// phase B; longer rows: 12 warps (8 movers), the row held in registers. Every
+// wait is bounded.
 #include <cmath>
 
 #include "kernels.cuh"
@@ -49,32 +51,42 @@
 namespace vsa {
 namespace {
 
-constexpr int kThreads = 384;                 // 12 warps: up to 168 registers a thread for a row in registers
-constexpr int kWarps = kThreads / 32;
+// Two builds: rows of up to 1,280 keys (NM <= 10) stay in shared memory in
+// phase B, so the CTA runs 24 warps of at most 80 registers (twice the warps
+// to hide a row's dependent chain); longer rows are held in registers by 12
+// warps of up to 168 registers.
+__host__ __device__ constexpr bool smem_rows(int nm) { return nm <= 10; }
+__host__ __device__ constexpr int threads_of(int nm) { return smem_rows(nm) ? 768 : 384; }
 constexpr int kRows = 64;                     // query tiles per unit: the MMA's N
 constexpr int kChunk = 128;                   // key tiles per chunk: the MMA's M
 constexpr int kStages = 5;                    // ring stages of 32 KB
 constexpr uint32_t kStageBytes = kChunk * kHeadDim * 2;
 constexpr uint32_t kQBytes = 2 * kRows * kHeadDim * 2;  // Qbar hi and lo, 64 rows each
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpEpi0 = 4;
-constexpr int kEpiWarps = 8;                  // warps 4-11: lane quarter warp % 4, column half (warp - 4) / 4
+// TMEM movers from warp 4: lane quarter warp % 4, column group (warp - 4) / 4
+__host__ __device__ constexpr int epi_warps_of(int nm) { return smem_rows(nm) ? 16 : 8; }
 constexpr uint32_t kTmemCols = 256;           // two accumulator pairs of 64 columns
 constexpr unsigned int kDetailQ = 0xE00, kDetailFull = 0xE10, kDetailEmpty = 0xE20, kDetailAcc = 0xE30,
                        kDetailAccEmpty = 0xE40, kDetailC = 0xE50, kDetailRow = 0xE60;
 
-// shared memory from a 1024-byte aligned base: Qbar hi/lo, the ring, then
-// the row sums, the selection histograms, the barriers and the TMEM slot
+// shared memory from a 1024-byte aligned base: Qbar hi/lo, the ring (which
+// holds the staged score rows in phase B), then the row sums, the selection
+// histograms, the barriers and the TMEM slot
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffRing = kOffQ + kQBytes;
 constexpr uint32_t kOffL = kOffRing + kStages * kStageBytes;
 constexpr uint32_t kOffHist = kOffL + kRows * 4;
-constexpr uint32_t kOffBar = kOffHist + kWarps * kBins * 4;
+__host__ __device__ constexpr uint32_t off_bar_of(int nm) { return kOffHist + (threads_of(nm) / 32) * kBins * 4; }
 constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = kBarFull + kStages, kBarAccFull = kBarEmpty + kStages,
-              kBarAccEmpty = kBarAccFull + 2, kBarC = kBarAccEmpty + 2, kBarRow = kBarC + 1,
-              kNumBars = kBarRow + 2 * kWarps;  // kBarRow: two staged score rows a warp in phase B
-constexpr uint32_t kOffSlot = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;  // + alignment slack
-static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+              kBarAccEmpty = kBarAccFull + 2, kBarC = kBarAccEmpty + 2, kBarRow = kBarC + 1;
+// kBarRow: the staged score row of each warp in phase B
+__host__ __device__ constexpr int num_bars_of(int nm) { return kBarRow + threads_of(nm) / 32; }
+__host__ __device__ constexpr uint32_t off_slot_of(int nm) { return off_bar_of(nm) + num_bars_of(nm) * 8; }
+__host__ __device__ constexpr uint32_t smem_bytes_of(int nm) { return off_slot_of(nm) + 16 + 1024; }  // + alignment slack
+static_assert(smem_bytes_of(5) <= 227 * 1024 && smem_bytes_of(10) <= 227 * 1024 && smem_bytes_of(18) <= 227 * 1024,
+              "shared memory");
+// phase B, rows in shared memory: one 128 NM-key buffer a warp in the ring
+static_assert(24 * 128 * 10 * 4 <= kStages * kStageBytes, "staged rows fit the ring");
 
 struct CoarseParams {
   Geometry cap;             // the plan's geometry: T_cap, k_cap and the layouts
@@ -87,8 +99,8 @@ struct CoarseParams {
   unsigned int* err;
 };
 
-// A query row held in registers: lane l holds keys 128 m + 4 l .. + 3 in
-// v[m].x .. .w, m < NM (-inf past T), so each m is one coalesced float4 load.
+// A query row as a warp sees it: lane l takes keys 128 m + 4 l .. + 3 as one
+// float4 for m < NM (-inf past T), one coalesced 16-byte access per m.
 
 // Exclusive prefix sum of a small per-lane count over the warp, and the total.
 __device__ __forceinline__ int warp_exclusive_scan(int x, int lane, int& total) {
@@ -107,15 +119,19 @@ __device__ __forceinline__ int warp_exclusive_scan(int x, int lane, int& total) 
 // counting search for a threshold with exactly k entries at or above it; the
 // radix select where entries tie at the cut or a score is not finite). h: kBins
 // ints of shared memory for the radix select.
-template <int NM>
-__device__ __forceinline__ void select_topk_regs(const float4 (&v)[NM], int T, int k, int* h, int32_t* dst,
-                                                 int lane) {
+__device__ __forceinline__ float f4_at(const float4& v, int e) {
+  return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+
+// row(m): lane l's keys 128 m + 4 l .. + 3 as a float4 (-inf past T), from
+// registers or from shared memory.
+template <int NM, typename Row>
+__device__ __forceinline__ void select_topk(const Row& row, int T, int k, int* h, int32_t* dst, int lane) {
   const unsigned full = 0xffffffffu;
   if (k >= T) {
     for (int j = lane; j < T; j += 32) dst[j] = j;
     return;
   }
-  auto at = [&](int m, int e) { return e == 0 ? v[m].x : e == 1 ? v[m].y : e == 2 ? v[m].z : v[m].w; };
   // Row moments. Slices m holding only keys < T take no per-entry test; the
   // slice with the row's end skips the -inf entries past T. Four partial sums
   // a lane keep the dependent chains short. A score that is not finite (or
@@ -125,18 +141,20 @@ __device__ __forceinline__ void select_topk_regs(const float4 (&v)[NM], int T, i
 #pragma unroll
   for (int m = 0; m < NM; ++m) {
     if (128 * m + 128 <= T) {
+      const float4 vm = row(m);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float x = at(m, e);
+        const float x = f4_at(vm, e);
         mn[e & 1] = fminf(mn[e & 1], x);
         mxv[e & 1] = fmaxf(mxv[e & 1], x);
         a1[e] += x;
         a2[e] = fmaf(x, x, a2[e]);
       }
     } else if (128 * m < T) {
+      const float4 vm = row(m);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float x = at(m, e);
+        const float x = f4_at(vm, e);
         if (128 * m + 4 * lane + e < T) {
           mn[e & 1] = fminf(mn[e & 1], x);
           mxv[e & 1] = fmaxf(mxv[e & 1], x);
@@ -163,7 +181,11 @@ __device__ __forceinline__ void select_topk_regs(const float4 (&v)[NM], int T, i
   auto count_ge = [&](float x) {  // -inf past T never counts (x > vmin >= -inf)
     int c = 0;
 #pragma unroll
-    for (int m = 0; m < NM; ++m) c += (v[m].x >= x) + (v[m].y >= x) + (v[m].z >= x) + (v[m].w >= x);
+    for (int m = 0; m < NM; ++m)
+      if (128 * m < T) {  // slices past T hold -inf only
+        const float4 vm = row(m);
+        c += (vm.x >= x) + (vm.y >= x) + (vm.z >= x) + (vm.w >= x);
+      }
     return static_cast<int>(__reduce_add_sync(full, static_cast<unsigned>(c)));
   };
   float theta = 0.f;
@@ -206,7 +228,9 @@ __device__ __forceinline__ void select_topk_regs(const float4 (&v)[NM], int T, i
     int written = 0;
 #pragma unroll
     for (int m = 0; m < NM; ++m) {
-      const bool s0 = v[m].x >= theta, s1b = v[m].y >= theta, s2b = v[m].z >= theta, s3 = v[m].w >= theta;
+      if (128 * m >= T) break;  // slices past T hold -inf only
+      const float4 vm = row(m);
+      const bool s0 = vm.x >= theta, s1b = vm.y >= theta, s2b = vm.z >= theta, s3 = vm.w >= theta;
       const unsigned b0 = __ballot_sync(full, s0), b1 = __ballot_sync(full, s1b), b2 = __ballot_sync(full, s2b),
                      b3 = __ballot_sync(full, s3);  // -inf past T never reaches theta
       int pos = written + __popc(b0 & lt_mask) + __popc(b1 & lt_mask) + __popc(b2 & lt_mask) + __popc(b3 & lt_mask);
@@ -228,13 +252,15 @@ __device__ __forceinline__ void select_topk_regs(const float4 (&v)[NM], int T, i
     for (int b = lane; b < kBins; b += 32) h[b] = 0;
     __syncwarp();
 #pragma unroll
-    for (int m = 0; m < NM; ++m)
+    for (int m = 0; m < NM; ++m) {
+      const float4 vm = row(m);
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         if (128 * m + 4 * lane + e < T) {
-          const uint32_t key = order_key(at(m, e));
+          const uint32_t key = order_key(f4_at(vm, e));
           if ((key & pmask) == prefix) atomicAdd(&h[(key >> shift) & 0xFFu], 1);
         }
+    }
     __syncwarp();
     int c[8], lsum = 0;
 #pragma unroll
@@ -270,10 +296,11 @@ __device__ __forceinline__ void select_topk_regs(const float4 (&v)[NM], int T, i
   for (int m = 0; m < NM; ++m) {
     bool gt[4], eq[4];
     int n_eq = 0;
+    const float4 vm = row(m);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const bool in = 128 * m + 4 * lane + e < T;
-      const uint32_t key = in ? order_key(at(m, e)) : 0u;
+      const uint32_t key = in ? order_key(f4_at(vm, e)) : 0u;
       gt[e] = in && key > prefix;
       eq[e] = in && key == prefix;
       n_eq += eq[e];
@@ -298,6 +325,10 @@ __device__ __forceinline__ void select_topk_regs(const float4 (&v)[NM], int T, i
   }
 }
 
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -312,7 +343,7 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 }
 
 template <int NM>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of(NM), 1)
 coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
                  const __grid_constant__ CUtensorMap map_kh, const __grid_constant__ CUtensorMap map_kl,
                  const __grid_constant__ CUtensorMap map_vh, const __grid_constant__ CUtensorMap map_vl,
@@ -322,6 +353,10 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.dl.invalid = 1u;
     return;
   }
+  constexpr int kThreads = threads_of(NM), kWarps = kThreads / 32, kEpiWarps = epi_warps_of(NM);
+  constexpr int kMoverCols = 4 * kRows / kEpiWarps;  // query columns a mover takes
+  constexpr bool kSmemRows = smem_rows(NM);
+  constexpr uint32_t kOffBar = off_bar_of(NM), kOffSlot = off_slot_of(NM);
   const int T = dg.T, k = dg.k, T_cap = p.cap.T, k_cap = p.cap.k;
   const int n_chunks = (T + kChunk - 1) / kChunk;
   const int groups_cap = (T_cap + kRows - 1) / kRows;
@@ -348,7 +383,7 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
       mbar_init(bar(kBarAccEmpty + a), kEpiWarps);
     }
     mbar_init(bar(kBarC), 2);
-    for (int i = 0; i < 2 * kWarps; ++i) mbar_init(bar(kBarRow + i), 1);
+    for (int i = 0; i < kWarps; ++i) mbar_init(bar(kBarRow + i), 1);
     fence_barrier_init();
   }
   if (warp == kWarpMma) tmem_alloc(smem_u32(tslot), kTmemCols);
@@ -440,7 +475,7 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
         if (!failed) umma_commit_elect(bar(kBarAccFull + a));
       }
     } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
-      // lane quarter q (TMEM lane = key 128 c + 32 q + lane), columns 32 ch .. + 31
+      // lane quarter q (TMEM lane = key 128 c + 32 q + lane), columns kMoverCols ch ..
       const int q = warp % 4, ch = (warp - kWarpEpi0) / 4;
       const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
       for (int c = 0; c < n_chunks && !failed; ++c) {
@@ -453,8 +488,8 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
         tc_fence_after();
         const int key = kChunk * c + 32 * q + lane;
 #pragma unroll
-        for (int part = 0; part < kRows / 32; ++part) {
-          const int col = 32 * ch + 16 * part;
+        for (int part = 0; part < kMoverCols / 16; ++part) {
+          const int col = kMoverCols * ch + 16 * part;
           uint32_t x0[16], x1[16];
           tmem_ld16(tbase + lane_off + static_cast<uint32_t>(2 * a * kRows + col), x0);
           tmem_ld16(tbase + lane_off + static_cast<uint32_t>((2 * a + 1) * kRows + col), x1);
@@ -482,52 +517,14 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
     if (failed) break;
 
     // ------------------------------------------------------------ phase B: selection, softmax, P
-    // With rows of up to 1,280 keys, each warp's next row is copied into shared
-    // memory (the ring is idle in this phase; two buffers a warp) while the
-    // current one is worked on, so its loads come from shared memory.
-    constexpr bool kStaged = NM <= 10;
-    static_assert(!kStaged || 2 * kWarps * 128 * 10 * 4 <= kStages * kStageBytes, "staged rows fit the ring");
-    const uint32_t row_bytes = (static_cast<uint32_t>(T) * 4u + 15u) & ~15u;
-    auto stage_buf = [&](uint32_t n) {
-      return sbase + kOffRing + static_cast<uint32_t>(warp * 2 + static_cast<int>(n & 1u)) * p.tp_cap * 4u;
-    };
-    auto stage_issue = [&](uint32_t n, int r) {
-      if (lane == 0) {
-        const uint32_t b = bar(kBarRow + warp * 2 + static_cast<int>(n & 1u));
-        fence_proxy_async_smem();  // this buffer's earlier reads come before the copy overwrites it
-        mbar_arrive_expect_tx(b, row_bytes);
-        bulk_load(stage_buf(n), rows + static_cast<size_t>(r) * p.tp_cap, row_bytes, b);
-      }
-    };
-    if (kStaged && warp < n_rows) stage_issue(rows_staged, warp);
-    for (int r = warp; r < n_rows && !failed; r += kWarps, ++rows_staged) {
-      float* row = rows + static_cast<size_t>(r) * p.tp_cap;
-      if (kStaged && r + kWarps < n_rows) stage_issue(rows_staged + 1, r + kWarps);
-      if (kStaged &&
-          !__all_sync(0xffffffffu, mbar_wait(bar(kBarRow + warp * 2 + static_cast<int>(rows_staged & 1u)),
-                                             (rows_staged >> 1) & 1u, err, kDetailRow))) {
-        failed = true;
-        break;
-      }
-      float4 v[NM];
-#pragma unroll
-      for (int m = 0; m < NM; ++m) {
-        const int j = 128 * m + 4 * lane;  // T_pad is a multiple of 128, so j + 3 < T_pad
-        float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        if (j < T) x = kStaged ? ld_shared_f4(stage_buf(rows_staged) + 16u * static_cast<uint32_t>(32 * m + lane))
-                               : reinterpret_cast<const float4*>(row)[32 * m + lane];
-        v[m] = x;
-        if (j + 3 >= T) {  // the row's ragged end: entries past T are -inf
-          if (j + 1 >= T) v[m].y = -INFINITY;
-          if (j + 2 >= T) v[m].z = -INFINITY;
-          if (j + 3 >= T) v[m].w = -INFINITY;
-        }
-      }
-      select_topk_regs<NM>(v, T, k, hist + warp * kBins,
-                           p.tile_index + (static_cast<size_t>(bh) * T_cap + q0 + r) * k_cap, lane);
+    auto softmax_row = [&](auto&& rowf, float* row, int r) {
       float mx = -INFINITY;
 #pragma unroll
-      for (int m = 0; m < NM; ++m) mx = fmaxf(mx, fmaxf(fmaxf(v[m].x, v[m].y), fmaxf(v[m].z, v[m].w)));
+      for (int m = 0; m < NM; ++m)
+        if (128 * m < T) {
+          const float4 vm = rowf(m);
+          mx = fmaxf(mx, fmaxf(fmaxf(vm.x, vm.y), fmaxf(vm.z, vm.w)));
+        }
 #pragma unroll
       for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       // p = exp(s - max) = 2^((s - max) log2 e); entries past T give 2^-inf = 0
@@ -539,10 +536,11 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
 #pragma unroll
       for (int m = 0; m < NM; ++m) {
         if (128 * m < kChunk * n_chunks) {
-          const float e0 = ex2_approx(fmaf(v[m].x, 1.4426950408889634f, nmx));
-          const float e1 = ex2_approx(fmaf(v[m].y, 1.4426950408889634f, nmx));
-          const float e2 = ex2_approx(fmaf(v[m].z, 1.4426950408889634f, nmx));
-          const float e3 = ex2_approx(fmaf(v[m].w, 1.4426950408889634f, nmx));
+          const float4 vm = rowf(m);
+          const float e0 = ex2_approx(fmaf(vm.x, 1.4426950408889634f, nmx));
+          const float e1 = ex2_approx(fmaf(vm.y, 1.4426950408889634f, nmx));
+          const float e2 = ex2_approx(fmaf(vm.z, 1.4426950408889634f, nmx));
+          const float e3 = ex2_approx(fmaf(vm.w, 1.4426950408889634f, nmx));
           l += (e0 + e1) + (e2 + e3);
           uint32_t h01, l01, h23, l23;
           split_bf16_pair(e0, e1, h01, l01);
@@ -554,6 +552,57 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
 #pragma unroll
       for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
       if (lane == 0) l_row[r] = l;
+    };
+    if constexpr (kSmemRows) {
+      // each warp copies its row into its own buffer in the ring (idle in this
+      // phase), marks the entries past T as -inf, and reads it from there
+      const uint32_t buf = sbase + kOffRing + static_cast<uint32_t>(warp) * (NM * 512u);
+      const uint32_t row_bytes = (static_cast<uint32_t>(T) * 4u + 15u) & ~15u;
+      for (int r = warp; r < n_rows && !failed; r += kWarps, ++rows_staged) {
+        float* row = rows + static_cast<size_t>(r) * p.tp_cap;
+        if (lane == 0) {
+          fence_proxy_async_smem();  // the buffer's earlier reads come before the copy overwrites it
+          mbar_arrive_expect_tx(bar(kBarRow + warp), row_bytes);
+          bulk_load(buf, row, row_bytes, bar(kBarRow + warp));
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarRow + warp), rows_staged & 1u, err, kDetailRow))) {
+          failed = true;
+          break;
+        }
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+          const int j = 128 * m + 4 * lane;
+          if (j + 3 >= T)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (j + e >= T) st_shared_f32(buf + 4u * static_cast<uint32_t>(j + e), -INFINITY);
+        }
+        __syncwarp();
+        auto rowf = [&](int m) { return ld_shared_f4(buf + 16u * static_cast<uint32_t>(32 * m + lane)); };
+        select_topk<NM>(rowf, T, k, hist + warp * kBins,
+                        p.tile_index + (static_cast<size_t>(bh) * T_cap + q0 + r) * k_cap, lane);
+        softmax_row(rowf, row, r);
+      }
+    } else {
+      for (int r = warp; r < n_rows; r += kWarps) {
+        float* row = rows + static_cast<size_t>(r) * p.tp_cap;
+        float4 v[NM];
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+          const int j = 128 * m + 4 * lane;  // T_pad is a multiple of 128, so j + 3 < T_pad
+          v[m] = j < T ? reinterpret_cast<const float4*>(row)[32 * m + lane]
+                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          if (j + 3 >= T) {  // the row's ragged end: entries past T are -inf
+            if (j + 1 >= T) v[m].y = -INFINITY;
+            if (j + 2 >= T) v[m].z = -INFINITY;
+            if (j + 3 >= T) v[m].w = -INFINITY;
+          }
+        }
+        auto rowf = [&](int m) { return v[m]; };
+        select_topk<NM>(rowf, T, k, hist + warp * kBins,
+                        p.tile_index + (static_cast<size_t>(bh) * T_cap + q0 + r) * k_cap, lane);
+        softmax_row(rowf, row, r);
+      }
     }
     // P is read back by TMA (the async proxy): order these generic writes before it,
     // and the reads of the staged rows before the TMA writes of phase C
@@ -628,7 +677,7 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
       }
       if (!failed) umma_commit_elect(bar(kBarC));
     } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
-      // lane quarter q (TMEM lane = head dim 32 q + lane), columns 32 ch .. + 31
+      // lane quarter q (TMEM lane = head dim 32 q + lane), columns kMoverCols ch ..
       const int q = warp % 4, ch = (warp - kWarpEpi0) / 4;
       const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
       const int dim = 32 * q + lane;
@@ -637,8 +686,8 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
       } else {
         tc_fence_after();
 #pragma unroll
-        for (int part = 0; part < kRows / 32; ++part) {
-          const int col = 32 * ch + 16 * part;
+        for (int part = 0; part < kMoverCols / 16; ++part) {
+          const int col = kMoverCols * ch + 16 * part;
           uint32_t x0[16], x1[16];
           tmem_ld16(tbase + lane_off + static_cast<uint32_t>(col), x0);
           tmem_ld16(tbase + lane_off + static_cast<uint32_t>(kRows + col), x1);
@@ -699,10 +748,11 @@ split_kernel(const float* __restrict__ pq, const float* __restrict__ pk, const f
 
 template <int NM>
 cudaError_t launch_nm(const CUtensorMap (&maps)[7], const CoarseParams& p, int grid, cudaStream_t stream) {
+  constexpr uint32_t kSmemBytes = smem_bytes_of(NM);
   cudaError_t e = cudaFuncSetAttribute(coarse_tc_kernel<NM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  coarse_tc_kernel<NM><<<grid, kThreads, kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
+  coarse_tc_kernel<NM><<<grid, threads_of(NM), kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
                                                               maps[5], maps[6], p);
   return cudaGetLastError();
 }
