@@ -20,7 +20,8 @@
 //        S^T[128 keys x 64 queries] = Kbar_chunk . Qbar^T      (A, B K-major)
 //      for each 128-key chunk; four warps move each chunk from TMEM (lane =
 //      key, column = query), scaled by 1/sqrt(128), into the scratch rows;
-//   B. one warp per query row: the row copied into shared memory and read
+//   B. one warp per query row (rows handed out one at a time, as a row's cost
+//      varies with its search): the row copied into shared memory and read
 //      from there (rows of up to 1,280 keys) or held in registers, the exact
 //      top-k (a
 //      counting threshold search; the radix select where scores tie at the
@@ -369,6 +370,7 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
   int* hist = reinterpret_cast<int*>(smem + kOffHist);
   auto bar = [&](int i) { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
+  int* next_row = reinterpret_cast<int*>(smem + kOffSlot + 4);  // phase B: rows handed out so far
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   unsigned int* err = p.err;
@@ -511,6 +513,7 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
       // phase B copies the score rows into shared memory through the async proxy
       fence_proxy_async_global();
     }
+    if (tid == 0) *next_row = 0;  // read in phase B, after the barrier below
     ring0 += 2 * n_chunks;
     acc0 += n_chunks;
     failed = __syncthreads_or(failed);
@@ -558,7 +561,8 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
       // phase), marks the entries past T as -inf, and reads it from there
       const uint32_t buf = sbase + kOffRing + static_cast<uint32_t>(warp) * (NM * 512u);
       const uint32_t row_bytes = (static_cast<uint32_t>(T) * 4u + 15u) & ~15u;
-      for (int r = warp; r < n_rows && !failed; r += kWarps, ++rows_staged) {
+      // rows are handed out one at a time (a row's cost varies with its search)
+      for (int r = warp; r < n_rows && !failed; ++rows_staged) {
         float* row = rows + static_cast<size_t>(r) * p.tp_cap;
         if (lane == 0) {
           fence_proxy_async_smem();  // the buffer's earlier reads come before the copy overwrites it
@@ -582,9 +586,12 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
         select_topk<NM>(rowf, T, k, hist + warp * kBins,
                         p.tile_index + (static_cast<size_t>(bh) * T_cap + q0 + r) * k_cap, lane);
         softmax_row(rowf, row, r);
+        int nr = 0;
+        if (lane == 0) nr = kWarps + atomicAdd(next_row, 1);
+        r = __shfl_sync(0xffffffffu, nr, 0);
       }
     } else {
-      for (int r = warp; r < n_rows; r += kWarps) {
+      for (int r = warp; r < n_rows;) {
         float* row = rows + static_cast<size_t>(r) * p.tp_cap;
         float4 v[NM];
 #pragma unroll
@@ -602,6 +609,9 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
         select_topk<NM>(rowf, T, k, hist + warp * kBins,
                         p.tile_index + (static_cast<size_t>(bh) * T_cap + q0 + r) * k_cap, lane);
         softmax_row(rowf, row, r);
+        int nr = 0;
+        if (lane == 0) nr = kWarps + atomicAdd(next_row, 1);
+        r = __shfl_sync(0xffffffffu, nr, 0);
       }
     }
     // P is read back by TMA (the async proxy): order these generic writes before it,
