@@ -234,7 +234,7 @@ vsa_status_t create_plan(const vsa_shape_t* shape, int device, bool subblock, do
 
 void destroy_plan(vsa_plan* p);
 
-// The host-buffer path pipelines up to 8 head groups (host only: the streams
+// The host-buffer path pipelines head groups of up to 8 heads (host only: the streams
 // and events are created on the first call).
 // Head widths of the pipeline's groups. Up to 8 heads: two halves. Beyond:
 // 4, 6, then 8 heads per group, the remainder last, split into (r - 2, 2)
