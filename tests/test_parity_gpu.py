@@ -38,6 +38,15 @@ def test_small_shapes_full_parity(cuda_ok, name):
     full_check(*SMALL[name])
 
 
+@pytest.mark.parametrize("keep", [0.1, 0.2, 0.4])
+def test_ragged_sweep_scaled_down_full_parity(cuda_ok, keep):
+    """The ragged sparsity sweep's structure at a size the oracle checks in full:
+    batch 2, a 1,000 + 700 token prefix (not a multiple of 64), 8,100 video
+    tokens (127 tiles, the last with 36 tokens), keep 0.1 / 0.2 / 0.4 (k = 13,
+    25, 51). Every head, query tile, prefix row and selection."""
+    full_check(2, 2, 1000, 700, 8100, keep, 41)
+
+
 def test_medium_full_parity(cuda_ok):
     c = CONFIGS["medium"]
     full_check(c.batch, c.heads, c.len_text, c.len_audio, c.len_video, c.keep[0], c.seed)
