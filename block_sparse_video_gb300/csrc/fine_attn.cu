@@ -694,22 +694,28 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         return true;
       };
       // The epilogue's gate and coarse inputs were prefetched into L2 when the
-      // item was fetched; all of them are requested together (loading them
-      // inside the store loop serialised one round trip per column).
-      const size_t gate_base = (static_cast<size_t>(it.b) * p.N + it.q_row0) * row_stride +
-                               static_cast<size_t>(it.h) * kHeadDim + r;
-      float gv[kCols];
-      float cz = 0.f;
+      // item was fetched; they are requested together, before the wait for the
+      // item's last PV product. Each lane loads them in the layout of its output
+      // stores: tokens col0 + tr and col0 + tr + 8, channels kc .. kc + 7.
+      const int tr = lane >> 2;
+      const int kc = 32 * q4 + 8 * (lane & 3);
+      uint4 g8[2];     // gate, 8 bf16 per token
+      float4 cz8[2];   // the coarse row's 8 channels
       long long my_row = 0;  // output row of query column col0 + (lane % kCols)
       auto prefetch_gate = [&]() {
-#pragma unroll
-        for (int c = 0; c < kCols; ++c) gv[c] = 0.f;
+        g8[0] = g8[1] = make_uint4(0u, 0u, 0u, 0u);
+        cz8[0] = cz8[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (it.video && p.coarse) {
-          cz = __ldg(p.coarse + ((static_cast<size_t>(it.b) * p.H + it.h) * p.T + it.t) * kHeadDim + r);
+          const float4* crow = reinterpret_cast<const float4*>(
+              p.coarse + ((static_cast<size_t>(it.b) * p.H + it.h) * p.T + it.t) * kHeadDim + kc);
+          cz8[0] = __ldg(crow);
+          cz8[1] = __ldg(crow + 1);
 #pragma unroll
-          for (int c = 0; c < kCols; ++c)
-            if (col0 + c < it.q_valid)
-              gv[c] = __bfloat162float(__ldg(p.gate + gate_base + static_cast<size_t>(col0 + c) * row_stride));
+          for (int j = 0; j < 2; ++j)
+            if (col0 + tr + 8 * j < it.q_valid)
+              g8[j] = __ldg(reinterpret_cast<const uint4*>(
+                  p.gate + (static_cast<size_t>(it.b) * p.N + it.q_row0 + col0 + tr + 8 * j) * row_stride +
+                  static_cast<size_t>(it.h) * kHeadDim + kc));
         }
         const int qc = col0 + (lane % kCols);
         my_row = it.q_row0 + qc;
@@ -780,19 +786,48 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarOEmpty + ob));  // accumulator ob may be reused
+        // Each warp stages O / l (fp32) in its own 2 KB of the P^T ring, then
+        // reads it back eight channels a lane, so that the gate loads and the
+        // output stores are 16 bytes a lane: two a lane per item instead of one
+        // 2-byte access per lane and column. The ring is idle here: the item's
+        // last PV product has completed, and the next P^T is written after the
+        // all-softmax barrier at the next item's start. Word (column c, channel
+        // d) sits at 32 c + ((d + 4 (c & 1)) mod 32): both the column-wise writes
+        // and the 16-byte reads are free of bank conflicts.
+        const uint32_t stage = sP + static_cast<uint32_t>(warp - kWarpSoftmax0) * 2048u;
 #pragma unroll
         for (int c = 0; c < kCols; ++c) {
+          const float4 x = reinterpret_cast<const float4*>(red)[wg * kCols + c];
+          const float lsum = (x.x + x.y) + (x.z + x.w);
+          const uint32_t w = 32u * c + ((static_cast<uint32_t>(lane) + 4u * (c & 1)) & 31u);
+          st_shared_f32(stage + 4u * w, __fdividef(__uint_as_float(o[c]), lsum));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int c = tr + 8 * j;
           const int qc = col0 + c;
           const long long row = __shfl_sync(0xffffffffu, my_row, c);
+          const uint32_t w0 = (8u * static_cast<uint32_t>(lane & 3) + 4u * (c & 1)) & 31u;
+          const float4 v0 = ld_shared_f4(stage + 4u * (32u * c + w0));
+          const float4 v1 = ld_shared_f4(stage + 4u * (32u * c + ((w0 + 4u) & 31u)));
           if (qc < it.q_valid) {
-            const float4 x = reinterpret_cast<const float4*>(red)[wg * kCols + c];
-            const float lsum = (x.x + x.y) + (x.z + x.w);
-            float val = __fdividef(__uint_as_float(o[c]), lsum);
-            if (it.video && p.coarse) val += __fdividef(cz, 1.0f + __expf(-gv[c]));
+            float val[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            if (it.video && p.coarse) {
+              const float cz[8] = {cz8[0].x, cz8[0].y, cz8[0].z, cz8[0].w, cz8[1].x, cz8[1].y, cz8[1].z, cz8[1].w};
+              const uint32_t gw[4] = {g8[j].x, g8[j].y, g8[j].z, g8[j].w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float gv = __uint_as_float((e & 1) ? (gw[e / 2] & 0xffff0000u) : (gw[e / 2] << 16));
+                val[e] += __fdividef(cz[e], 1.0f + __expf(-gv));
+              }
+            }
             if (row >= 0 && row < p.out_rows) {
-              p.out[(static_cast<size_t>(it.b) * p.out_rows + row) * p.out_row_stride +
-                    static_cast<size_t>(it.h) * kHeadDim + r] = __float2bfloat16_rn(val);
-            } else if (r == 0) {  // a map entry outside the output: skipped and reported (token + 1)
+              *reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(it.b) * p.out_rows + row) * p.out_row_stride +
+                                        static_cast<size_t>(it.h) * kHeadDim + kc) =
+                  make_uint4(pack_bf16x2(val[0], val[1]), pack_bf16x2(val[2], val[3]),
+                             pack_bf16x2(val[4], val[5]), pack_bf16x2(val[6], val[7]));
+            } else if (q4 == 0 && (lane & 3) == 0) {  // a map entry outside the output: skipped and reported (token + 1)
               atomicCAS(err + 3, 0u, static_cast<unsigned int>(it.q_row0 + qc) + 1u);
             }
           }
