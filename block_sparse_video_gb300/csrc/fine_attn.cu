@@ -591,8 +591,9 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
           slow = named_bar_or(bar_id, 128, failed || mxall > kRescaleThreshold);
         }
         if (slow) {
-          if (named_bar_or(bar_id, 128, failed)) { failed = true; return; }
-          // slow path: exact block maximum per query column across the 128 key lanes
+          // slow path: exact block maximum per query column across the 128 key lanes.
+          // A failed warp runs it on zeros (its outputs are void) and so meets
+          // the same named barriers as the others; the item's end reports it.
           float u[kCols];
 #pragma unroll
           for (int c = 0; c < kCols; ++c) u[c] = s[c] * sl2;
@@ -612,9 +613,11 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             l2[j] = make_float2(l2[j].x * alpha[2 * j], l2[j].y * alpha[2 * j + 1]);
             nm2[j] = make_float2(n0, n1);
           }
-          // every warp has read the block maxima before red is written again
-          named_bar_sync(bar_id, 128);
-          if (i > 0) {
+          // every warp has read the block maxima before red is written again: in
+          // exact mode by the next slow block; in fast mode only the item's end
+          // writes red, after the all-softmax barrier there
+          if (kExact) named_bar_sync(bar_id, 128);
+          if (i > 0 && !failed) {
             // O^T must hold every PV product issued so far: wait for PV of block
             // g-1 on its P-buffer barrier (PV of block g-1-kNumP is already known
             // to be complete, so this parity wait cannot alias an older phase;
@@ -757,10 +760,13 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
           overflow = overflow || (col0 + 2 * j < it.q_valid && !(l2[j].x < kFastLimitSum)) ||
                      (col0 + 2 * j + 1 < it.q_valid && !(l2[j].y < kFastLimitSum));
       }
-      if (named_bar_or(kBarSoftmaxAll, 32 * kSoftmaxWarps, failed)) break;
-      if (!kExact && named_bar_or(kBarSoftmaxAll, 32 * kSoftmaxWarps, overflow) && tid == 32 * kWarpSoftmax0) {
-        const int pos = atomicAdd(p.redo_count, 1);  // at most once per item: pos < n_items
-        p.redo_list[pos] = item;
+      // one barrier in the common case; a second tells a failure from an overflow
+      if (named_bar_or(kBarSoftmaxAll, 32 * kSoftmaxWarps, failed || overflow)) {
+        if (named_bar_or(kBarSoftmaxAll, 32 * kSoftmaxWarps, failed)) break;
+        if (!kExact && tid == 32 * kWarpSoftmax0) {  // some column overflowed
+          const int pos = atomicAdd(p.redo_count, 1);  // at most once per item: pos < n_items
+          p.redo_list[pos] = item;
+        }
       }
       // ---- epilogue: out = O / l (+ sigmoid(gate) * coarse on video rows, unless
       // there is no coarse term: SubBlock routing)
@@ -786,8 +792,8 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarOEmpty + ob));  // accumulator ob may be reused
-        // Each warp stages O / l (fp32) in its own 2 KB of the P^T ring, then
-        // reads it back eight channels a lane, so that the gate loads and the
+        // Each warp stages O (fp32) in its own 2 KB of the P^T ring, then reads
+        // it back eight channels a lane, so that the gate loads and the
         // output stores are 16 bytes a lane: two a lane per item instead of one
         // 2-byte access per lane and column. The ring is idle here: the item's
         // last PV product has completed, and the next P^T is written after the
@@ -797,10 +803,8 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         const uint32_t stage = sP + static_cast<uint32_t>(warp - kWarpSoftmax0) * 2048u;
 #pragma unroll
         for (int c = 0; c < kCols; ++c) {
-          const float4 x = reinterpret_cast<const float4*>(red)[wg * kCols + c];
-          const float lsum = (x.x + x.y) + (x.z + x.w);
           const uint32_t w = 32u * c + ((static_cast<uint32_t>(lane) + 4u * (c & 1)) & 31u);
-          st_shared_f32(stage + 4u * w, __fdividef(__uint_as_float(o[c]), lsum));
+          st_shared_f32(stage + 4u * w, __uint_as_float(o[c]));
         }
         __syncwarp();
 #pragma unroll
@@ -812,7 +816,11 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
           const float4 v0 = ld_shared_f4(stage + 4u * (32u * c + w0));
           const float4 v1 = ld_shared_f4(stage + 4u * (32u * c + ((w0 + 4u) & 31u)));
           if (qc < it.q_valid) {
+            const float4 x = reinterpret_cast<const float4*>(red)[wg * kCols + c];
+            const float lsum = (x.x + x.y) + (x.z + x.w);
             float val[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) val[e] = __fdividef(val[e], lsum);
             if (it.video && p.coarse) {
               const float cz[8] = {cz8[0].x, cz8[0].y, cz8[0].z, cz8[0].w, cz8[1].x, cz8[1].y, cz8[1].z, cz8[1].w};
               const uint32_t gw[4] = {g8[j].x, g8[j].y, g8[j].z, g8[j].w};
