@@ -533,7 +533,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       failed = failed || !ok;
       // all softmax warps read the same item sequence; agree on stopping
       if (named_bar_or(kBarSoftmaxAll, 32 * kSoftmaxWarps, failed || item < 0)) break;
-      const Item it = decode_item(p, G, item);
+      Item it = decode_item(p, G, item);
       const int nblk = (it.n_kv + 1) / 2;
       const uint32_t ob = n % kNumO;
       const bool last_is_ragged =
@@ -748,6 +748,8 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         }
         if (nblk > 1 && !failed) general_block(nblk - 1, gs + nblk - 1);
       }
+      // decoded again: nothing of the item but n_kv is held through the block loops
+      it = decode_item(p, G, item);
       // The fast mode is valid while every P stayed below kFastLimitSum: P >= 0,
       // so one larger P (or an overflow to inf) leaves a partial row sum at or
       // above that bound (a NaN fails the comparison too).
