@@ -519,12 +519,13 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     const float2 sl2v = make_float2(sl2, sl2);
     // Only two key tiles can be ragged: the last prefix tile, and video tile T-1,
     // which (selections being ascending) can only be the item's last key tile.
-    const int prefix_tail = G.TP > 0 ? G.P - (G.TP - 1) * kTile : kTile;
-    const int video_tail = G.Lv - (G.T - 1) * kTile;
+    // Worked out from the geometry where they are needed, so that the block loops
+    // hold no register for them.
+    auto prefix_tail = [&]() { return G.TP > 0 ? G.P - (G.TP - 1) * kTile : kTile; };
+    auto video_tail = [&]() { return G.Lv - (G.T - 1) * kTile; };
     // Blocks that may hold masked key lanes: the one with the ragged last prefix
     // tile, and the last block (an absent second tile, or ragged video tile T-1).
-    const int ragged_prefix_blk = (G.TP > 0 && prefix_tail < kTile) ? (G.TP - 1) / 2 : -1;
-    const size_t row_stride = static_cast<size_t>(p.in_row_stride);
+    const int ragged_prefix_blk = (G.TP > 0 && prefix_tail() < kTile) ? (G.TP - 1) / 2 : -1;
     bool failed = false;
     uint32_t gs = 0;  // blocks consumed so far, over all items
     for (int n = 0;; ++n) {
@@ -535,9 +536,8 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       if (named_bar_or(kBarSoftmaxAll, 32 * kSoftmaxWarps, failed || item < 0)) break;
       Item it = decode_item(p, G, item);
       const int nblk = (it.n_kv + 1) / 2;
-      const uint32_t ob = n % kNumO;
       const bool last_is_ragged =
-          video_tail < kTile && (it.list == nullptr || __ldg(it.list + G.k - 1) == G.T - 1);
+          video_tail() < kTile && (it.list == nullptr || __ldg(it.list + G.k - 1) == G.T - 1);
       // Per column pair: -reference (log2 units) and this lane's partial row sums.
       float2 nm2[kCols / 2], l2[kCols / 2];
 #pragma unroll
@@ -552,8 +552,8 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         const uint32_t ph = (g / kNumS) & 1, pph = (g / kNumP) & 1;
         const int ti = 2 * i + key_slot;
         bool valid = ti < it.n_kv;
-        if (ti == G.TP - 1) valid = key_row < prefix_tail;
-        if (ti == it.n_kv - 1 && last_is_ragged) valid = valid && key_row < video_tail;
+        if (ti == G.TP - 1) valid = key_row < prefix_tail();
+        if (ti == it.n_kv - 1 && last_is_ragged) valid = valid && key_row < video_tail();
 
         failed = warp_any(failed || !mbar_wait(bar(kBarSFull + st), ph, err, 0x800u));
         float s[kCols];
@@ -627,11 +627,12 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             if (!failed) {
               tc_fence_after();
               uint32_t o[kCols];
-              tmem_ld16(tbase + lane_off + kColO + ob * 64 + col0, o);
+              const uint32_t ocol = tbase + lane_off + kColO + static_cast<uint32_t>(n % kNumO) * 64 + col0;
+              tmem_ld16(ocol, o);
               tmem_wait_ld();
 #pragma unroll
               for (int c = 0; c < kCols; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha[c]);
-              tmem_st16(tbase + lane_off + kColO + ob * 64 + col0, o);
+              tmem_st16(ocol, o);
               tmem_wait_st();
               tc_fence_before();
             }
@@ -717,7 +718,8 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
           for (int j = 0; j < 2; ++j)
             if (col0 + tr + 8 * j < it.q_valid)
               g8[j] = __ldg(reinterpret_cast<const uint4*>(
-                  p.gate + (static_cast<size_t>(it.b) * p.N + it.q_row0 + col0 + tr + 8 * j) * row_stride +
+                  p.gate +
+                  (static_cast<size_t>(it.b) * p.N + it.q_row0 + col0 + tr + 8 * j) * static_cast<size_t>(p.in_row_stride) +
                   static_cast<size_t>(it.h) * kHeadDim + kc));
         }
         const int qc = col0 + (lane % kCols);
@@ -734,22 +736,18 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         // fast blocks 1 .. nblk-2, the ragged-prefix block (if any) excepted;
         // in fast mode these general blocks use no named barrier
         uint32_t g = gs + 1;
-        int st = g % kNumS, pt = g % kNumP;
-        uint32_t ph = (g / kNumS) & 1, pph = (g / kNumP) & 1;
-        for (int i = 1; i < nblk - 1 && !failed; ++i) {
+        for (int i = 1; i < nblk - 1 && !failed; ++i, ++g) {
           if (i == ragged_prefix_blk) {
             general_block(i, g);
-          } else if (!fast_block(st, ph, pt, pph)) {
+          } else if (!fast_block(g % kNumS, (g / kNumS) & 1, g % kNumP, (g / kNumP) & 1)) {
             failed = true;
           }
-          ++g;
-          if (++st == kNumS) { st = 0; ph ^= 1u; }
-          if (++pt == kNumP) { pt = 0; pph ^= 1u; }
         }
         if (nblk > 1 && !failed) general_block(nblk - 1, gs + nblk - 1);
       }
       // decoded again: nothing of the item but n_kv is held through the block loops
       it = decode_item(p, G, item);
+      const uint32_t ob = n % kNumO;
       // The fast mode is valid while every P stayed below kFastLimitSum: P >= 0,
       // so one larger P (or an overflow to inf) leaves a partial row sum at or
       // above that bound (a NaN fails the comparison too).
