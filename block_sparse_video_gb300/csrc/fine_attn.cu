@@ -24,16 +24,22 @@
 // query). Each softmax thread owns one key lane for 16 query columns, so
 // masking a ragged or absent key tile is a per-thread select.
 //
-// Online softmax. The fast kernel fixes, per query column, the reference m
-// (log2 units) to the exact maximum of the item's first block and never
-// rescales afterwards; it is valid while every P = 2^(score - m) stays below
-// kFastLimitSum. An item whose row sums end at or above that bound (P >= 0, so
-// one such P suffices) is appended to a redo list, and the exact kernel (the
-// same code, exact mode) recomputes the redo list with per-block rescaling: a
-// block whose scores all stay below m + 8 (P <= 256) needs no cross-lane work;
-// otherwise the exact block maximum is reduced across the 128 lanes, m is
-// raised, and the row sums and O^T are rescaled. Row sums are per-lane
-// partials, reduced once per item.
+// Online softmax. The fast kernel fixes the reference m (log2 units) to 0, so
+// P = 2^score, and never rescales. Softmax does not depend on m. P (bf16) and
+// the row sums and O^T (fp32) keep their relative precision at any scale
+// between the limits, so the fast result is valid while every P stays below
+// kFastLimitSum (2^64) and every row sum stays at or above kFastMinSum (2^-60;
+// below it, P values that still matter could be subnormal). Both are checked
+// on each lane's partial row sums: P >= 0, so one P at or above 2^64 leaves
+// its lane's partial above the bound, and partials at or above 2^-60 make the
+// row sum so too (a lane whose own keys all score far below the rest of the
+// row fails the floor alone and only costs a redo). An item that fails is
+// appended to a redo list. The exact kernel (the same code, exact mode) then
+// recomputes the redo list with per-block rescaling. Its reference starts at
+// the first block's exact maximum. A later block whose scores all stay below
+// m + 8 (P <= 256) needs no cross-lane work; otherwise the exact block maximum
+// is reduced across the 128 lanes, m is raised, and the row sums and O^T are
+// rescaled. Row sums are per-lane partials, reduced once per item.
 //
 // Warp roles (640 threads): warp 0 fetches the items, loads each item's Q tile
 // as soon as it has fetched it (two buffers, alternating by item) and issues
@@ -77,6 +83,7 @@ constexpr int kItemSlots = 8;            // item ring between the fetching warp 
 constexpr int kItemReaders = 3 + kSoftmaxWarps;  // V loader, both MMA issuers, softmax warps
 constexpr float kRescaleThreshold = 8.0f;  // exact mode: rescale when P would exceed 2^8
 constexpr float kFastLimitSum = 18446744073709551616.0f;  // 2^64: fast-mode bound on P (and on each row sum)
+constexpr float kFastMinSum = 8.673617379884035e-19f;       // 2^-60: fast-mode floor on each row sum
 constexpr uint32_t kBarSoftmaxAll = 1 + kSoftmaxWGs;  // named barrier over all softmax warps
 
 constexpr uint32_t kOffQ = 0;
@@ -542,11 +549,11 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       float2 nm2[kCols / 2], l2[kCols / 2];
 #pragma unroll
       for (int j = 0; j < kCols / 2; ++j) {
-        nm2[j] = make_float2(INFINITY, INFINITY);
+        nm2[j] = kExact ? make_float2(INFINITY, INFINITY) : make_float2(0.f, 0.f);
         l2[j] = make_float2(0.f, 0.f);
       }
-      // ---- general block: masking, and (exact mode or first block) the exact
-      // per-column block maximum with rescaling. g: the block's ring counter.
+      // ---- general block: masking, and (exact mode) the exact per-column block
+      // maximum with rescaling. g: the block's ring counter.
       auto general_block = [&](const int i, const uint32_t g) {
         const int st = g % kNumS, pt = g % kNumP;
         const uint32_t ph = (g / kNumS) & 1, pph = (g / kNumP) & 1;
@@ -584,7 +591,7 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
           t[2 * j + 1] = tt.y;
         }
         bool slow = false;
-        if (kExact || i == 0) {
+        if (kExact) {
           const float mxall =
               fmax3(fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmax3(t[6], t[7], t[8])),
                     fmax3(t[9], t[10], t[11]), fmax3(fmax3(t[12], t[13], t[14]), t[15], -INFINITY));
@@ -732,38 +739,39 @@ fine_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         // named barriers (a failed warp skips the work)
         for (int i = 0; i < nblk; ++i) general_block(i, gs + i);
       } else {
-        general_block(0, gs);
-        // fast blocks 1 .. nblk-2, the ragged-prefix block (if any) excepted;
-        // in fast mode these general blocks use no named barrier
-        uint32_t g = gs + 1;
-        for (int i = 1; i < nblk - 1 && !failed; ++i, ++g) {
+        // fast blocks 0 .. nblk-2, the ragged-prefix block (if any) excepted;
+        // in fast mode the general blocks use no named barrier
+        uint32_t g = gs;
+        for (int i = 0; i < nblk - 1 && !failed; ++i, ++g) {
           if (i == ragged_prefix_blk) {
             general_block(i, g);
           } else if (!fast_block(g % kNumS, (g / kNumS) & 1, g % kNumP, (g / kNumP) & 1)) {
             failed = true;
           }
         }
-        if (nblk > 1 && !failed) general_block(nblk - 1, gs + nblk - 1);
+        if (!failed) general_block(nblk - 1, gs + nblk - 1);
       }
       // decoded again: nothing of the item but n_kv is held through the block loops
       it = decode_item(p, G, item);
       const uint32_t ob = n % kNumO;
       // The fast mode is valid while every P stayed below kFastLimitSum: P >= 0,
       // so one larger P (or an overflow to inf) leaves a partial row sum at or
-      // above that bound (a NaN fails the comparison too).
+      // above that bound (a NaN fails the comparison too). Partials at or above
+      // kFastMinSum keep every P that matters out of the subnormal range.
       // Only the item's valid query columns count: the others are never stored
       // (with device lengths their Q rows may be padding with any contents).
       bool overflow = false;
       if (!kExact) {
 #pragma unroll
         for (int j = 0; j < kCols / 2; ++j)
-          overflow = overflow || (col0 + 2 * j < it.q_valid && !(l2[j].x < kFastLimitSum)) ||
-                     (col0 + 2 * j + 1 < it.q_valid && !(l2[j].y < kFastLimitSum));
+          overflow = overflow ||
+                     (col0 + 2 * j < it.q_valid && !(l2[j].x < kFastLimitSum && l2[j].x >= kFastMinSum)) ||
+                     (col0 + 2 * j + 1 < it.q_valid && !(l2[j].y < kFastLimitSum && l2[j].y >= kFastMinSum));
       }
       // one barrier in the common case; a second tells a failure from an overflow
       if (named_bar_or(kBarSoftmaxAll, 32 * kSoftmaxWarps, failed || overflow)) {
         if (named_bar_or(kBarSoftmaxAll, 32 * kSoftmaxWarps, failed)) break;
-        if (!kExact && tid == 32 * kWarpSoftmax0) {  // some column overflowed
+        if (!kExact && tid == 32 * kWarpSoftmax0) {  // some column left the fast bounds
           const int pos = atomicAdd(p.redo_count, 1);  // at most once per item: pos < n_items
           p.redo_list[pos] = item;
         }

@@ -225,3 +225,19 @@ def test_large_score_jump_after_first_block(cuda_ok, level):
     q.fill_(1.0)
     k[:, lt + la + 5 * 64: lt + la + 6 * 64] = level
     check_inputs(q, k, v, g, lt, la, lv, 0.2, f"score jump {level}")
+
+
+def test_uniformly_low_scores_use_the_exact_pass(cuda_ok):
+    """Every score sits between about -130 and -146 in softmax (log2) units. Against the
+    fast pass's fixed reference every P would underflow, so the floor on the row sums
+    must send every item to the exact pass, which rescales to the running maximum.
+    Video tile j's keys are one bf16 step (1/16) above tile j-1's, so the coarse
+    scores are distinct and the selection has no near-tie."""
+    lt, la, lv = 40, 24, 1024
+    q, k, v, g = make_inputs(1, 2, lt, la, lv, 37, device="cuda")
+    q.fill_(-1.0)
+    k.mul_(0.02).add_(8.0)
+    p = lt + la
+    for j in range(lv // 64):
+        k[:, p + 64 * j: p + 64 * (j + 1)] += 0.0625 * j
+    check_inputs(q, k, v, g, lt, la, lv, 0.2, "uniformly low scores")
