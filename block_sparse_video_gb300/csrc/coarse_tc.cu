@@ -125,13 +125,14 @@ __device__ __forceinline__ float f4_at(const float4& v, int e) {
 }
 
 // row(m): lane l's keys 128 m + 4 l .. + 3 as a float4 (-inf past T), from
-// registers or from shared memory.
+// registers or from shared memory. Returns the row's maximum, taken with its
+// moments (NaN when k >= T, where no moments are taken).
 template <int NM, typename Row>
-__device__ __forceinline__ void select_topk(const Row& row, int T, int k, int* h, int32_t* dst, int lane) {
+__device__ __forceinline__ float select_topk(const Row& row, int T, int k, int* h, int32_t* dst, int lane) {
   const unsigned full = 0xffffffffu;
   if (k >= T) {
     for (int j = lane; j < T; j += 32) dst[j] = j;
-    return;
+    return __int_as_float(0x7fffffff);  // no moments taken: NaN
   }
   // Row moments. Slices m holding only keys < T take no per-entry test; the
   // slice with the row's end skips the -inf entries past T. Four partial sums
@@ -242,7 +243,7 @@ __device__ __forceinline__ void select_topk(const Row& row, int T, int k, int* h
       if (s3) dst[pos] = key + 3;
       written += __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
     }
-    return;
+    return vmax;
   }
   // radix select, 8 bits per pass from the top, over the order-preserving
   // integer image of the scores (-0 and +0 alike)
@@ -324,6 +325,7 @@ __device__ __forceinline__ void select_topk(const Row& row, int T, int k, int* h
     written += total;
     eq_seen += eq_total;
   }
+  return vmax;
 }
 
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -507,16 +509,20 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
     if (failed) break;
 
     // ------------------------------------------------------------ phase B: selection, softmax, P
-    auto softmax_row = [&](auto&& rowf, float* row, int r) {
-      float mx = -INFINITY;
+    // mx: the row's maximum as the selection took it (the same fmaxf over the
+    // same entries, so the same value), or NaN to take it here
+    auto softmax_row = [&](auto&& rowf, float* row, int r, float mx) {
+      if (mx != mx) {
+        mx = -INFINITY;
 #pragma unroll
-      for (int m = 0; m < NM; ++m)
-        if (128 * m < T) {
-          const float4 vm = rowf(m);
-          mx = fmaxf(mx, fmaxf(fmaxf(vm.x, vm.y), fmaxf(vm.z, vm.w)));
-        }
+        for (int m = 0; m < NM; ++m)
+          if (128 * m < T) {
+            const float4 vm = rowf(m);
+            mx = fmaxf(mx, fmaxf(fmaxf(vm.x, vm.y), fmaxf(vm.z, vm.w)));
+          }
 #pragma unroll
-      for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
       // p = exp(s - max) = 2^((s - max) log2 e); entries past T give 2^-inf = 0
       const float nmx = -mx * 1.4426950408889634f;
       float l = 0.f;
@@ -570,9 +576,9 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
         }
         __syncwarp();
         auto rowf = [&](int m) { return ld_shared_f4(buf + 16u * static_cast<uint32_t>(32 * m + lane)); };
-        select_topk<NM>(rowf, T, k, hist + warp * kBins,
-                        p.tile_index + (static_cast<size_t>(bh) * T_cap + q0 + r) * k_cap, lane);
-        softmax_row(rowf, row, r);
+        const float mx = select_topk<NM>(rowf, T, k, hist + warp * kBins,
+                                         p.tile_index + (static_cast<size_t>(bh) * T_cap + q0 + r) * k_cap, lane);
+        softmax_row(rowf, row, r, mx);
         int nr = 0;
         if (lane == 0) nr = kWarps + atomicAdd(next_row, 1);
         r = __shfl_sync(0xffffffffu, nr, 0);
@@ -593,9 +599,9 @@ coarse_tc_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_consta
           }
         }
         auto rowf = [&](int m) { return v[m]; };
-        select_topk<NM>(rowf, T, k, hist + warp * kBins,
-                        p.tile_index + (static_cast<size_t>(bh) * T_cap + q0 + r) * k_cap, lane);
-        softmax_row(rowf, row, r);
+        const float mx = select_topk<NM>(rowf, T, k, hist + warp * kBins,
+                                         p.tile_index + (static_cast<size_t>(bh) * T_cap + q0 + r) * k_cap, lane);
+        softmax_row(rowf, row, r, mx);
         int nr = 0;
         if (lane == 0) nr = kWarps + atomicAdd(next_row, 1);
         r = __shfl_sync(0xffffffffu, nr, 0);
